@@ -1,0 +1,194 @@
+/*
+ * gdn_paged.h -- C ABI of paged Gated Delta-Rule (GDN) prefill and decode on
+ * GB300 (sm_103a).
+ *
+ * Source: "flashinfer.gdn_paged" (docs.flashinfer.ai/api/gdn_paged.html) --
+ * the intro, §Page table, the prefill bullets, the decode paragraph, the pool /
+ * padding paragraph and "Slot arguments of chunk_gated_delta_rule".  The pages
+ * name the method but print no formula for it; the library computes the
+ * standard gated delta rule on a V x K state per (sequence, head):
+ *     S_t = exp(g_t) S_{t-1} + beta_t (v_t - exp(g_t) S_{t-1} k_t) k_t^T
+ *     o_t = scale * S_t q_t
+ *
+ * Conventions shared by every call
+ *   - All array pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates no memory and keeps no pointer after a call returns.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and never synchronises the host.
+ *   - bf16 tensors are passed as raw 16-bit patterns (gdn_bf16).
+ *   - Token layout is packed varlen: q, k are [T, H, K], v and o are [T, H, V],
+ *     g and beta are [T, H] (fp32, g is the log-space gate applied as exp(g)).
+ *     Decode uses [B, H, .] (the same memory as [B, 1, H, .]).
+ *   - The state pool is fp32 [rows, H, V, K]; one row is a dense [H, V, K]
+ *     block at row * pool_row_stride elements.  Page j of a sequence holds the
+ *     state after the last token of that page.
+ *   - Page tables are CSR: sequence b owns page_indices[page_indptr[b] ..
+ *     page_indptr[b+1]) (any ids, any order) and has
+ *     (num_pages_b - 1) * page_size + last_page_len[b] tokens AFTER the call;
+ *     its new tokens are the last ones, the ones before are its prefix.
+ *   - K and V must be 128.  q, k, v, o, g, beta and every pool must be 16-byte
+ *     aligned.
+ *   - scale <= 0 selects the default 1/sqrt(K).
+ *   - Return value: GDN_OK, or a negative status (no exception crosses the
+ *     ABI).  Host-side checks cover scalars, null pointers and alignment only;
+ *     nothing is read back from the device.
+ *   - err_word (nullable, device int32 the caller zeroes): when given, the
+ *     kernels also check device-side data (page ids against [0, num_pages),
+ *     page-table consistency) and record the first violation as
+ *     (kind << 24) | sequence, kind one of GDN_DEVERR_*; a sequence that fails
+ *     a check is skipped.  Without it the data are trusted.
+ *   - Preconditions (unchecked): page ids are real ids (-1 is not a padding
+ *     value); rows written by one sequence are not read or written by another
+ *     sequence of the same call; a decoded sequence holds at least one token
+ *     before the decoded one; prefill input values stay within the fp16 range
+ *     (|x| < 65504), since the tensor-core products run on fp16 operands.
+ */
+#ifndef GDN_PAGED_H
+#define GDN_PAGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t gdn_bf16; /* raw bfloat16 bit pattern */
+
+#define GDN_OK 0
+#define GDN_ERR_INVALID_ARGUMENT (-1) /* null pointer, bad scalar, misalignment */
+#define GDN_ERR_UNSUPPORTED (-2)      /* K or V other than 128, no sm_103a device */
+#define GDN_ERR_CUDA (-3)             /* a CUDA launch or driver call failed */
+
+#define GDN_DEVERR_PAGE_ID 1       /* a page id outside [0, num_pages) */
+#define GDN_DEVERR_PAGE_TABLE 2    /* no page, last_page_len outside 1..page_size, more new tokens than tokens, or tokens past total_tokens */
+#define GDN_DEVERR_NO_PREV_TOKEN 3 /* decode: the decoded token is the sequence's first */
+#define GDN_DEVERR_TIMEOUT 15      /* an internal wait ran past its iteration limit */
+
+/* Per-sequence pool rows of a paged prefill batch, each int32 [num_seqs] on
+ * the device ("GDNPagedPrefillSlots"). */
+typedef struct {
+    int32_t *state_indices;        /* row of the page holding the last prefix token, -1 if no prefix */
+    int32_t *output_state_indices; /* last page, -1 for a zero-length sequence */
+    int32_t *checkpoint_cu_starts; /* index into page_indices of the first page ending after the prefix */
+    int32_t *prefix_lens;          /* tokens before the new ones */
+} gdn_prefill_slots;
+
+/* Per-sequence pool rows of a paged decode batch, each int32 [B] on the device
+ * ("GDNPagedDecodeSlots"). */
+typedef struct {
+    int32_t *initial_state_indices; /* previous page when last_page_len == 1, else the last page */
+    int32_t *output_state_indices;  /* last page */
+} gdn_decode_slots;
+
+/* gdn_paged_prefill_slots -- "gdn_paged_prefill_slots(cu_seqlens, ...)" and
+ * §Page table: derive the rows the paged prefill uses, in one launch with no
+ * host synchronisation.  For sequence b with n_b pages, L_b new tokens and
+ * P_b = (n_b - 1) * page_size + last_page_len[b] - L_b prefix tokens:
+ *   state_indices[b]        = P_b > 0 ? page_indices[page_indptr[b] + (P_b - 1) / page_size] : -1
+ *   output_state_indices[b] = L_b > 0 ? page_indices[page_indptr[b+1] - 1] : -1
+ *   checkpoint_cu_starts[b] = page_indptr[b] + P_b / page_size
+ *   prefix_lens[b]          = P_b
+ * A sequence with no page or with P_b < 0 gets -1 rows, prefix 0.
+ * Inputs: cu_seqlens [num_seqs+1], page_indptr [num_seqs+1], page_indices,
+ * last_page_len [num_seqs]; outputs four int32 [num_seqs] arrays.
+ * page_size must be a positive multiple of 64. */
+int gdn_paged_prefill_slots(const int32_t *cu_seqlens, const int32_t *page_indptr,
+                            const int32_t *page_indices, const int32_t *last_page_len,
+                            int32_t num_seqs, int32_t page_size, int32_t *state_indices,
+                            int32_t *output_state_indices, int32_t *checkpoint_cu_starts,
+                            int32_t *prefix_lens, void *stream);
+
+/* gdn_paged_decode_slots -- "gdn_paged_decode_slots(page_indices, ...)" and the
+ * decode paragraph: initial_state_indices[b] is the previous page when the
+ * decoded token opens a page (last_page_len[b] == 1), otherwise the last page;
+ * output_state_indices[b] is the last page.  A one-page sequence with
+ * last_page_len 1 (outside the contract) reads -1, the zero state.
+ * Inputs: page_indptr [batch+1], page_indices, last_page_len [batch]; outputs
+ * two int32 [batch] arrays. */
+int gdn_paged_decode_slots(const int32_t *page_indptr, const int32_t *page_indices,
+                           const int32_t *last_page_len, int32_t batch,
+                           int32_t *initial_state_indices, int32_t *output_state_indices,
+                           void *stream);
+
+/* gdn_chunk_gated_delta_rule -- "Slot arguments of chunk_gated_delta_rule":
+ * chunked prefill on explicit rows.  For every sequence b (new tokens
+ * cu_seqlens[b] .. cu_seqlens[b+1]-1) and head:
+ *   - start from row state_indices[b] of initial_state, or from the zero state
+ *     when state_indices is NULL or the row is -1 (the pool is not read);
+ *   - after new token n with (prefix_lens[b] + n) % N == 0 (N =
+ *     checkpoint_every_n_tokens) store the state to row
+ *     checkpoint_state_indices[checkpoint_cu_starts[b] + j] of
+ *     state_checkpoints, j counting this call's checkpoints of b from 0; a row
+ *     of -1 skips it.  Sequence b has (P_b + L_b) / N - P_b / N checkpoints;
+ *   - store the final state to row output_state_indices[b] of output_state
+ *     unless that is NULL or -1;
+ *   - a zero-length sequence reads and writes nothing.
+ * Tokens are processed in 64-token chunks aligned to absolute positions
+ * (prefix_lens, 0 when NULL); a prefix that is not a multiple of 64 pads the
+ * first chunk on the left.  The checkpoint arrays (state_checkpoints,
+ * checkpoint_state_indices, checkpoint_cu_starts) are all given or all NULL;
+ * when given, prefix_lens is required and N must be a positive multiple of 64.
+ * initial_state, output_state and state_checkpoints may be the same pool;
+ * pool_row_stride (elements) is >= H*V*K and a multiple of 4.
+ * total_tokens is T, the first dimension of q/k/v/o. */
+int gdn_chunk_gated_delta_rule(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                               const float *g, const float *beta, gdn_bf16 *o,
+                               const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                               int32_t H, int32_t K, int32_t V, float scale,
+                               const float *initial_state, const int32_t *state_indices,
+                               float *output_state, const int32_t *output_state_indices,
+                               float *state_checkpoints, const int32_t *checkpoint_state_indices,
+                               const int32_t *checkpoint_cu_starts, const int32_t *prefix_lens,
+                               int32_t checkpoint_every_n_tokens, int64_t pool_row_stride,
+                               int32_t *err_word, void *stream);
+
+/* gdn_chunk_gated_delta_rule_paged -- "chunk_gated_delta_rule_paged(q, k, v,
+ * ...)": chunked prefill over a paged pool state_pool[num_pages, H, V, K].  It
+ * reads the page holding the last prefix token (zero state for an empty
+ * prefix), stores the state at every page boundary the new tokens cross to the
+ * page ending there and the final state to the last page, and never writes a
+ * page that ends at or before the prefix.  It is the slot-argument call above
+ * with state_pool as all three pools, page_indices as checkpoint rows and
+ * N = page_size.  slots (nullable): rows from gdn_paged_prefill_slots, e.g.
+ * computed once per step and shared by all layers; when NULL the kernel
+ * derives them itself from the page table (no extra launch, no workspace).
+ * page_size must be a positive multiple of 64. */
+int gdn_chunk_gated_delta_rule_paged(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                                     const float *g, const float *beta, gdn_bf16 *o,
+                                     const int32_t *cu_seqlens, int32_t num_seqs,
+                                     int32_t total_tokens, int32_t H, int32_t K, int32_t V,
+                                     float scale, float *state_pool, int32_t num_pages,
+                                     const int32_t *page_indices, const int32_t *page_indptr,
+                                     int32_t page_size, const int32_t *last_page_len,
+                                     const gdn_prefill_slots *slots, int32_t *err_word,
+                                     void *stream);
+
+/* gdn_gated_delta_rule_decode_paged -- "gated_delta_rule_decode_paged(q, k, v,
+ * ...)": one token per sequence.  When the token opens a new page
+ * (last_page_len[b] == 1) the state is read from the previous page and written
+ * to the new one; otherwise the last page is updated in place.  q, k are
+ * [batch, H, K], v and o [batch, H, V], g and beta [batch, H].  slots
+ * (nullable): rows from gdn_paged_decode_slots (or any explicit read / write
+ * rows, -1 read = zero state, -1 write = skip); when NULL the kernel derives
+ * them from the page table. */
+int gdn_gated_delta_rule_decode_paged(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                                      const float *g, const float *beta, gdn_bf16 *o,
+                                      int32_t batch, int32_t H, int32_t K, int32_t V, float scale,
+                                      float *state_pool, int32_t num_pages,
+                                      const int32_t *page_indices, const int32_t *page_indptr,
+                                      const int32_t *last_page_len, const gdn_decode_slots *slots,
+                                      int32_t *err_word, void *stream);
+
+/* Bytes of device workspace a prefill call needs: always 0 (the calls take no
+ * workspace; kept so callers can size one uniformly). */
+size_t gdn_prefill_workspace_bytes(int32_t num_seqs, int32_t total_tokens, int32_t H);
+
+/* Static text for a status code. */
+const char *gdn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_PAGED_H */

@@ -1,0 +1,108 @@
+"""The C-ABI library loads, exports every declared symbol, and rejects bad
+arguments on the host before touching the GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_deltanet_paged_gb300 as gdn
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "gdn_paged.h")
+
+
+def declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char \*)\s*(gdn_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared()
+    for n in ("gdn_paged_prefill_slots", "gdn_paged_decode_slots", "gdn_chunk_gated_delta_rule",
+              "gdn_chunk_gated_delta_rule_paged", "gdn_gated_delta_rule_decode_paged",
+              "gdn_prefill_workspace_bytes", "gdn_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(gdn.LIB_PATH if gdn.library() else None)
+    for n in declared():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_workspace():
+    lib = gdn.library()
+    for code in (0, -1, -2, -3):
+        assert lib.gdn_status_string(code) and lib.gdn_status_string(code) != b"unknown status"
+    assert lib.gdn_status_string(-99) == b"unknown status"
+    assert lib.gdn_prefill_workspace_bytes(64, 100000, 32) == 0
+
+
+FAKE = 0x10000  # a 16-byte aligned non-null address; never dereferenced by the host checks below
+
+
+def test_slot_calls_reject_bad_arguments():
+    lib = gdn.library()
+    p = FAKE
+    assert lib.gdn_paged_prefill_slots(p, p, p, p, 4, 100, p, p, p, p, None) == -1  # page_size % 64
+    assert lib.gdn_paged_prefill_slots(p, p, p, p, 4, 0, p, p, p, p, None) == -1
+    assert lib.gdn_paged_prefill_slots(None, p, p, p, 4, 64, p, p, p, p, None) == -1
+    assert lib.gdn_paged_prefill_slots(p, p, p, p, -1, 64, p, p, p, p, None) == -1
+    assert lib.gdn_paged_prefill_slots(p, p, p, p, 0, 64, p, p, p, p, None) == 0  # empty batch: no launch
+    assert lib.gdn_paged_decode_slots(p, None, p, 3, p, p, None) == -1
+    assert lib.gdn_paged_decode_slots(p, p, p, 0, p, p, None) == 0
+
+
+def _chunk(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, o=FAKE, cu=FAKE, S=2, T=10, H=2, K=128, V=128, scale=0.0,
+             init=None, si=None, out=None, osi=None, ck=None, cki=None, ccs=None, pl=None, N=0, stride=0,
+             err=None)
+    a.update(kw)
+    return lib.gdn_chunk_gated_delta_rule(a["q"], a["k"], a["v"], a["g"], a["beta"], a["o"], a["cu"], a["S"],
+                                          a["T"], a["H"], a["K"], a["V"], a["scale"], a["init"], a["si"],
+                                          a["out"], a["osi"], a["ck"], a["cki"], a["ccs"], a["pl"], a["N"],
+                                          a["stride"], a["err"], None)
+
+
+def test_prefill_rejects_bad_arguments():
+    lib = gdn.library()
+    assert _chunk(lib, K=64) == -2
+    assert _chunk(lib, V=256) == -2
+    assert _chunk(lib, H=0) == -1
+    assert _chunk(lib, q=None) == -1
+    assert _chunk(lib, q=FAKE + 8) == -1                      # q not 16-byte aligned
+    assert _chunk(lib, init=FAKE, stride=2 * 128 * 128) == -1  # pool without read rows
+    assert _chunk(lib, ck=FAKE, cki=FAKE, stride=2 * 128 * 128) == -1  # checkpoint arrays partly given
+    ck = dict(ck=FAKE, cki=FAKE, ccs=FAKE, stride=2 * 128 * 128)
+    assert _chunk(lib, **ck, pl=FAKE, N=0) == -1               # N must be > 0
+    assert _chunk(lib, **ck, pl=FAKE, N=96) == -1              # N must be a multiple of 64
+    assert _chunk(lib, **ck, N=128) == -1                      # prefix_lens required
+    assert _chunk(lib, **dict(ck, stride=100), pl=FAKE, N=128) == -1  # stride < H*V*K
+    assert _chunk(lib, S=0) == 0                               # nothing to do
+    assert _chunk(lib, T=0) == 0
+
+
+def test_paged_calls_reject_bad_arguments():
+    lib = gdn.library()
+    p = FAKE
+    f = lib.gdn_chunk_gated_delta_rule_paged
+    assert f(p, p, p, p, p, p, p, 1, 10, 2, 128, 128, 0.0, p, 8, p, p, 96, p, None, None, None) == -1
+    assert f(p, p, p, p, p, p, p, 1, 10, 2, 128, 128, 0.0, None, 8, p, p, 64, p, None, None, None) == -1
+    assert f(p, p, p, p, p, p, p, 1, 10, 2, 128, 64, 0.0, p, 8, p, p, 64, p, None, None, None) == -2
+    assert f(p, p, p, p, p, p, p, 1, 10, 2, 128, 128, 0.0, p, 0, p, p, 64, p, None, None, None) == -1
+    d = lib.gdn_gated_delta_rule_decode_paged
+    assert d(p, p, p, p, p, p, 4, 2, 128, 128, 0.0, p, 8, None, p, p, None, None, None) == -1
+    assert d(p, p, p, p, p, p, 4, 2, 96, 128, 0.0, p, 8, p, p, p, None, None, None) == -2
+    assert d(p, p, p, p, p, p, 0, 2, 128, 128, 0.0, p, 8, p, p, p, None, None, None) == 0
+
+
+def test_binding_has_no_fallback_without_gpu():
+    """The Python entry points go through the CUDA library only; on a
+    machine without a GPU they raise instead of computing anything."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("GPU present")
+    t = torch.zeros(4, dtype=torch.int32)
+    with pytest.raises((ValueError, RuntimeError)):
+        gdn.gdn_paged_decode_slots(t, t, t)

@@ -1,0 +1,170 @@
+"""GPU parity at the full workload sizes: the 256-sequence decode batch, the
+64-sequence mixed prefill through the general slot API, and the 4 x 65,536
+token long-context prefill followed by 128 decode steps.  The oracle runs on
+every chain where that is cheap (decode, mixed prefill) and on sampled
+(sequence, head) chains of the long-context run; properties that hold at any
+size (finite outputs, untouched rows bit-exact) are checked everywhere."""
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_paged_gb300 as gdn
+import oracle
+from gated_deltanet_paged_gb300 import workloads
+from conftest import bf16_bits, f32, i32
+from gpu_util import SCALE, Errors, bits_equal, check_o, check_pool, rel_fro_rows, S_TOL, O_TOL
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def test_decode_batch_full_size():
+    w = workloads.decode_batch("cuda")
+    call = w.calls[0]
+    pool = w.pool
+    ip, pi, lpl = (i32(t) for t in (call.page_indptr, call.page_indices, call.last_page_len))
+    s = oracle.decode_slots(ip, pi, lpl, call.page_size)
+    slots = gdn.gdn_paged_decode_slots(call.page_indptr, call.page_indices, call.last_page_len)
+    for k in s:
+        assert (slots[k].cpu().numpy() == s[k]).all()
+    rows = sorted(set(s["initial_state_indices"].tolist()) | set(s["output_state_indices"].tolist()))
+    rows = [r for r in rows if r >= 0]
+    remap = {r: i for i, r in enumerate(rows)}
+    local = pool[torch.tensor(rows, device="cuda")].cpu().numpy()
+    before = pool.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = gdn.gdn_gated_delta_rule_decode_paged(call.q, call.k, call.v, call.g, call.beta, pool, call.page_indices,
+                                              call.page_indptr, call.last_page_len, scale=SCALE, err_word=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    o_ref, written = oracle.gated_delta_rule_decode(
+        bf16_bits(call.q), bf16_bits(call.k), bf16_bits(call.v), f32(call.g), f32(call.beta), local,
+        [remap.get(r, -1) for r in s["initial_state_indices"].tolist()],
+        [remap[r] for r in s["output_state_indices"].tolist()], SCALE)
+    errs = Errors()
+    check_o(o, o_ref, errs)
+    wrows = [rows[i] for i in np.flatnonzero(written)]
+    got = pool[torch.tensor(wrows, device="cuda")].cpu().numpy()
+    e = rel_fro_rows(got, local[np.flatnonzero(written)])
+    errs.state = float(e.max())
+    assert e.max() <= S_TOL
+    keep = torch.ones(pool.shape[0], dtype=torch.bool, device="cuda")
+    keep[torch.tensor(wrows, device="cuda")] = False
+    assert bits_equal(pool[keep], before[keep])
+    print("decode batch B=256 H=32: %r" % errs)
+
+
+def _checkpoint_layout(prefix, lens, N):
+    """Checkpoint count per sequence, (prefix + len) // N - prefix // N
+    ("Slot arguments"), laid out densely: (cu_starts, total)."""
+    counts = (prefix + lens) // N - prefix // N
+    starts = np.concatenate([[0], np.cumsum(counts)[:-1]]).astype(np.int32)
+    return starts, int(counts.sum())
+
+
+def test_mixed_prefill_general_api_full_size():
+    w = workloads.mixed_prefill("cpu")
+    call = w.calls[0]
+    N = w.checkpoint_every
+    P, L = w.prefix_lens.numpy(), w.seq_lens.numpy()
+    ccs, total = _checkpoint_layout(P, L, N)
+    dev = lambda t: torch.as_tensor(t).cuda()
+    cu, ip, pi, lpl = dev(call.cu_seqlens), dev(call.page_indptr), dev(call.page_indices), dev(call.last_page_len)
+    slots = gdn.gdn_paged_prefill_slots(cu, ip, pi, lpl, call.page_size)
+    ref = oracle.prefill_slots(i32(call.cu_seqlens), i32(call.page_indptr), i32(call.page_indices),
+                               i32(call.last_page_len), call.page_size)
+    for k in ref:
+        assert (slots[k].cpu().numpy() == ref[k]).all(), k
+    assert (ref["prefix_lens"] == P).all()
+    cki = np.arange(total, dtype=np.int32)
+    ck = workloads.sentinel_pool(total, w.H, "cpu")
+    pool_g, ck_g = w.pool.cuda(), ck.cuda()
+    pb, cb = pool_g.clone(), ck_g.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = gdn.gdn_chunk_gated_delta_rule(
+        dev(call.q), dev(call.k), dev(call.v), dev(call.g), dev(call.beta), cu, scale=SCALE, initial_state=pool_g,
+        state_indices=slots["state_indices"], output_state=pool_g,
+        output_state_indices=slots["output_state_indices"], state_checkpoints=ck_g,
+        checkpoint_state_indices=dev(cki), checkpoint_cu_starts=dev(ccs), prefix_lens=slots["prefix_lens"],
+        checkpoint_every_n_tokens=N, err_word=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    pool_o, ck_o = w.pool.numpy().copy(), ck.numpy().copy()
+    o_ref, w_out, w_ck = oracle.chunk_gated_delta_rule(
+        bf16_bits(call.q), bf16_bits(call.k), bf16_bits(call.v), f32(call.g), f32(call.beta), i32(call.cu_seqlens),
+        SCALE, initial_state=pool_o, state_indices=ref["state_indices"], output_state=pool_o,
+        output_state_indices=ref["output_state_indices"], state_checkpoints=ck_o, checkpoint_state_indices=cki,
+        checkpoint_cu_starts=ccs, prefix_lens=P, checkpoint_every_n_tokens=N)
+    errs = Errors()
+    check_o(o, o_ref, errs)
+    check_pool(pool_g, pb, pool_o, w_out, errs, "pool")
+    check_pool(ck_g, cb, ck_o, w_ck, errs, "checkpoints")
+    assert w_ck.all()
+    print("mixed prefill S=64 H=16 (T=%d, %d checkpoints): %r" % (call.q.shape[0], total, errs))
+
+
+SAMPLED_CHAINS = [(0, 0), (1, 13), (2, 22), (3, 31)]
+
+
+def test_long_context_prefill_then_decode():
+    w = workloads.long_context("cuda")
+    pre, decs = w.calls[0], w.calls[1:]
+    pool = w.pool
+    before = pool.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = gdn.gdn_chunk_gated_delta_rule_paged(pre.q, pre.k, pre.v, pre.g, pre.beta, pre.cu_seqlens, pool,
+                                             pre.page_indices, pre.page_indptr, pre.page_size, pre.last_page_len,
+                                             scale=SCALE, err_word=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.isfinite(o.float()).all()
+    owned = pre.page_indices.long()
+    assert torch.isfinite(pool[owned]).all()
+    free = torch.ones(pool.shape[0], dtype=torch.bool, device="cuda")
+    free[owned] = False
+    assert bits_equal(pool[free], before[free])
+
+    cu = pre.cu_seqlens.cpu().numpy()
+    ip = pre.page_indptr.cpu().numpy()
+    pages = pre.page_indices.cpu().numpy()
+    errs = Errors()
+    locals_ = {}
+    for b, h in SAMPLED_CHAINS:
+        t0, t1 = int(cu[b]), int(cu[b + 1])
+        ids = pages[ip[b]:ip[b + 1]]
+        n = len(ids)
+        local = workloads.sentinel_pool(n, 1, "cpu").numpy().copy()
+        sl = slice(t0, t1)
+        o_ref, written = oracle.chunk_gated_delta_rule_paged(
+            bf16_bits(pre.q[sl, h:h + 1]), bf16_bits(pre.k[sl, h:h + 1]), bf16_bits(pre.v[sl, h:h + 1]),
+            f32(pre.g[sl, h:h + 1]), f32(pre.beta[sl, h:h + 1]), [0, t1 - t0], local, np.arange(n, dtype=np.int32),
+            [0, n], pre.page_size, i32(pre.last_page_len[b:b + 1]), SCALE)
+        assert written.all()
+        check_o(o[sl, h:h + 1], o_ref, errs)
+        got = pool[torch.as_tensor(ids, device="cuda").long(), h:h + 1].cpu().numpy()
+        e = rel_fro_rows(got, local)
+        errs.state = max(errs.state, float(e.max()))
+        assert e.max() <= S_TOL, "chain %s: state rel-fro %.4g" % ((b, h), e.max())
+        locals_[(b, h)] = (local, ids)
+
+    # 128 decode steps on the same pool (in place; last_page_len 1025 .. 1152)
+    for step, call in enumerate(decs):
+        o_d = gdn.gdn_gated_delta_rule_decode_paged(call.q, call.k, call.v, call.g, call.beta, pool,
+                                                    call.page_indices, call.page_indptr, call.last_page_len,
+                                                    scale=SCALE, err_word=err)
+        for b, h in SAMPLED_CHAINS:
+            local, ids = locals_[(b, h)]
+            n = len(ids)
+            o_ref, _ = oracle.gated_delta_rule_decode(
+                bf16_bits(call.q[b:b + 1, h:h + 1]), bf16_bits(call.k[b:b + 1, h:h + 1]),
+                bf16_bits(call.v[b:b + 1, h:h + 1]), f32(call.g[b:b + 1, h:h + 1]),
+                f32(call.beta[b:b + 1, h:h + 1]), local, [n - 1], [n - 1], SCALE)
+            check_o(o_d[b:b + 1, h:h + 1], o_ref, errs)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    for b, h in SAMPLED_CHAINS:
+        local, ids = locals_[(b, h)]
+        got = pool[int(ids[-1]), h:h + 1].cpu().numpy()[None]
+        e = rel_fro_rows(got, local[-1:])
+        errs.state = max(errs.state, float(e.max()))
+        assert e.max() <= S_TOL
+    print("long context 4 x 65536, H=32, then 128 decode steps: %r" % errs)

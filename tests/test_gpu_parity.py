@@ -1,0 +1,226 @@
+"""GPU parity of the CUDA library against the fp64 oracle on small cases:
+the tiny two-sequence workload, the worked 2500-token example, ragged
+prefixes / lengths around the 64-token chunk, the general slot API with -1
+rows, and device-side validation."""
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_paged_gb300 as gdn
+import oracle
+from gated_deltanet_paged_gb300 import workloads
+from conftest import bf16_bits, f32, i32
+from gpu_util import (SCALE, Errors, bits_equal, check_o, check_pool, decode_paged_both, prefill_paged_both)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("use_slots", [False, True])
+@pytest.mark.parametrize("decay", [1.0, 0.01])
+def test_tiny_workload(decay, use_slots):
+    w = workloads.tiny("cpu", decay)
+    pool_gpu, pool_ora = w.pool.cuda(), w.pool.numpy().copy()
+    errs = Errors()
+    for call in w.calls:
+        if call.kind == "prefill":
+            prefill_paged_both(call, pool_gpu, pool_ora, errs, use_slots)
+        else:
+            decode_paged_both(call, pool_gpu, pool_ora, errs, use_slots)
+    print("tiny decay=%g slots=%s: %r" % (decay, use_slots, errs))
+
+
+@pytest.mark.parametrize("decay", [1.0, 0.01])
+def test_worked_example(decay):
+    """2048 cached tokens in pages [7, 3], 452 new with page 12: the second
+    call reads page 3, writes page 12 and leaves 7 and 3 bit-unchanged."""
+    w = workloads.worked_example("cpu", decay)
+    pool_gpu, pool_ora = w.pool.cuda(), w.pool.numpy().copy()
+    errs = Errors()
+    prefill_paged_both(w.calls[0], pool_gpu, pool_ora, errs)
+    kept = pool_gpu[[7, 3]].clone()
+    _, written = prefill_paged_both(w.calls[1], pool_gpu, pool_ora, errs)
+    assert np.flatnonzero(written).tolist() == [12]
+    assert bits_equal(pool_gpu[[7, 3]], kept)
+    print("worked example decay=%g: %r" % (decay, errs))
+
+
+def _ragged_case(seed, ps, lens, prefixes, H=2, decay=1.0):
+    gen = torch.Generator().manual_seed(seed)
+    ctx = [l + p for l, p in zip(lens, prefixes)]
+    npages = sum(max(1, -(-c // ps)) for c in ctx)
+    ids = torch.randperm(npages + 3, generator=gen)
+    ip, pi, lpl = workloads.page_table(ctx, ids, ps, "cpu")
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    q, k, v, g, b = workloads.draw_tokens(gen, int(sum(lens)), H, "cpu", decay)
+    pool = workloads.sentinel_pool(npages + 3, H, "cpu")
+    s = oracle.prefill_slots(i32(cu), i32(ip), i32(pi), i32(lpl), ps)
+    workloads.fill_rows(pool, [r for r in s["state_indices"].tolist() if r >= 0], gen)
+    return workloads.PrefillCall(q, k, v, g, b, cu, ip, pi, lpl, ps), pool
+
+
+RAGGED = [
+    (64, [1, 5, 63, 64, 65, 127, 128, 200], [0, 0, 0, 0, 0, 0, 0, 0]),
+    (64, [1, 5, 63, 64, 65, 127, 128, 200], [1, 63, 64, 65, 127, 128, 129, 191]),
+    (128, [3, 61, 64, 70, 129, 250, 0, 300], [60, 4, 128, 58, 1, 6, 77, 255]),
+    (192, [500, 1, 191, 192, 193], [191, 383, 1, 0, 64]),
+]
+
+
+@pytest.mark.parametrize("decay", [1.0, 0.01])
+@pytest.mark.parametrize("case", range(len(RAGGED)))
+def test_ragged_prefixes_and_tails(case, decay):
+    ps, lens, prefixes = RAGGED[case]
+    call, pool = _ragged_case(100 + case, ps, lens, prefixes, decay=decay)
+    errs = Errors()
+    prefill_paged_both(call, pool.cuda(), pool.numpy().copy(), errs)
+    print("ragged case %d decay=%g: %r" % (case, decay, errs))
+
+
+def test_split_prompt_matches_single_call_on_gpu():
+    """Chunked prefill can split a prompt at any token: a 173 + 527 split on the
+    GPU equals one 700-token GPU call within the state tolerance."""
+    ps, H, L, split = 128, 2, 700, 173
+    gen = torch.Generator().manual_seed(5)
+    q, k, v, g, b = workloads.draw_tokens(gen, L, H, "cpu", 0.01)
+    ids = torch.tensor([3, 8, 1, 12, 6, 10], dtype=torch.int32)
+    full = workloads.PrefillCall(q, k, v, g, b, torch.tensor([0, L], dtype=torch.int32),
+                                 *workloads.page_table([L], ids, ps, "cpu"), ps)
+    part1 = workloads.PrefillCall(q[:split], k[:split], v[:split], g[:split], b[:split],
+                                  torch.tensor([0, split], dtype=torch.int32),
+                                  *workloads.page_table([split], ids, ps, "cpu"), ps)
+    part2 = workloads.PrefillCall(q[split:], k[split:], v[split:], g[split:], b[split:],
+                                  torch.tensor([0, L - split], dtype=torch.int32),
+                                  *workloads.page_table([L], ids, ps, "cpu"), ps)
+    base = workloads.sentinel_pool(16, H, "cpu")
+    errs = Errors()
+    p1, r1 = base.cuda(), base.numpy().copy()
+    o_full, _ = prefill_paged_both(full, p1, r1, errs)
+    p2, r2 = base.cuda(), base.numpy().copy()
+    o_a, _ = prefill_paged_both(part1, p2, r2, errs)
+    o_b, _ = prefill_paged_both(part2, p2, r2, errs)
+    d = (torch.cat([o_a, o_b]).float() - o_full.float()).abs().max().item()
+    assert d <= 1e-2
+    e = (p2[ids.long()] - p1[ids.long()]).flatten(1).norm(dim=1) / p1[ids.long()].flatten(1).norm(dim=1)
+    assert e.max().item() <= 1e-3
+
+
+def test_general_slot_api_minus_one_rows():
+    """Read row -1 = zero state; write and checkpoint rows of -1 are skipped."""
+    H, N = 2, 64
+    lens = [150, 90, 200]
+    prefixes = [0, 30, 64]
+    gen = torch.Generator().manual_seed(9)
+    q, k, v, g, b = workloads.draw_tokens(gen, sum(lens), H, "cpu")
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    pool = workloads.sentinel_pool(6, H, "cpu")
+    workloads.fill_rows(pool, [1, 2], gen)
+    si = torch.tensor([-1, 1, 2], dtype=torch.int32)
+    osi = torch.tensor([3, -1, 4], dtype=torch.int32)
+    P = torch.tensor(prefixes, dtype=torch.int32)
+    counts = [(p + l) // N - p // N for p, l in zip(prefixes, lens)]
+    ccs = torch.tensor(np.concatenate([[0], np.cumsum(counts)[:-1]]), dtype=torch.int32)
+    cki = torch.arange(sum(counts), dtype=torch.int32)
+    cki[1] = -1
+    cki[-1] = -1
+    ck = workloads.sentinel_pool(sum(counts), H, "cpu")
+    dev = lambda t: t.cuda()
+    pool_g, ck_g = pool.cuda(), ck.cuda()
+    pb, cb = pool_g.clone(), ck_g.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = gdn.gdn_chunk_gated_delta_rule(dev(q), dev(k), dev(v), dev(g), dev(b), dev(cu), scale=SCALE,
+                                       initial_state=pool_g, state_indices=dev(si), output_state=pool_g,
+                                       output_state_indices=dev(osi), state_checkpoints=ck_g,
+                                       checkpoint_state_indices=dev(cki), checkpoint_cu_starts=dev(ccs),
+                                       prefix_lens=dev(P), checkpoint_every_n_tokens=N, err_word=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    pool_o, ck_o = pool.numpy().copy(), ck.numpy().copy()
+    o_ref, w_out, w_ck = oracle.chunk_gated_delta_rule(
+        bf16_bits(q), bf16_bits(k), bf16_bits(v), f32(g), f32(b), i32(cu), SCALE, initial_state=pool_o,
+        state_indices=i32(si), output_state=pool_o, output_state_indices=i32(osi), state_checkpoints=ck_o,
+        checkpoint_state_indices=i32(cki), checkpoint_cu_starts=i32(ccs), prefix_lens=i32(P),
+        checkpoint_every_n_tokens=N)
+    errs = Errors()
+    check_o(o, o_ref, errs)
+    check_pool(pool_g, pb, pool_o, w_out, errs, "pool")
+    check_pool(ck_g, cb, ck_o, w_ck, errs, "checkpoints")
+    assert w_ck[1] == 0 and w_ck[-1] == 0
+
+
+def test_device_validation_skips_bad_sequences():
+    """With err_word, a page id outside the pool is reported and that sequence
+    is skipped; the others still match the oracle."""
+    call, pool = _ragged_case(7, 64, [100, 80], [10, 0])
+    bad = call.page_indices.clone()
+    n0 = int(call.page_indptr[1])
+    bad[0] = 10_000                               # sequence 0 reads a page outside the pool
+    call_bad = workloads.PrefillCall(call.q, call.k, call.v, call.g, call.beta, call.cu_seqlens, call.page_indptr,
+                                     bad, call.last_page_len, call.page_size)
+    pool_g = pool.cuda()
+    before = pool_g.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dev = lambda t: t.cuda()
+    o = torch.zeros(call.q.shape[0], 2, 128, dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_chunk_gated_delta_rule_paged(dev(call.q), dev(call.k), dev(call.v), dev(call.g), dev(call.beta),
+                                         dev(call.cu_seqlens), pool_g, dev(bad), dev(call.page_indptr), 64,
+                                         dev(call.last_page_len), scale=SCALE, o=o, err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == (1 << 24) | 0
+    # sequence 0 wrote nothing; sequence 1 matches the oracle
+    assert bits_equal(pool_g[bad[:n0][bad[:n0] < pool.shape[0]].long()], before[bad[:n0][bad[:n0] < pool.shape[0]].long()])
+    assert (o[:100] == 0).all()
+    pool_o = pool.numpy().copy()
+    o_ref, written = oracle.chunk_gated_delta_rule_paged(
+        bf16_bits(call.q), bf16_bits(call.k), bf16_bits(call.v), f32(call.g), f32(call.beta), i32(call.cu_seqlens),
+        pool_o, i32(call.page_indices), i32(call.page_indptr), 64, i32(call.last_page_len), SCALE,
+        chains=np.array([[0, 0], [1, 1]], bool))
+    errs = Errors()
+    check_o(o[100:], o_ref[100:], errs)
+
+
+def test_empty_and_all_zero_length_batches():
+    H = 2
+    pool = workloads.sentinel_pool(4, H, "cuda")
+    before = pool.clone()
+    z = torch.zeros(0, H, 128, dtype=torch.bfloat16, device="cuda")
+    zg = torch.zeros(0, H, device="cuda")
+    ip = torch.tensor([0, 1, 2], dtype=torch.int32, device="cuda")
+    pi = torch.tensor([1, 3], dtype=torch.int32, device="cuda")
+    lpl = torch.tensor([5, 64], dtype=torch.int32, device="cuda")
+    cu = torch.zeros(3, dtype=torch.int32, device="cuda")
+    gdn.gdn_chunk_gated_delta_rule_paged(z, z, z, zg, zg, cu, pool, pi, ip, 64, lpl, scale=SCALE)
+    torch.cuda.synchronize()
+    assert bits_equal(pool, before)
+    slots = gdn.gdn_paged_prefill_slots(cu, ip, pi, lpl, 64)
+    assert slots["output_state_indices"].tolist() == [-1, -1]
+    assert slots["state_indices"].tolist() == [1, 3]
+
+
+def test_decode_padding_and_scratch_rows():
+    """A padded decode sequence on its own scratch page (last_page_len >= 2)
+    updates only that page; explicit -1 write rows skip the store."""
+    H = 2
+    gen = torch.Generator().manual_seed(3)
+    q, k, v, g, b = workloads.draw_tokens(gen, 3, H, "cpu")
+    ip = torch.tensor([0, 2, 3, 4], dtype=torch.int32)
+    pi = torch.tensor([5, 0, 2, 7], dtype=torch.int32)
+    lpl = torch.tensor([1, 2, 9], dtype=torch.int32)
+    call = workloads.DecodeCall(q, k, v, g, b, ip, pi, lpl, 64)
+    pool = workloads.sentinel_pool(8, H, "cpu")
+    workloads.fill_rows(pool, [5, 2, 7], gen)
+    errs = Errors()
+    decode_paged_both(call, pool.cuda(), pool.numpy().copy(), errs, use_slots=True)
+    # explicit rows with a skipped write
+    pool_g = pool.cuda()
+    before = pool_g.clone()
+    slots = {"initial_state_indices": torch.tensor([5, -1, 7], dtype=torch.int32, device="cuda"),
+             "output_state_indices": torch.tensor([-1, 1, 7], dtype=torch.int32, device="cuda")}
+    o = gdn.gdn_gated_delta_rule_decode_paged(q.cuda(), k.cuda(), v.cuda(), g.cuda(), b.cuda(), pool_g, pi.cuda(),
+                                              ip.cuda(), lpl.cuda(), scale=SCALE, slots=slots)
+    pool_o = pool.numpy().copy()
+    o_ref, written = oracle.gated_delta_rule_decode(bf16_bits(q), bf16_bits(k), bf16_bits(v), f32(g), f32(b),
+                                                    pool_o, [5, -1, 7], [-1, 1, 7], SCALE)
+    torch.cuda.synchronize()
+    check_o(o, o_ref, errs)
+    check_pool(pool_g, before, pool_o, written, errs)
+    print("decode padding: %r" % errs)
