@@ -1,0 +1,416 @@
+"""Benchmark of paged GDN prefill and decode on one GB300 (or N replicas).
+
+One step = the long-context prefill workload: gdn_paged_prefill_slots plus the
+chunked paged prefill of 4 sequences x 65,536 new tokens (H = 32, K = V = 128,
+page_size 1152, state stored at all 57 page ends of every sequence).  The
+decode batch (B = 256, H = 32, page_size 1024, 10,000-page pool) is timed the
+same way as a second measurement: gdn_paged_decode_slots + one decode step.
+
+Timing: W untimed warm-up steps, then exactly K steps between a barrier and a
+device synchronize on both sides, CUDA events on the launching stream, max
+over ranks.  Every input is larger than L2 (prefill streams 8.6 GB of
+q/k/v/o, decode 1.08 GB of state), so no L2 flush is needed.  N > 1 runs N
+independent replicas (one per GPU, no collective on the data path).
+
+--impl reference times the fp64 CPU oracle (the only reference this method
+has) on the host cores over a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "GDN paged prefill tok/s + decode seq/s on 1 GB300; % HBM / tensor roofline"
+UNIT = "tok/s"
+SCALE = 128 ** -0.5
+K = V = 128
+FLOP_PER_TOKEN_HEAD = 10 * 64 * 128 + 6 * 128 * 128      # 180,224 (tensor-core contractions)
+BYTES_PER_TOKEN_HEAD = 2 * (2 * K + 2 * V) + 8           # q, k, v, o bf16 + g, beta fp32 = 1032
+STATE_BYTES = V * K * 4                                   # one (row, head) state, fp32
+DECODE_BYTES_PER_SEQ_HEAD = 2 * STATE_BYTES + 2 * (2 * K + 2 * V) + 8   # 132,104
+
+PREFILL = dict(S=4, L=65536, H=32, page_size=1152, num_pages=256)
+DECODE = dict(B=256, H=32, page_size=1024, num_pages=10000)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, rank, world, local_rank):
+    import gated_deltanet_paged_gb300 as gdn
+    from gated_deltanet_paged_gb300 import workloads
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    hbm, bf16, peak_kind = peaks()
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- prefill workload (one replica per rank) ----
+    line = {}
+    launches = 0
+    if args.workload in ("all", "prefill"):
+        launches += _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, rank, world,
+                                   hbm, bf16, peak_kind, line)
+    if args.workload in ("all", "decode"):
+        launches += _bench_decode(args, gdn, workloads, dev, stream, barrier, max_over_ranks, rank, world, hbm,
+                                  line)
+    line["gpu_launches"] = launches
+    if rank == 0 and not args.no_cpu_baseline and args.workload in ("all", "prefill"):
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, rank, world, hbm, bf16, peak_kind,
+                   line):
+    wp = workloads.long_context(dev, L=args.prefill_tokens, decode_steps=0, seed=1238 + rank)
+    pre = wp.calls[0]
+    pool = wp.pool
+    T, H = pre.q.shape[0], pre.q.shape[1]
+    o = torch.empty(T, H, V, dtype=torch.bfloat16, device=dev)
+    stores = sum(-(-(int(l)) // PREFILL["page_size"]) for l in wp.seq_lens.tolist())  # page ends + final
+    prefill_bytes = T * H * BYTES_PER_TOKEN_HEAD + stores * H * STATE_BYTES
+    prefill_flops = T * H * FLOP_PER_TOKEN_HEAD
+    slot_out = gdn.gdn_paged_prefill_slots(pre.cu_seqlens, pre.page_indptr, pre.page_indices, pre.last_page_len,
+                                           pre.page_size)
+
+    def prefill_step(ev=None):
+        gdn.gdn_paged_prefill_slots(pre.cu_seqlens, pre.page_indptr, pre.page_indices, pre.last_page_len,
+                                    pre.page_size, out=slot_out)
+        if ev is not None:
+            ev[0].record(stream)
+        gdn.gdn_chunk_gated_delta_rule_paged(pre.q, pre.k, pre.v, pre.g, pre.beta, pre.cu_seqlens, pool,
+                                             pre.page_indices, pre.page_indptr, pre.page_size, pre.last_page_len,
+                                             scale=SCALE, slots=slot_out, o=o)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        prefill_step()
+    torch.cuda.synchronize(dev)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for i in range(args.steps):
+            prefill_step(kev[i])
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    ms_prefill = max_over_ranks(start.elapsed_time(stop) / args.steps)
+    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    clocks = clk.summary()
+    launches = 2 * args.steps
+
+    # ---- e2e: host buffers, copies inside the timed region ----
+    e2e = None
+    if not args.no_e2e:
+        host = {n: getattr(pre, n).cpu().pin_memory() for n in ("q", "k", "v", "g", "beta")}
+        host_o = torch.empty(T, H, V, dtype=torch.bfloat16).pin_memory()
+        dbuf = {n: torch.empty_like(getattr(pre, n)) for n in host}
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = host_o.numel() * host_o.element_size()
+
+        def e2e_step():
+            for n, t in host.items():
+                dbuf[n].copy_(t, non_blocking=True)
+            gdn.gdn_chunk_gated_delta_rule_paged(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"],
+                                                 pre.cu_seqlens, pool, pre.page_indices, pre.page_indptr,
+                                                 pre.page_size, pre.last_page_len, scale=SCALE, o=o)
+            host_o.copy_(o, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        e2e_steps = max(1, min(args.steps, 5))
+        barrier()
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        ms_e2e = max_over_ranks(start.elapsed_time(stop) / e2e_steps)
+        e2e = {"value": T * world / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
+        launches += e2e_steps + 1
+        del host, host_o, dbuf
+
+    value = T * world / (ms_prefill * 1e-3)
+    achieved = prefill_bytes / (kernel_ms * 1e-3) / 1e9
+    full = args.prefill_tokens == PREFILL["L"]
+    line.update({
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_prefill,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "precision": "bf16 q/k/v/o, fp32 g/beta/state, fp16 tensor-core operands with fp32 accumulation",
+        "data": "synthetic (seeded; q,k L2-normalised bf16, v bf16, g=-softplus(N), beta=sigmoid(N))",
+        "config": {"workload": "long-context paged prefill: 4 seqs x %d new tokens, H=32, K=V=128, "
+                               "page_size=1152, state stored at every page end (step = slots + prefill)%s"
+                               % (args.prefill_tokens, "" if full else " [reduced size: not a headline run]"),
+                   "tokens_per_step": T, "l2": "inputs larger than L2 (streamed q/k/v/o per step), no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": None, "kernel": "prefill_kernel", "kernel_ms": kernel_ms,
+                     "algorithmic_bytes": prefill_bytes, "peak_kind": peak_kind},
+        "tensor": {"achieved_tflops": prefill_flops / (kernel_ms * 1e-3) / 1e12, "peak_tflops": bf16,
+                   "frac": prefill_flops / (kernel_ms * 1e-3) / 1e12 / bf16, "flops_per_launch": prefill_flops},
+        "clocks": clocks,
+    })
+    if e2e is not None:
+        line["e2e"] = e2e
+    del o
+    return launches
+
+
+def _bench_decode(args, gdn, workloads, dev, stream, barrier, max_over_ranks, rank, world, hbm, line):
+    H = DECODE["H"]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wd = workloads.decode_batch(dev, seed=1236 + rank)
+    dc = wd.calls[0]
+    dpool = wd.pool
+    od = torch.empty(DECODE["B"], H, V, dtype=torch.bfloat16, device=dev)
+    dslots = gdn.gdn_paged_decode_slots(dc.page_indptr, dc.page_indices, dc.last_page_len)
+
+    def decode_step(ev=None):
+        gdn.gdn_paged_decode_slots(dc.page_indptr, dc.page_indices, dc.last_page_len, out=dslots)
+        if ev is not None:
+            ev[0].record(stream)
+        gdn.gdn_gated_delta_rule_decode_paged(dc.q, dc.k, dc.v, dc.g, dc.beta, dpool, dc.page_indices,
+                                              dc.page_indptr, dc.last_page_len, scale=SCALE, slots=dslots, o=od)
+        if ev is not None:
+            ev[1].record(stream)
+
+    dsteps = max(args.steps, 20)
+    for _ in range(max(args.warmup, 3)):
+        decode_step()
+    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(dsteps)]
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for i in range(dsteps):
+            decode_step(dev_ev[i])
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    ms_decode = max_over_ranks(start.elapsed_time(stop) / dsteps)
+    dkernel_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
+    decode_bytes = DECODE["B"] * H * DECODE_BYTES_PER_SEQ_HEAD
+    ach = decode_bytes / (dkernel_ms * 1e-3) / 1e9
+    dec = {"metric": "decode seq/s", "value": DECODE["B"] * world / (ms_decode * 1e-3), "unit": "seq/s",
+           "ms_per_step": ms_decode, "kernel_ms": dkernel_ms, "steps": dsteps,
+           "workload": "paged decode batch: B=256, H=32, page_size=1024, ctx U{2..32768}, "
+                       "25% open a page, 10,000-page pool (step = decode slots + decode)",
+           "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                        "algorithmic_bytes": decode_bytes},
+           "clocks": clk.summary()}
+    if "metric" in line:
+        line["decode"] = dec
+    else:  # decode-only run: the decode measurement is the line
+        line.update({"metric": METRIC, "value": dec["value"], "unit": "seq/s", "n_gpus": world, "steps": dsteps,
+                     "warmup": max(args.warmup, 3), "ms_per_step": ms_decode, "higher_is_better": True,
+                     "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+                     "config": {"workload": dec["workload"]}, "roofline": dec["roofline"], "clocks": dec["clocks"]})
+    return 2 * dsteps
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_sample(n_tok):
+    """Seconds the fp64 oracle takes for the first n_tok tokens of each of the
+    4 long-context sequences, all 32 heads (one paged prefill call)."""
+    import oracle
+    from gated_deltanet_paged_gb300 import workloads
+
+    H, S, ps = PREFILL["H"], PREFILL["S"], PREFILL["page_size"]
+    gen = torch.Generator().manual_seed(1238)
+    q, k, v, g, b = workloads.draw_tokens(gen, S * n_tok, H, "cpu")
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    npg = -(-n_tok // ps)
+    pool = np.zeros((S * npg, H, V, K), np.float32)
+    ip = np.arange(S + 1, dtype=np.int32) * npg
+    pi = np.arange(S * npg, dtype=np.int32)
+    lpl = np.full(S, n_tok - (npg - 1) * ps, np.int32)
+    cu = np.arange(S + 1, dtype=np.int32) * n_tok
+    t0 = time.perf_counter()
+    oracle.chunk_gated_delta_rule_paged(bits(q), bits(k), bits(v), g.numpy(), b.numpy(), cu, pool, pi, ip, ps,
+                                        lpl, SCALE)
+    return time.perf_counter() - t0
+
+
+def _calibrate(target_s):
+    probe = 64
+    dt = _oracle_sample(probe)
+    return int(max(probe, min(PREFILL["L"], probe * target_s / max(dt, 1e-3))))
+
+
+def _cores():
+    cores = os.cpu_count() or 1
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    return int(os.environ["OMP_NUM_THREADS"])
+
+
+def cpu_baseline(target_s=15.0):
+    """The oracle as it stands, on the host cores, over a bounded sample of
+    the prefill workload (~target_s seconds)."""
+    cores = _cores()
+    n_tok = _calibrate(target_s)
+    dt = _oracle_sample(n_tok)
+    return {"value": PREFILL["S"] * n_tok / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "first %d tokens of each of the 4 long-context sequences, all 32 heads (%.1f s)"
+                      % (n_tok, dt)}
+
+
+def run_reference(args, rank):
+    """Reference arm: the fp64 oracle timed on the host cores, each step a
+    bounded sample of the prefill workload; rank 0 only."""
+    if rank != 0:
+        return None
+    cores = _cores()
+    per_step = args.cpu_seconds / max(1, args.steps + args.warmup)
+    n_tok = _calibrate(per_step)
+    for _ in range(args.warmup):
+        _oracle_sample(n_tok)
+    times = [_oracle_sample(n_tok) for _ in range(args.steps)]
+    ms = 1e3 * sum(times) / len(times)
+    value = PREFILL["S"] * n_tok / (ms * 1e-3)
+    sample = "first %d tokens of each of the 4 long-context sequences, all 32 heads" % n_tok
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "impl": "reference",
+        "config": {"workload": "long-context paged prefill: 4 seqs x 65,536 new tokens, H=32, K=V=128, "
+                               "page_size=1152 (bounded sample per step)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", choices=["all", "prefill", "decode"], default="all")
+    ap.add_argument("--prefill-tokens", type=int, default=PREFILL["L"],
+                    help="new tokens per sequence of the prefill workload (smaller only for profiling)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "gdn" else args.warmup
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+    else:
+        line = run_gpu(args, rank, world, local_rank)
+    if rank == 0 and line is not None:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()
