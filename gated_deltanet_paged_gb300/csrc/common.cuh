@@ -137,6 +137,36 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
       : "memory");
 }
 
+// Four (two) consecutive K-steps of one product, issued as a single asm block:
+// step s uses descriptors a + s*astep and b + s*bstep (steps in 16-byte units
+// of the start-address field); the first step accumulates iff acc0 != 0, the
+// others always accumulate.
+__device__ __forceinline__ void tc_mma4(uint32_t d, uint64_t a, uint32_t astep, uint64_t b, uint32_t bstep,
+                                        uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 q, %6, %6;\n\t"
+      "add.s64 a1, %1, %2;\n\tadd.s64 a2, a1, %2;\n\tadd.s64 a3, a2, %2;\n\t"
+      "add.s64 b1, %3, %4;\n\tadd.s64 b2, b1, %4;\n\tadd.s64 b3, b2, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %3, %5, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %5, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %5, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %5, q;\n\t}\n" ::"r"(d),
+      "l"(a), "l"(static_cast<uint64_t>(astep)), "l"(b), "l"(static_cast<uint64_t>(bstep)), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma2(uint32_t d, uint64_t a, uint32_t astep, uint64_t b, uint32_t bstep,
+                                        uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b64 a1, b1;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 q, %6, %6;\n\t"
+      "add.s64 a1, %1, %2;\n\tadd.s64 b1, %3, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %3, %5, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %5, q;\n\t}\n" ::"r"(d),
+      "l"(a), "l"(static_cast<uint64_t>(astep)), "l"(b), "l"(static_cast<uint64_t>(bstep)), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+
 // Load 32 consecutive fp32 columns of this thread's TMEM lane and wait for them.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
   uint32_t* u = reinterpret_cast<uint32_t*>(r);
@@ -150,6 +180,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
         "=r"(u[15]), "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]), "=r"(u[20]), "=r"(u[21]),
         "=r"(u[22]), "=r"(u[23]), "=r"(u[24]), "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]),
         "=r"(u[29]), "=r"(u[30]), "=r"(u[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Load 16 consecutive fp32 columns of this thread's TMEM lane and wait for them.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
+  uint32_t* u = reinterpret_cast<uint32_t*>(r);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+        "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]),
+        "=r"(u[15])
       : "r"(taddr)
       : "memory");
 }

@@ -6,26 +6,37 @@
 // skip, checkpoints at absolute positions (prefix + n) % N == 0).
 //
 // Method (gated delta rule, chunked).  Per (sequence, head) chain and 64-token
-// chunk with rows t = 0..63, cumulative gate G_t = g_0 + ... + g_t (padded
-// rows have g = beta = 0 and k = v = 0 in effect, so they are the identity),
+// chunk with rows t = 0..63, cumulative gate G_t = g_0 + ... + g_t (rows outside
+// the sequence have g = beta = 0 and k = v = 0, so they are the identity),
 // gamma_t = exp(G_t), S0 the V x K state at the chunk start:
 //   A[t][j] = beta_t exp(G_t - G_j) (k_t . k_j)      j < t   (strictly lower)
-//   T       = (I + A)^-1                             (forward substitution)
+//   T       = (I + A)^-1
 //   W       = T diag(beta gamma) K,   U~ = T diag(beta) V
-//   U       = U~ - W S0^T                            (the chunk's "new values")
+//   U       = U~ - W S0^T                            (the chunk's new values)
 //   O[t]    = scale (gamma_t S0 q_t + sum_{j<=t} exp(G_t - G_j)(q_t . k_j) U[j])
 //   S1      = gamma_C S0 + U^T diag(exp(G_C - G_j)) K
-// which equals the token-by-token recurrence exactly up to rounding.
+// which equals the token-by-token recurrence up to rounding.
 //
 // Mapping.  One CTA (256 threads) per chain, chains ordered by decreasing
-// length so the longest start first.  Q, K, V tiles arrive by TMA (3-D tensor
-// map over [T, H, 128], 128-byte swizzle, zero fill outside the tensor); the
-// products run as tcgen05.mma (M = 128) with fp32 accumulators in TMEM:
-//   [K;Q] K^T (bf16) -> KK^T, QK^T;   W^T, U~^T (fp16);   S0 W^T, S0 Q^T;
-//   U^T K~ (state update, N = 128);   U^T P^T (intra-chunk output).
-// The fp32 state lives in registers (thread = state row v, half of K) and is
-// re-staged as an fp16 MMA operand each chunk.  fp16 (11-bit significand)
-// rather than bf16 operands keep written states within 1e-3 relative error.
+// length.  Per chunk the work splits into a state-independent "prep" (TMA of
+// Q/K/V, gates, [K;Q]K^T, A and P, the inverse T, W^T and U~^T) and the state
+// "chain" (S0 W^T and S0 Q~^T, U, U^T K~ and U^T P^T, the state update and the
+// outputs).  The loop runs chain(c) and prep(c+1) in one software-pipelined
+// instruction stream: every tcgen05.mma is followed by CUDA-core work that does
+// not depend on it, so MMA latency hides behind the other half.  TMA runs two
+// chunks ahead into a pair of slots.
+//   - MMAs (M = 128, fp32 accumulators in TMEM): [K;Q]K^T on bf16 straight from
+//     TMA; everything else on fp16 operands (11-bit significand keeps written
+//     states within 1e-3 relative error; bf16 would not).
+//   - decay factors exp(G_t - G_j) come from running products of exp(g).
+//   - T = (I + A)^-1: 16x16 diagonal blocks by forward substitution, the 16->32
+//     merges T10 = -T11 A10 T00 on CUDA cores, the 32->64 merge as two MMAs.
+//   - beta gamma and beta fold into the columns of T (T', T''), gamma into Q~
+//     and exp(G_C - G) into K~, so O = scale (S0 Q~^T + U P^T) is one
+//     accumulator and S1 = gamma_C S0 + U^T K~.
+//   - the fp32 state lives in registers (thread = state row v, half of K) and is
+//     restaged as the fp16 MMA operand every chunk; page-boundary and final
+//     states go from registers to the pool.
 #include <math.h>
 
 #include "common.cuh"
@@ -34,32 +45,36 @@ namespace {
 
 using namespace gdn;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr uint32_t kTile = 8192;  // 64 rows x 128 B
 
-// Shared-memory map (byte offsets from a 1024-byte aligned base).
-constexpr uint32_t OFF_A1 = 0;           // [kb0: K | Q][kb1: K | Q], 8 KB each; K -> K~, Q -> Q fp16 in place
-constexpr uint32_t OFF_V = 32768;        // [vb0 | vb1]; V -> beta V fp16 in place
-constexpr uint32_t OFF_BGK = 49152;      // beta gamma K, fp16 [kb0 | kb1]
-constexpr uint32_t OFF_T = 65536;        // T fp16, rows t
-constexpr uint32_t OFF_P = 73728;        // P fp16, rows t
-constexpr uint32_t OFF_WT = 81920;       // W^T fp16, rows k (128)
-constexpr uint32_t OFF_U = 98304;        // U^T fp16, rows v (128)
-constexpr uint32_t OFF_S = 114688;       // S fp16 [kb0 | kb1], rows v (128 each)
-constexpr uint32_t OFF_AM = 147456;      // A matrix fp32 64 x 68 / output staging bf16 64 x 128
-constexpr uint32_t OFF_SMALL = OFF_AM + 64 * 68 * 4;
+// Slot: the raw TMA tiles of one chunk (two slots), converted in place.
+constexpr uint32_t SLOT_BYTES = 49152;
+constexpr uint32_t SL_K0 = 0;      // K cols 0-63   -> K fp16 (MN-major A of W^T)
+constexpr uint32_t SL_Q0 = 8192;   // Q cols 0-63   -> M16 (merge operands) -> T' fp16
+constexpr uint32_t SL_K1 = 16384;  // K cols 64-127 -> K fp16
+constexpr uint32_t SL_Q1 = 24576;  // Q cols 64-127 -> Y16 (merge operand) -> T'' fp16
+constexpr uint32_t SL_V0 = 32768;  // V cols 0-63   -> V fp16 (MN-major A of U~^T)
+constexpr uint32_t SL_V1 = 40960;  // V cols 64-127 -> V fp16
+// Other tiles (byte offsets from the 1024-aligned base).
+constexpr uint32_t OFF_QT = 2 * SLOT_BYTES;  // Q~ = diag(gamma) Q fp16 [kb0 | kb1], rows t
+constexpr uint32_t OFF_KT = OFF_QT + 16384;  // K~ = diag(exp(G_C - G)) K fp16 [kb0 | kb1], rows t
+constexpr uint32_t OFF_P = OFF_KT + 16384;   // P fp16, two buffers, rows t
+constexpr uint32_t OFF_WT = OFF_P + 16384;   // W^T fp16 rows k; also the fp32 A -> T matrix
+constexpr uint32_t OFF_U = OFF_WT + 16384;   // U^T fp16 rows v
+constexpr uint32_t OFF_S = OFF_U + 16384;    // S fp16 [kb0 | kb1], rows v
+constexpr uint32_t OFF_SMALL = OFF_S + 32768;
 constexpr uint32_t SMEM_USED = OFF_SMALL + 2048;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
-constexpr int AM_LD = 68;
 
 // TMEM columns (fp32, 128 lanes).
-constexpr uint32_t COL_D1 = 0;    // lanes 0-63: K K^T, lanes 64-127: Q K^T  (64 cols)
+constexpr uint32_t COL_D1 = 0;    // [K;Q]K^T
 constexpr uint32_t COL_WT = 64;   // W^T   (lane = k)
 constexpr uint32_t COL_UT = 128;  // U~^T  (lane = v)
 constexpr uint32_t COL_X1 = 192;  // S0 W^T
-constexpr uint32_t COL_X2 = 256;  // S0 Q^T
+constexpr uint32_t COL_O = 256;   // S0 Q~^T + U^T P^T
 constexpr uint32_t COL_SU = 320;  // U^T K~ (128 cols)
-constexpr uint32_t COL_Y = 448;   // U^T P^T
+constexpr uint32_t COL_L2 = 448;  // 32->64 merge products of the inverse
 constexpr uint32_t TMEM_COLS = 512;
 
 struct PrefillArgs {
@@ -90,13 +105,16 @@ struct PrefillArgs {
   int32_t* err_word;
 };
 
+// Per-chunk scalars of the chunk being prepared.
 struct Small {
-  float G[64];
-  float gam[64];
-  float bet[64];
-  int valid[64];
-  uint64_t bar_tma;
-  uint64_t bar_mma;
+  float G[64];    // cumulative gate
+  float e[64];    // exp(g)
+  float gam[64];  // exp(G)
+  float bet[64];  // beta (0 outside the sequence)
+  float sT1[64];  // beta * gamma  (column scale of T')
+  float ksc[64];  // exp(G_C - G)  (row scale of K~)
+  uint64_t bar_tma[2];
+  uint64_t bar_x, bar_1, bar_s, bar_2, bar_l2;
   uint32_t tmem_base;
   int seq;
   int flag;
@@ -115,11 +133,25 @@ __device__ __forceinline__ void cvt8_store(uint8_t* dst, const uint8_t* src_bf16
   *reinterpret_cast<uint4*>(dst) = out;
 }
 
-// All threads wait for an mbarrier phase; false (for every thread) if any
-// thread timed out.
-__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity) {
-  const bool ok = mbar_wait(bar, parity);
-  return __syncthreads_or(ok ? 0 : 1) == 0;
+__device__ __forceinline__ uint32_t scale_half2(uint32_t u, float sc) {
+  __half2 h = *reinterpret_cast<__half2*>(&u);
+  const float2 f = __half22float2(h);
+  return pack_half2(f.x * sc, f.y * sc);
+}
+
+__device__ __forceinline__ uint4 pack8_half(const float* x) {
+  uint4 u;
+  u.x = pack_half2(x[0], x[1]);
+  u.y = pack_half2(x[2], x[3]);
+  u.z = pack_half2(x[4], x[5]);
+  u.w = pack_half2(x[6], x[7]);
+  return u;
+}
+
+// fp32 64 x 64 matrix, 16-byte chunk cj of row r stored at chunk cj ^ (r % 16).
+__device__ __forceinline__ float* am_chunk(float* AM, int r, int cj) { return AM + r * 64 + ((cj ^ (r & 15)) << 2); }
+__device__ __forceinline__ float& am_at(float* AM, int r, int j) {
+  return AM[r * 64 + ((((j >> 2) ^ (r & 15)) << 2) | (j & 3))];
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -129,15 +161,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
   Small& sh = *reinterpret_cast<Small*>(sm + OFF_SMALL);
-  float* AM = reinterpret_cast<float*>(sm + OFF_AM);
+  float* AM = reinterpret_cast<float*>(sm + OFF_WT);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.H;
   const int rank = blockIdx.x / H, h = blockIdx.x % H;
 
   // ---- pick the sequence: rank-th longest (ties by index) ----
-  if (a.num_seqs > 1 && a.num_seqs <= 4096) {
-    int* cu_s = reinterpret_cast<int*>(sm + OFF_AM);
+  if (a.num_seqs > 1 && a.num_seqs < 4096) {
+    int* cu_s = reinterpret_cast<int*>(sm + OFF_QT);
     for (int i = tid; i <= a.num_seqs; i += kThreads) cu_s[i] = a.cu_seqlens[i];
     if (tid == 0) sh.seq = -1;
     __syncthreads();
@@ -172,8 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lpl = a.last_len[b];
     const long long tot = static_cast<long long>(n - 1) * a.page_size + lpl;
     P = static_cast<int>(tot - L);
-    bool bad = n < 1 || lpl < 1 || lpl > a.page_size || tot < L;
-    if (bad) {
+    if (n < 1 || lpl < 1 || lpl > a.page_size || tot < L) {
       if (tid == 0) record_error(a.err_word, GDN_DEVERR_PAGE_TABLE, b);
       return;
     }
@@ -184,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (a.err_word) {
       if (tid == 0) {
         int badp = 0;
-        for (int i = (P > 0 ? (P - 1) / a.page_size : P / a.page_size); i < n; ++i) {
+        for (int i = (P > 0 ? (P - 1) / a.page_size : 0); i < n; ++i) {
           const int id = a.pages[i0 + i];
           badp |= (id < 0 || id >= a.num_pages);
         }
@@ -216,8 +247,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- set-up: barriers, TMEM ----
   if (tid == 0) {
-    mbar_init(&sh.bar_tma, 1);
-    mbar_init(&sh.bar_mma, 1);
+    mbar_init(&sh.bar_tma[0], 1);
+    mbar_init(&sh.bar_tma[1], 1);
+    mbar_init(&sh.bar_x, 1);
+    mbar_init(&sh.bar_1, 1);
+    mbar_init(&sh.bar_s, 1);
+    mbar_init(&sh.bar_2, 1);
+    mbar_init(&sh.bar_l2, 1);
     fence_mbar_init();
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_k);
@@ -232,18 +268,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
 
-  const int v_row = tid & 127;        // state row / TMEM lane of this thread
-  const int khalf = tid >> 7;         // which 64 columns of K this thread keeps
+  // Thread roles: v_row = state row / TMEM lane (0..127), quarter = which 32
+  // state columns (and which quarter of a 64-column accumulator) it handles.
+  // For tile conversions every thread owns row cr = tid / 8, 16-byte chunk
+  // tid % 8, in both 64-column blocks (byte offset tid * 16 in a block).
+  const int v_row = tid & 127;
+  const int quarter = tid >> 7;
+  const int cr = tid >> 3;
+  const uint32_t coff = static_cast<uint32_t>(tid) * 16u;
   const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
   const int64_t head_off = static_cast<int64_t>(h) * kDimV * kDimK;
-  const int64_t my_off = head_off + static_cast<int64_t>(v_row) * kDimK + 64 * khalf;
 
   // ---- initial state: pool row or literal zeros (the pool is never scaled by 0) ----
-  float S[64];
+  float S[32];
   if (in_row >= 0) {
-    const float4* src = reinterpret_cast<const float4*>(init_pool + in_row * a.row_stride + my_off);
+    const float4* src =
+        reinterpret_cast<const float4*>(init_pool + in_row * a.row_stride + head_off + v_row * kDimK + 32 * quarter);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 8; ++i) {
       const float4 x = src[i];
       S[4 * i] = x.x;
       S[4 * i + 1] = x.y;
@@ -252,23 +294,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < 64; ++i) S[i] = 0.f;
+    for (int i = 0; i < 32; ++i) S[i] = 0.f;
   }
-  auto stage_state = [&]() {
+  auto stage_state = [&]() {  // fp16 copy of S as the MMA operand
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      uint4 u;
-      u.x = pack_half2(S[8 * c], S[8 * c + 1]);
-      u.y = pack_half2(S[8 * c + 2], S[8 * c + 3]);
-      u.z = pack_half2(S[8 * c + 4], S[8 * c + 5]);
-      u.w = pack_half2(S[8 * c + 6], S[8 * c + 7]);
-      *reinterpret_cast<uint4*>(sm + OFF_S + khalf * 16384 + swz(v_row, c)) = u;
-    }
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint4*>(sm + OFF_S + (quarter >> 1) * 16384 + swz(v_row, 4 * (quarter & 1) + c)) =
+          pack8_half(&S[8 * c]);
   };
+  // Store the fp32 state to a pool row with coalesced 16-byte stores, staging
+  // 32 state rows (16 KB) at a time in the U tile (free whenever this runs).
   auto store_state = [&](float* pool, int row) {
-    float4* dst = reinterpret_cast<float4*>(pool + row * a.row_stride + my_off);
+    float4* stg = reinterpret_cast<float4*>(sm + OFF_U);
+    float4* dst = reinterpret_cast<float4*>(pool + row * a.row_stride + head_off);
+#pragma unroll 1
+    for (int r = 0; r < 4; ++r) {
+      if ((warp & 3) == r) {
+        const int rr = v_row - 32 * r;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
+        for (int i = 0; i < 8; ++i)
+          stg[rr * 32 + ((8 * quarter + i) ^ rr)] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int i = tid + k * kThreads;
+        dst[r * 1024 + i] = stg[(i >> 5) * 32 + ((i & 31) ^ (i >> 5))];
+      }
+      __syncthreads();
+    }
   };
   stage_state();
 
@@ -276,8 +330,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int first_pos = (P / kChunk) * kChunk;
   const int nchunks = (end_pos + kChunk - 1) / kChunk - P / kChunk;
   const int first_ck = (ck_rows && N > 0) ? P / N : 0;
-  uint32_t mma_phase = 0;
-  bool failed = false;
 
   const uint32_t id_bf16_kk = idesc_f16(128, 64, true, true, false, false);
   const uint32_t id_mnA = idesc_f16(128, 64, false, false, true, false);
@@ -285,295 +337,486 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t id_kk64 = idesc_f16(128, 64, false, false, false, false);
   const uint32_t id_mnB128 = idesc_f16(128, 128, false, false, false, true);
 
-  for (int c = 0; c < nchunks; ++c) {
-    const int a0 = first_pos + kChunk * c;   // absolute position of chunk row 0
-    const int t_first = cu_b + (a0 - P);     // packed token index of chunk row 0
+  // Geometry of chunk ch: absolute position of row 0, valid rows [lo, hi),
+  // packed token index of row 0.
+  auto chunk_a0 = [&](int ch) { return first_pos + kChunk * ch; };
+  auto chunk_lo = [&](int ch) { return max(P - chunk_a0(ch), 0); };
+  auto chunk_hi = [&](int ch) { return min(end_pos - chunk_a0(ch), kChunk); };
+  auto chunk_tf = [&](int ch) { return cu_b + (chunk_a0(ch) - P); };
+  auto slot_off = [&](int ch) { return static_cast<uint32_t>(ch & 1) * SLOT_BYTES; };
+  // Shared-memory descriptors: K-major (8-row groups 1024 B apart) and MN-major.
+  auto dK = [&](uint32_t off) { return sdesc(sbase + off, 16, 1024); };
+  auto dMN = [&](uint32_t off, uint32_t lbo) { return sdesc(sbase + off, lbo, 1024); };
 
-    // (1) TMA loads of K, Q, V; gates of the 64 rows.
-    if (tid == 0) {
-      mbar_arrive_expect_tx(&sh.bar_tma, 6 * kTile);
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb) {
-        tma_load_3d(sm + OFF_A1 + kb * 16384, &tm_k, &sh.bar_tma, kb * 64, h, t_first);
-        tma_load_3d(sm + OFF_A1 + kb * 16384 + kTile, &tm_q, &sh.bar_tma, kb * 64, h, t_first);
-        tma_load_3d(sm + OFF_V + kb * kTile, &tm_v, &sh.bar_tma, kb * 64, h, t_first);
-      }
+  uint32_t ph_x = 0, ph_1 = 0, ph_s = 0, ph_2 = 0, ph_l2 = 0;
+  bool failed = false;
+  // One thread polls the mbarrier; everybody meets at a hardware barrier.
+  auto wait_bar = [&](uint64_t* bar, uint32_t parity) -> bool {
+    int bad = 0;
+    if (tid == 0) bad = mbar_wait(bar, parity) ? 0 : 1;
+    return __syncthreads_or(bad) == 0;
+  };
+
+  // ---------------------------------------------------------------- prep ----
+  auto issue_tma = [&](int ch) {  // one thread
+    const int tf = chunk_tf(ch);
+    uint8_t* s = sm + slot_off(ch);
+    uint64_t* bar = &sh.bar_tma[ch & 1];
+    mbar_arrive_expect_tx(bar, 6 * kTile);
+    tma_load_3d(s + SL_K0, &tm_k, bar, 0, h, tf);
+    tma_load_3d(s + SL_K1, &tm_k, bar, 64, h, tf);
+    tma_load_3d(s + SL_Q0, &tm_q, bar, 0, h, tf);
+    tma_load_3d(s + SL_Q1, &tm_q, bar, 64, h, tf);
+    tma_load_3d(s + SL_V0, &tm_v, bar, 0, h, tf);
+    tma_load_3d(s + SL_V1, &tm_v, bar, 64, h, tf);
+  };
+  float pg0 = 0.f, pg1 = 0.f, pb0 = 0.f, pb1 = 0.f;  // gates of rows 2*lane, 2*lane+1 (warp 1)
+  auto prefetch_gates = [&](int ch) {
+    if (warp == 1) {
+      const int lo = chunk_lo(ch), hi = chunk_hi(ch);
+      const int64_t tf = chunk_tf(ch);
+      const int r0 = 2 * lane, r1 = 2 * lane + 1;
+      const bool v0 = r0 >= lo && r0 < hi, v1 = r1 >= lo && r1 < hi;
+      pg0 = v0 ? a.g[(tf + r0) * H + h] : 0.f;
+      pb0 = v0 ? a.beta[(tf + r0) * H + h] : 0.f;
+      pg1 = v1 ? a.g[(tf + r1) * H + h] : 0.f;
+      pb1 = v1 ? a.beta[(tf + r1) * H + h] : 0.f;
     }
-    if (tid < 64) {
-      const int pos = a0 + tid;
-      const bool valid = pos >= P && pos < end_pos;
-      const int64_t t = static_cast<int64_t>(t_first) + tid;
-      sh.G[tid] = valid ? a.g[t * H + h] : 0.f;
-      sh.bet[tid] = valid ? a.beta[t * H + h] : 0.f;
-      sh.valid[tid] = valid;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const float x0 = sh.G[2 * lane], x1 = sh.G[2 * lane + 1];
-      float s = x0 + x1;
+  };
+  auto gates = [&]() {  // warp 1: cumulative gate and the per-row scalars
+    if (warp == 1) {
+      float s = pg0 + pg1;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const float y = __shfl_up_sync(0xffffffffu, s, off);
         if (lane >= off) s += y;
       }
-      const float g0 = s - x1;
-      sh.G[2 * lane] = g0;
-      sh.G[2 * lane + 1] = s;
-      sh.gam[2 * lane] = expf(g0);
-      sh.gam[2 * lane + 1] = expf(s);
+      const float G0 = s - pg1, G1 = s;
+      const float GC = __shfl_sync(0xffffffffu, s, 31);
+      const float gm0 = expf(G0), gm1 = expf(G1);
+      sh.G[2 * lane] = G0;
+      sh.G[2 * lane + 1] = G1;
+      sh.e[2 * lane] = expf(pg0);
+      sh.e[2 * lane + 1] = expf(pg1);
+      sh.gam[2 * lane] = gm0;
+      sh.gam[2 * lane + 1] = gm1;
+      sh.bet[2 * lane] = pb0;
+      sh.bet[2 * lane + 1] = pb1;
+      sh.sT1[2 * lane] = pb0 * gm0;
+      sh.sT1[2 * lane + 1] = pb1 * gm1;
+      sh.ksc[2 * lane] = expf(GC - G0);
+      sh.ksc[2 * lane + 1] = expf(GC - G1);
     }
-    if (!wait_all(&sh.bar_tma, c & 1)) {
-      failed = true;
-      break;
+  };
+  // Convert this thread's chunk of both 64-column blocks of a bf16 tile.
+  auto cvt_tile = [&](uint32_t dst, uint32_t dblk, uint32_t src, uint32_t sblk, float sc, bool keep) {
+    cvt8_store(sm + dst + coff, sm + src + coff, sc, keep);
+    cvt8_store(sm + dst + dblk + coff, sm + src + sblk + coff, sc, keep);
+  };
+  auto row_ok = [&](int ch) { return cr >= chunk_lo(ch) && cr < chunk_hi(ch); };
+  // A (fp32, AM) from K K^T rows, P (fp16 operand) from Q K^T rows; decay
+  // factors by running products exp(G_t - G_{j-1}) = exp(G_t - G_j) exp(g_j).
+  auto build_AP = [&](int ch) {
+    const int lo = chunk_lo(ch), hi = chunk_hi(ch);
+    const int j0 = 16 * quarter;
+    float x[16], ev[16];
+    tmem_ld16(lane_addr + COL_D1 + j0, x);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 e4 = *reinterpret_cast<const float4*>(&sh.e[j0 + 4 * q]);
+      ev[4 * q] = e4.x;
+      ev[4 * q + 1] = e4.y;
+      ev[4 * q + 2] = e4.z;
+      ev[4 * q + 3] = e4.w;
     }
-    const float GC = sh.G[63];
-    const float gamC = sh.gam[63];
-
-    // (2) MMA1: [K;Q] K^T -> D1 (bf16 operands straight from TMA).
-    if (tid == 0) {
-      tc_fence_after();
+    const int t = v_row & 63;
+    const bool vt = t >= lo && t < hi;
+    const bool isA = v_row < 64;
+    const int jstart = min(j0 + 15, isA ? t - 1 : t);  // last column kept (j < t for A, j <= t for P)
+    float cur = 0.f;
+    if (vt && jstart >= j0) cur = (isA ? sh.bet[t] : 1.f) * expf(sh.G[t] - sh.G[jstart]);
+    float out[16];
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
-        tc_mma(tmem + COL_D1, sdesc(sbase + OFF_A1 + off, 16, 1024), sdesc(sbase + OFF_A1 + off, 16, 1024),
-               id_bf16_kk, s > 0);
-      }
-      tc_commit(&sh.bar_mma);
+    for (int jj = 15; jj >= 0; --jj) {
+      const int j = j0 + jj;
+      const bool in = (j <= jstart) && (j >= lo);
+      out[jj] = in ? cur * x[jj] : 0.f;
+      if (j <= jstart) cur *= ev[jj];
     }
-    // (3) beta gamma K -> BGK, beta V in place (while MMA1 reads K and Q).
-    for (int i = tid; i < 2048; i += kThreads) {
-      const int r = (i >> 3) & 63, p = i & 7;
-      const bool keep = sh.valid[r] != 0;
-      if (i < 1024) {
-        const int kb = i >> 9;
-        cvt8_store(sm + OFF_BGK + kb * kTile + r * 128 + p * 16, sm + OFF_A1 + kb * 16384 + r * 128 + p * 16,
-                   sh.bet[r] * sh.gam[r], keep);
-      } else {
-        const int vb = (i - 1024) >> 9;
-        uint8_t* ptr = sm + OFF_V + vb * kTile + r * 128 + p * 16;
-        cvt8_store(ptr, ptr, sh.bet[r], keep);
-      }
-    }
-    fence_proxy_async();
-    if (!wait_all(&sh.bar_mma, mma_phase)) {
-      failed = true;
-      break;
-    }
-    mma_phase ^= 1;
-    tc_fence_after();
-
-    // (4) A (fp32, smem) and P (fp16 operand) from D1; Q -> fp16, K -> K~ in place.
-    if (warp < 4) {
-      const int row = tid;
-      float x[32];
-      if (row < 64) {
-        const int t = row;
-        const float Gt = sh.G[t], bt = sh.bet[t];
-        const bool vt = sh.valid[t] != 0;
+    if (isA) {
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          tmem_ld32(lane_addr + COL_D1 + 32 * hh, x);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int j = 32 * hh + i;
-            AM[t * AM_LD + j] = (vt && j < t && sh.valid[j]) ? bt * expf(Gt - sh.G[j]) * x[i] : 0.f;
-          }
-        }
-      } else {
-        const int t = row - 64;
-        const float Gt = sh.G[t];
-        const bool vt = sh.valid[t] != 0;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          tmem_ld32(lane_addr + COL_D1 + 32 * hh, x);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            float pv[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int j = 32 * hh + 8 * q4 + e;
-              pv[e] = (vt && j <= t && sh.valid[j]) ? expf(Gt - sh.G[j]) * x[8 * q4 + e] : 0.f;
-            }
-            uint4 u;
-            u.x = pack_half2(pv[0], pv[1]);
-            u.y = pack_half2(pv[2], pv[3]);
-            u.z = pack_half2(pv[4], pv[5]);
-            u.w = pack_half2(pv[6], pv[7]);
-            *reinterpret_cast<uint4*>(sm + OFF_P + swz(t, 4 * hh + q4)) = u;
-          }
-        }
-      }
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<float4*>(am_chunk(AM, t, (j0 >> 2) + q)) =
+            make_float4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
     } else {
-      for (int i = tid - 128; i < 2048; i += 128) {
-        const int which = i >> 10, j = i & 1023;  // which: 0 = K, 1 = Q
-        const int kb = j >> 9, r = (j >> 3) & 63, p = j & 7;
-        uint8_t* ptr = sm + OFF_A1 + kb * 16384 + which * kTile + r * 128 + p * 16;
-        const bool keep = sh.valid[r] != 0;
-        cvt8_store(ptr, ptr, which ? 1.f : expf(GC - sh.G[r]), keep);
-      }
+      uint8_t* pbuf = sm + OFF_P + (ch & 1) * kTile;
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        *reinterpret_cast<uint4*>(pbuf + swz(t, 2 * quarter + q)) = pack8_half(&out[8 * q]);
     }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-
-    // (5) T = (I + A)^-1 by forward substitution, one column per thread.
-    if (tid < 64) {
-      const int j = tid;
-      float col[64];
+  };
+  // Level 0 of the inverse (threads 0-63): 16x16 diagonal blocks of T = (I + A)^-1,
+  // one column per thread, written in place of A.
+  auto inverse_l0 = [&]() {
+    const int bb = tid >> 4, jj = tid & 15;
+    float x[16];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) col[i] = 0.f;
+    for (int tt = 0; tt < 16; ++tt) {
+      const int row = 16 * bb + tt;
+      float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-      for (int t = 0; t < 64; ++t) {
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < t; i += 4) {
-          const float4 a4 = *reinterpret_cast<const float4*>(&AM[t * AM_LD + i]);
-          acc += a4.x * col[i] + a4.y * col[i + 1] + a4.z * col[i + 2] + a4.w * col[i + 3];
+      for (int m = 0; m < 4; ++m) {
+        if (4 * m < tt) {
+          const float4 a4 = *reinterpret_cast<const float4*>(am_chunk(AM, row, 4 * bb + m));
+          if (4 * m + 0 < tt) acc0 = fmaf(a4.x, x[4 * m + 0], acc0);
+          if (4 * m + 1 < tt) acc1 = fmaf(a4.y, x[4 * m + 1], acc1);
+          if (4 * m + 2 < tt) acc0 = fmaf(a4.z, x[4 * m + 2], acc0);
+          if (4 * m + 3 < tt) acc1 = fmaf(a4.w, x[4 * m + 3], acc1);
         }
-        col[t] = (t == j) ? 1.f : -acc;
       }
-      __half* Th = reinterpret_cast<__half*>(sm + OFF_T);
+      x[tt] = (tt == jj) ? 1.f : (tt > jj ? -(acc0 + acc1) : 0.f);
+    }
+    // every thread of this block read its rows of A before any column is written
+    asm volatile("bar.sync 1, 64;" ::: "memory");
 #pragma unroll
-      for (int t = 0; t < 64; ++t) Th[(swz(t, j >> 3) >> 1) + (j & 7)] = __float2half_rn(col[t]);
+    for (int tt = 0; tt < 16; ++tt) am_at(AM, 16 * bb + tt, 16 * bb + jj) = x[tt];
+  };
+  // Levels 1 and 2 of the inverse, then T' = T diag(beta gamma) and
+  // T'' = T diag(beta) as fp16 operands in the slot.
+  auto inverse_rest = [&](int ch) -> bool {
+    const uint32_t so = slot_off(ch);
+    uint8_t* s = sm + so;
+    // Level 1: T[R][Cb] = -T[R][R] A[R][Cb] T[Cb][Cb] for (R, Cb) = (1, 0), (3, 2);
+    // one output per thread.  The product A[R][Cb] T[Cb][Cb] goes to the unused
+    // block (Cb, R) above the diagonal.
+    {
+      const int pp = tid >> 8, i = (tid >> 4) & 15, j = tid & 15;
+      const int R = 2 * pp + 1, Cb = 2 * pp;
+      const int rowA = 16 * R + i;
+      float y = 0.f;
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const float4 a4 = *reinterpret_cast<const float4*>(am_chunk(AM, rowA, 4 * Cb + k4));
+        y = fmaf(a4.x, am_at(AM, 16 * Cb + 4 * k4 + 0, 16 * Cb + j), y);
+        y = fmaf(a4.y, am_at(AM, 16 * Cb + 4 * k4 + 1, 16 * Cb + j), y);
+        y = fmaf(a4.z, am_at(AM, 16 * Cb + 4 * k4 + 2, 16 * Cb + j), y);
+        y = fmaf(a4.w, am_at(AM, 16 * Cb + 4 * k4 + 3, 16 * Cb + j), y);
+      }
+      __syncthreads();
+      am_at(AM, 16 * Cb + i, 16 * R + j) = y;
+      __syncthreads();
+      float z = 0.f;
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const float4 t4 = *reinterpret_cast<const float4*>(am_chunk(AM, rowA, 4 * R + k4));
+        z = fmaf(t4.x, am_at(AM, 16 * Cb + 4 * k4 + 0, 16 * R + j), z);
+        z = fmaf(t4.y, am_at(AM, 16 * Cb + 4 * k4 + 1, 16 * R + j), z);
+        z = fmaf(t4.z, am_at(AM, 16 * Cb + 4 * k4 + 2, 16 * R + j), z);
+        z = fmaf(t4.w, am_at(AM, 16 * Cb + 4 * k4 + 3, 16 * R + j), z);
+      }
+      am_at(AM, rowA, 16 * Cb + j) = -z;
+    }
+    __syncthreads();
+    // Level 2 on the tensor core: rows 32-63 of T (cols 0-31) = -T22 (A21 T11).
+    // M16 (slot Q0): rows 0-31 = [T11 | 0], rows 32-63 = [A21 | T22], fp16 K-major.
+    // Only the lower triangle (j <= r) is taken: the level-1 scratch blocks sit
+    // above the diagonal.
+    {
+      const int r = tid >> 3, c = tid & 7;
+      uint4 u = make_uint4(0u, 0u, 0u, 0u);
+      if (r >= 32 || c < 4) {
+        const float4 f0 = *reinterpret_cast<const float4*>(am_chunk(AM, r, 2 * c));
+        const float4 f1 = *reinterpret_cast<const float4*>(am_chunk(AM, r, 2 * c + 1));
+        float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (8 * c + e > r) f[e] = 0.f;
+        u = pack8_half(f);
+      }
+      *reinterpret_cast<uint4*>(s + SL_Q0 + swz(r, c)) = u;
     }
     fence_proxy_async();
     __syncthreads();
-
-    // (6) MMA2: W^T = (beta gamma K)^T T^T,  U~^T = (beta V)^T T^T.
     if (tid == 0) {
       tc_fence_after();
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const uint64_t bd = sdesc(sbase + OFF_T + s * 32, 16, 1024);
-        tc_mma(tmem + COL_WT, sdesc(sbase + OFF_BGK + s * 2048, kTile, 1024), bd, id_mnA, s > 0);
-        tc_mma(tmem + COL_UT, sdesc(sbase + OFF_V + s * 2048, kTile, 1024), bd, id_mnA, s > 0);
-      }
-      tc_commit(&sh.bar_mma);
+      tc_mma2(tmem + COL_L2, dK(so + SL_Q0 + 32 * 128), 2, dMN(so + SL_Q0, kTile), 128, id_mnB64, 0);
+      tc_commit(&sh.bar_l2);
     }
-    if (!wait_all(&sh.bar_mma, mma_phase)) {
-      failed = true;
-      break;
-    }
-    mma_phase ^= 1;
+    if (!wait_bar(&sh.bar_l2, ph_l2)) return false;
+    ph_l2 ^= 1;
     tc_fence_after();
-
-    // (7) W^T -> fp16 operand, rows k.
-    {
-      float x[32];
-      tmem_ld32(lane_addr + COL_WT + 32 * khalf, x);
+    if ((warp & 3) == 0) {  // TMEM lanes 0-31 = rows of A21 T11; -Y -> Y16 rows k (MN-major B)
+      float y[16];
+      tmem_ld16(tmem + COL_L2 + 16 * quarter, y);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint4 u;
-        u.x = pack_half2(x[8 * q4], x[8 * q4 + 1]);
-        u.y = pack_half2(x[8 * q4 + 2], x[8 * q4 + 3]);
-        u.z = pack_half2(x[8 * q4 + 4], x[8 * q4 + 5]);
-        u.w = pack_half2(x[8 * q4 + 6], x[8 * q4 + 7]);
-        *reinterpret_cast<uint4*>(sm + OFF_WT + swz(v_row, 4 * khalf + q4)) = u;
-      }
+      for (int q = 0; q < 16; ++q) y[q] = -y[q];
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        *reinterpret_cast<uint4*>(s + SL_Q1 + swz(lane, 2 * quarter + q)) = pack8_half(&y[8 * q]);
     }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
-
-    // (8) X1 = S0 W^T, X2 = S0 Q^T.
     if (tid == 0) {
       tc_fence_after();
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t koff = (s >> 2) * 16384 + (s & 3) * 32;
-        const uint64_t ad = sdesc(sbase + OFF_S + koff, 16, 1024);
-        tc_mma(tmem + COL_X1, ad, sdesc(sbase + OFF_WT + s * 2048, kTile, 1024), id_mnB64, s > 0);
-        tc_mma(tmem + COL_X2, ad, sdesc(sbase + OFF_A1 + koff + kTile, 16, 1024), id_kk64, s > 0);
-      }
-      tc_commit(&sh.bar_mma);
+      tc_mma2(tmem + COL_L2, dK(so + SL_Q0 + 32 * 128 + 64), 2, dMN(so + SL_Q1, kTile), 128, id_mnB64, 0);
+      tc_commit(&sh.bar_l2);
     }
-    if (!wait_all(&sh.bar_mma, mma_phase)) {
-      failed = true;
-      break;
-    }
-    mma_phase ^= 1;
+    if (!wait_bar(&sh.bar_l2, ph_l2)) return false;
+    ph_l2 ^= 1;
     tc_fence_after();
-
-    // (9) U^T = U~^T - X1 -> fp16 operand, rows v.
-    {
-      float xu[32], xw[32];
-      tmem_ld32(lane_addr + COL_UT + 32 * khalf, xu);
-      tmem_ld32(lane_addr + COL_X1 + 32 * khalf, xw);
+    if ((warp & 3) == 0 && quarter < 2) {
+      float d[16];
+      tmem_ld16(tmem + COL_L2 + 16 * quarter, d);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint4 u;
-        u.x = pack_half2(xu[8 * q4] - xw[8 * q4], xu[8 * q4 + 1] - xw[8 * q4 + 1]);
-        u.y = pack_half2(xu[8 * q4 + 2] - xw[8 * q4 + 2], xu[8 * q4 + 3] - xw[8 * q4 + 3]);
-        u.z = pack_half2(xu[8 * q4 + 4] - xw[8 * q4 + 4], xu[8 * q4 + 5] - xw[8 * q4 + 5]);
-        u.w = pack_half2(xu[8 * q4 + 6] - xw[8 * q4 + 6], xu[8 * q4 + 7] - xw[8 * q4 + 7]);
-        *reinterpret_cast<uint4*>(sm + OFF_U + swz(v_row, 4 * khalf + q4)) = u;
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<float4*>(am_chunk(AM, 32 + lane, 4 * quarter + q)) =
+            make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
+    }
+    tc_fence_before();
+    __syncthreads();
+    // T' and T'' (lower triangle incl. diagonal; zeros above): 8 columns per thread.
+    {
+      const int t = tid >> 3, q8 = tid & 7;
+      float tv[8], s1[8], s2[8];
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const float4 f = *reinterpret_cast<const float4*>(am_chunk(AM, t, 2 * q8 + m));
+        const float4 a1 = *reinterpret_cast<const float4*>(&sh.sT1[8 * q8 + 4 * m]);
+        const float4 a2 = *reinterpret_cast<const float4*>(&sh.bet[8 * q8 + 4 * m]);
+        tv[4 * m] = f.x; tv[4 * m + 1] = f.y; tv[4 * m + 2] = f.z; tv[4 * m + 3] = f.w;
+        s1[4 * m] = a1.x; s1[4 * m + 1] = a1.y; s1[4 * m + 2] = a1.z; s1[4 * m + 3] = a1.w;
+        s2[4 * m] = a2.x; s2[4 * m + 1] = a2.y; s2[4 * m + 2] = a2.z; s2[4 * m + 3] = a2.w;
       }
+      float o1[8], o2[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const bool keep = (8 * q8 + e) <= t;
+        o1[e] = keep ? tv[e] * s1[e] : 0.f;
+        o2[e] = keep ? tv[e] * s2[e] : 0.f;
+      }
+      *reinterpret_cast<uint4*>(s + SL_Q0 + swz(t, q8)) = pack8_half(o1);
+      *reinterpret_cast<uint4*>(s + SL_Q1 + swz(t, q8)) = pack8_half(o2);
+    }
+    fence_proxy_async();
+    __syncthreads();
+    return true;
+  };
+  // K~ = diag(exp(G_C - G)) K from the fp16 K of the slot.
+  auto build_kt = [&](int ch) {
+    const uint8_t* src = sm + slot_off(ch) + SL_K0;
+    const float sc = sh.ksc[cr];
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb) {
+      uint4 u = *reinterpret_cast<const uint4*>(src + kb * 16384 + coff);
+      u.x = scale_half2(u.x, sc);
+      u.y = scale_half2(u.y, sc);
+      u.z = scale_half2(u.z, sc);
+      u.w = scale_half2(u.w, sc);
+      *reinterpret_cast<uint4*>(sm + OFF_KT + kb * kTile + coff) = u;
+    }
+  };
+
+  // ---- MMA batches (thread 0) ----
+  auto issue_mma1 = [&](int ch) {  // D1 = [K;Q] K^T (bf16 from TMA)
+    const uint32_t so = slot_off(ch);
+    tc_mma4(tmem + COL_D1, dK(so), 2, dK(so), 2, id_bf16_kk, 0);
+    tc_mma4(tmem + COL_D1, dK(so + 16384), 2, dK(so + 16384), 2, id_bf16_kk, 1);
+    tc_commit(&sh.bar_1);
+  };
+  auto issue_mma2 = [&](int ch) {  // W^T = K^T T'^T, U~^T = V^T T''^T
+    const uint32_t so = slot_off(ch);
+    tc_mma4(tmem + COL_WT, dMN(so + SL_K0, 16384), 128, dK(so + SL_Q0), 2, id_mnA, 0);
+    tc_mma4(tmem + COL_UT, dMN(so + SL_V0, kTile), 128, dK(so + SL_Q1), 2, id_mnA, 0);
+    tc_commit(&sh.bar_2);
+  };
+  auto issue_x = [&]() {  // X1 = S0 W^T, O = S0 Q~^T
+    const uint64_t aS = dK(OFF_S);
+    tc_mma4(tmem + COL_X1, aS, 2, dMN(OFF_WT, kTile), 128, id_mnB64, 0);
+    tc_mma4(tmem + COL_X1, aS + 1024, 2, dMN(OFF_WT + 8192, kTile), 128, id_mnB64, 1);
+    tc_mma4(tmem + COL_O, aS, 2, dK(OFF_QT), 2, id_kk64, 0);
+    tc_mma4(tmem + COL_O, aS + 1024, 2, dK(OFF_QT + kTile), 2, id_kk64, 1);
+    tc_commit(&sh.bar_x);
+  };
+  auto issue_su = [&](int c) {  // SU = U^T K~, O += U^T P^T
+    const uint64_t aU = dK(OFF_U);
+    tc_mma4(tmem + COL_SU, aU, 2, dMN(OFF_KT, kTile), 128, id_mnB128, 0);
+    tc_mma4(tmem + COL_O, aU, 2, dK(OFF_P + (c & 1) * kTile), 2, id_kk64, 1);
+    tc_commit(&sh.bar_s);
+  };
+
+  // ------------------------------------------------------------ prologue ----
+  if (tid == 0) {
+    issue_tma(0);
+    if (nchunks > 1) issue_tma(1);
+  }
+  prefetch_gates(0);
+  float gamC = 1.f;
+  do {
+    if (!wait_bar(&sh.bar_tma[0], 0)) { failed = true; break; }
+    gates();
+    cvt_tile(SL_V0, kTile, SL_V0, kTile, 1.f, row_ok(0));
+    if (tid == 0) {
+      tc_fence_after();
+      issue_mma1(0);
+    }
+    __syncthreads();
+    cvt_tile(OFF_QT, kTile, SL_Q0, 16384, sh.gam[cr], row_ok(0));
+    if (!wait_bar(&sh.bar_1, ph_1)) { failed = true; break; }
+    ph_1 ^= 1;
+    tc_fence_after();
+    build_AP(0);
+    cvt_tile(SL_K0, 16384, SL_K0, 16384, 1.f, row_ok(0));
+    tc_fence_before();
+    __syncthreads();
+    if (tid < 64) inverse_l0();
+    __syncthreads();
+    if (!inverse_rest(0)) { failed = true; break; }
+    if (tid == 0) {
+      tc_fence_after();
+      issue_mma2(0);
+    }
+    build_kt(0);
+    if (!wait_bar(&sh.bar_2, ph_2)) { failed = true; break; }
+    ph_2 ^= 1;
+    tc_fence_after();
+    {
+      float x[16];
+      tmem_ld16(lane_addr + COL_WT + 16 * quarter, x);
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        *reinterpret_cast<uint4*>(sm + OFF_WT + swz(v_row, 2 * quarter + q)) = pack8_half(&x[8 * q]);
+    }
+    gamC = sh.gam[63];
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+  } while (0);
+
+  // ---------------------------------------------------------------- loop ----
+  // Iteration c runs the state chain of chunk c and the prep of chunk p = c+1.
+  // A tcgen05.ld waits for every MMA issued before it, so each TMEM read comes
+  // right after the batch it needs, with shared-memory-only work in between.
+  for (int c = 0; c < nchunks && !failed; ++c) {
+    const int p = c + 1;
+    const bool has_p = p < nchunks;
+    const uint32_t sop = slot_off(p);
+    // [A] TMA two chunks ahead; chain MMAs X1 = S0 W^T, O = S0 Q~^T.
+    if (tid == 0) {
+      if (c + 2 < nchunks) issue_tma(c + 2);
+      tc_fence_after();
+      issue_x();
+    }
+    if (has_p) prefetch_gates(p);
+    // [B] prep p (shared memory only): gates, V -> fp16, K~ source rows.
+    if (has_p) {
+      if (!wait_bar(&sh.bar_tma[p & 1], (p >> 1) & 1)) { failed = true; break; }
+      gates();
+      cvt_tile(sop + SL_V0, kTile, sop + SL_V0, kTile, 1.f, row_ok(p));
+      __syncthreads();
+    }
+    // [C] chain c: U = U~ - X1; then SU = U^T K~, O += U^T P^T and MMA1 of p.
+    if (!wait_bar(&sh.bar_x, ph_x)) { failed = true; break; }
+    ph_x ^= 1;
+    tc_fence_after();
+    {
+      float xu[16], xw[16];
+      tmem_ld16(lane_addr + COL_UT + 16 * quarter, xu);
+      tmem_ld16(lane_addr + COL_X1 + 16 * quarter, xw);
+#pragma unroll
+      for (int q = 0; q < 16; ++q) xu[q] -= xw[q];
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        *reinterpret_cast<uint4*>(sm + OFF_U + swz(v_row, 2 * quarter + q)) = pack8_half(&xu[8 * q]);
     }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
-
-    // (10) SU = U^T K~ (state update), Y = U^T P^T (intra-chunk outputs).
     if (tid == 0) {
       tc_fence_after();
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const uint64_t ad = sdesc(sbase + OFF_U + s * 32, 16, 1024);
-        tc_mma(tmem + COL_SU, ad, sdesc(sbase + OFF_A1 + s * 2048, 16384, 1024), id_mnB128, s > 0);
-        tc_mma(tmem + COL_Y, ad, sdesc(sbase + OFF_P + s * 32, 16, 1024), id_kk64, s > 0);
-      }
-      tc_commit(&sh.bar_mma);
+      issue_su(c);
+      if (has_p) issue_mma1(p);
     }
-    if (!wait_all(&sh.bar_mma, mma_phase)) {
-      failed = true;
-      break;
-    }
-    mma_phase ^= 1;
+    // [C'] prep p (shared memory only, X(c) has finished reading Q~): Q~ of p.
+    if (has_p) cvt_tile(OFF_QT, kTile, sop + SL_Q0, 16384, sh.gam[cr], row_ok(p));
+    // [F1] chain c: S <- gamma_C S + SU (registers), outputs into the U tile.
+    if (!wait_bar(&sh.bar_s, ph_s)) { failed = true; break; }
+    ph_s ^= 1;
     tc_fence_after();
-
-    // (11) S <- gamma_C S + SU; outputs; checkpoint.
     {
       float x[32];
+      tmem_ld32(lane_addr + COL_SU + 32 * quarter, x);
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        tmem_ld32(lane_addr + COL_SU + 64 * khalf + 32 * hh, x);
+      for (int i = 0; i < 32; ++i) S[i] = fmaf(gamC, S[i], x[i]);
+      float y[16];
+      tmem_ld16(lane_addr + COL_O + 16 * quarter, y);
+      __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + OFF_U);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) S[32 * hh + i] = gamC * S[32 * hh + i] + x[i];
+      for (int i = 0; i < 16; ++i) ost[(16 * quarter + i) * 128 + v_row] = __float2bfloat16_rn(a.scale * y[i]);
+    }
+    // [D] prep p: A and P from MMA1, K -> fp16 in place.
+    if (has_p) {
+      if (!wait_bar(&sh.bar_1, ph_1)) { failed = true; break; }
+      ph_1 ^= 1;
+      tc_fence_after();
+      build_AP(p);
+      cvt_tile(sop + SL_K0, 16384, sop + SL_K0, 16384, 1.f, row_ok(p));
+    }
+    tc_fence_before();
+    __syncthreads();
+    // [E0] inverse level 0 (threads 0-63) || output rows of chunk c (the others).
+    {
+      if (has_p && tid < 64) {
+        inverse_l0();
+      } else if (tid >= 64) {
+        const int lo = chunk_lo(c), hi = chunk_hi(c);
+        const int64_t tstride = static_cast<int64_t>(H) * kDimV;
+        __nv_bfloat16* obase = a.o + (static_cast<int64_t>(chunk_tf(c)) * H + h) * kDimV;
+        const __nv_bfloat16* ost = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_U);
+        for (int i = tid - 64; i < 1024; i += kThreads - 64) {
+          const int r = i >> 4, part = i & 15;
+          if (r >= lo && r < hi)
+            *reinterpret_cast<uint4*>(obase + r * tstride + part * 8) =
+                *reinterpret_cast<const uint4*>(ost + r * 128 + part * 8);
+        }
       }
-      stage_state();
-      float x2[32], y[32];
-      tmem_ld32(lane_addr + COL_X2 + 32 * khalf, x2);
-      tmem_ld32(lane_addr + COL_Y + 32 * khalf, y);
-      __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + OFF_AM);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int t = 32 * khalf + i;
-        ost[t * 128 + v_row] = __float2bfloat16_rn(a.scale * (sh.gam[t] * x2[i] + y[i]));
+    }
+    __syncthreads();
+    stage_state();  // S16 for chunk c+1 (X(c) finished reading it)
+    // [E] prep p: inverse levels 1-2, T', T''; then MMA2.
+    if (has_p) {
+      if (!inverse_rest(p)) { failed = true; break; }
+      if (tid == 0) {
+        tc_fence_after();
+        issue_mma2(p);
       }
-      const int a_end = a0 + kChunk;
+    }
+    // [G1] while MMA2 runs: checkpoint of chunk c, K~ of p (SU(c) has finished).
+    {
+      const int a_end = chunk_a0(c) + kChunk;
       if (ck_rows && ck_pool && a_end % N == 0 && a_end <= end_pos) {
         const int row = ck_rows[a_end / N - 1 - first_ck];
         if (row >= 0) store_state(ck_pool, row);
       }
     }
+    float gamC_next = gamC;
+    if (has_p) {
+      build_kt(p);
+      // [G2] W^T of p -> fp16 rows k.
+      if (!wait_bar(&sh.bar_2, ph_2)) { failed = true; break; }
+      ph_2 ^= 1;
+      tc_fence_after();
+      float x[16];
+      tmem_ld16(lane_addr + COL_WT + 16 * quarter, x);
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        *reinterpret_cast<uint4*>(sm + OFF_WT + swz(v_row, 2 * quarter + q)) = pack8_half(&x[8 * q]);
+      gamC_next = sh.gam[63];
+    }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
-
-    // (12) Output rows of this chunk that belong to the sequence.
-    {
-      const __nv_bfloat16* ost = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_AM);
-      for (int i = tid; i < 64 * 16; i += kThreads) {
-        const int r = i >> 4, p = i & 15;
-        const int pos = a0 + r;
-        if (pos >= P && pos < end_pos) {
-          const int64_t t = static_cast<int64_t>(t_first) + r;
-          *reinterpret_cast<uint4*>(a.o + (t * H + h) * kDimV + p * 8) =
-              *reinterpret_cast<const uint4*>(ost + r * 128 + p * 8);
-        }
-      }
-    }
-    __syncthreads();
+    gamC = gamC_next;
   }
 
   if (failed) {
