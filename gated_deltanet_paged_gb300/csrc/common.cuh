@@ -59,6 +59,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As above, but the thread may be suspended in the instruction for up to
+// ~1 ms while the phase is incomplete (no busy polling).
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -70,9 +84,9 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer_ns() - t0 > 2000000000ull) return false;
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > 2000000000ull) return false;
   }
 }
 
@@ -164,6 +178,41 @@ __device__ __forceinline__ void tc_mma2(uint32_t d, uint64_t a, uint32_t astep, 
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %3, %5, p;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %5, q;\n\t}\n" ::"r"(d),
       "l"(a), "l"(static_cast<uint64_t>(astep)), "l"(b), "l"(static_cast<uint64_t>(bstep)), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+
+// Same with the A operand in TMEM (lane m = row m, column c = elements 2c and
+// 2c+1 of the K dimension, fp16/bf16 pairs); astep in TMEM columns.
+__device__ __forceinline__ void tc_mma4_ts(uint32_t d, uint32_t a_tmem, uint32_t astep, uint64_t b, uint32_t bstep,
+                                           uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 q, %6, %6;\n\t"
+      "add.u32 a1, %1, %2;\n\tadd.u32 a2, a1, %2;\n\tadd.u32 a3, a2, %2;\n\t"
+      "add.s64 b1, %3, %4;\n\tadd.s64 b2, b1, %4;\n\tadd.s64 b3, b2, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %3, %5, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %5, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %5, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %5, q;\n\t}\n" ::"r"(d),
+      "r"(a_tmem), "r"(astep), "l"(b), "l"(static_cast<uint64_t>(bstep)), "r"(idesc), "r"(acc0)
+      : "memory");
+}
+
+// Store 16 (8) consecutive 32-bit columns of this thread's TMEM lane and wait.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
       : "memory");
 }
 

@@ -17,7 +17,7 @@
 //   S1      = gamma_C S0 + U^T diag(exp(G_C - G_j)) K
 // which equals the token-by-token recurrence up to rounding.
 //
-// Mapping.  One CTA (256 threads) per chain, chains ordered by decreasing
+// Mapping.  One CTA (512 threads) per chain, chains ordered by decreasing
 // length.  Per chunk the work splits into a state-independent "prep" (TMA of
 // Q/K/V, gates, [K;Q]K^T, A and P, the inverse T, W^T and U~^T) and the state
 // "chain" (S0 W^T and S0 Q~^T, U, U^T K~ and U^T P^T, the state update and the
@@ -29,12 +29,14 @@
 //     TMA; everything else on fp16 operands (11-bit significand keeps written
 //     states within 1e-3 relative error; bf16 would not).
 //   - decay factors exp(G_t - G_j) come from running products of exp(g).
-//   - T = (I + A)^-1: 16x16 diagonal blocks by forward substitution, the 16->32
-//     merges T10 = -T11 A10 T00 on CUDA cores, the 32->64 merge as two MMAs.
+//   - T = (I + A)^-1: the 16x16 diagonal blocks T_d by forward substitution on
+//     CUDA cores, the rest as three MMAs: N = -T_d A_o (A_o the block-lower
+//     part of A, N^4 = 0), T = (I + N)(I + N^2) T_d = Z + N^2 Z with
+//     Z = (I + N) T_d.
 //   - beta gamma and beta fold into the columns of T (T', T''), gamma into Q~
 //     and exp(G_C - G) into K~, so O = scale (S0 Q~^T + U P^T) is one
 //     accumulator and S1 = gamma_C S0 + U^T K~.
-//   - the fp32 state lives in registers (thread = state row v, half of K) and is
+//   - the fp32 state lives in registers (thread = state row v, 32 columns) and is
 //     restaged as the fp16 MMA operand every chunk; page-boundary and final
 //     states go from registers to the pool.
 #include <math.h>
@@ -51,30 +53,31 @@ constexpr uint32_t kTile = 8192;  // 64 rows x 128 B
 // Slot: the raw TMA tiles of one chunk (two slots), converted in place.
 constexpr uint32_t SLOT_BYTES = 49152;
 constexpr uint32_t SL_K0 = 0;      // K cols 0-63   -> K fp16 (MN-major A of W^T)
-constexpr uint32_t SL_Q0 = 8192;   // Q cols 0-63   -> M16 (merge operands) -> T' fp16
+constexpr uint32_t SL_Q0 = 8192;   // Q cols 0-63   -> A_o, N^2 (inverse operands) -> T' fp16
 constexpr uint32_t SL_K1 = 16384;  // K cols 64-127 -> K fp16
-constexpr uint32_t SL_Q1 = 24576;  // Q cols 64-127 -> Y16 (merge operand) -> T'' fp16
+constexpr uint32_t SL_Q1 = 24576;  // Q cols 64-127 -> Z (inverse operand) -> T'' fp16
 constexpr uint32_t SL_V0 = 32768;  // V cols 0-63   -> V fp16 (MN-major A of U~^T)
 constexpr uint32_t SL_V1 = 40960;  // V cols 64-127 -> V fp16
 // Other tiles (byte offsets from the 1024-aligned base).
-constexpr uint32_t OFF_QT = 2 * SLOT_BYTES;  // Q~ = diag(gamma) Q fp16 [kb0 | kb1], rows t
-constexpr uint32_t OFF_KT = OFF_QT + 16384;  // K~ = diag(exp(G_C - G)) K fp16 [kb0 | kb1], rows t
-constexpr uint32_t OFF_P = OFF_KT + 16384;   // P fp16, two buffers, rows t
-constexpr uint32_t OFF_WT = OFF_P + 16384;   // W^T fp16 rows k; also the fp32 A -> T matrix
-constexpr uint32_t OFF_U = OFF_WT + 16384;   // U^T fp16 rows v
-constexpr uint32_t OFF_S = OFF_U + 16384;    // S fp16 [kb0 | kb1], rows v
-constexpr uint32_t OFF_SMALL = OFF_S + 32768;
+constexpr uint32_t OFF_FREE = 2 * SLOT_BYTES;  // 16 KB scratch (sequence ranking at start-up)
+constexpr uint32_t OFF_KT = OFF_FREE + 16384;  // K~ = diag(exp(G_C - G)) K fp16 [kb0 | kb1], rows t
+constexpr uint32_t OFF_P = OFF_KT + 16384;     // P fp16, two buffers, rows t
+constexpr uint32_t OFF_WT = OFF_P + 16384;     // inverse scratch: fp32 A / T_d, then N | T_d (fp16)
+constexpr uint32_t OFF_U = OFF_WT + 16384;     // output / state staging for coalesced stores
+constexpr uint32_t OFF_XB = OFF_U + 16384;     // [W | Q~] fp16 per 64-column block: the B operand of S0 [W; Q~]^T
+constexpr uint32_t OFF_SMALL = OFF_XB + 32768;
 constexpr uint32_t SMEM_USED = OFF_SMALL + 2048;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
 
 // TMEM columns (fp32, 128 lanes).
-constexpr uint32_t COL_D1 = 0;    // [K;Q]K^T
-constexpr uint32_t COL_WT = 64;   // W^T   (lane = k)
-constexpr uint32_t COL_UT = 128;  // U~^T  (lane = v)
-constexpr uint32_t COL_X1 = 192;  // S0 W^T
-constexpr uint32_t COL_O = 256;   // S0 Q~^T + U^T P^T
-constexpr uint32_t COL_SU = 320;  // U^T K~ (128 cols)
-constexpr uint32_t COL_L2 = 448;  // 32->64 merge products of the inverse
+constexpr uint32_t COL_D1 = 0;     // [K;Q]K^T, then the inverse's products (cols 0-127)
+constexpr uint32_t COL_WT = 64;    // W^T   (lane = k)
+constexpr uint32_t COL_U = 64;     // U^T as the fp16 A operand (32 cols; free between W^T uses)
+constexpr uint32_t COL_UT = 128;   // U~^T  (lane = v)
+constexpr uint32_t COL_X1 = 192;   // S0 W^T       } one N = 128 product
+constexpr uint32_t COL_O = 256;    // S0 Q~^T      } + U^T P^T accumulated later
+constexpr uint32_t COL_SU = 320;   // U^T K~ (128 cols)
+constexpr uint32_t COL_S16 = 448;  // S0 as the fp16 A operand (64 cols)
 constexpr uint32_t TMEM_COLS = 512;
 
 struct PrefillArgs {
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- pick the sequence: rank-th longest (ties by index) ----
   if (a.num_seqs > 1 && a.num_seqs < 4096) {
-    int* cu_s = reinterpret_cast<int*>(sm + OFF_QT);
+    int* cu_s = reinterpret_cast<int*>(sm + OFF_FREE);
     for (int i = tid; i <= a.num_seqs; i += kThreads) cu_s[i] = a.cu_seqlens[i];
     if (tid == 0) sh.seq = -1;
     __syncthreads();
@@ -296,11 +299,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int i = 0; i < 32; ++i) S[i] = 0.f;
   }
-  auto stage_state = [&]() {  // fp16 copy of S as the MMA operand
+  auto stage_state = [&]() {  // fp16 copy of S as the TMEM A operand
+    uint32_t w[16];
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      *reinterpret_cast<uint4*>(sm + OFF_S + (quarter >> 1) * 16384 + swz(v_row, 4 * (quarter & 1) + c)) =
-          pack8_half(&S[8 * c]);
+    for (int c = 0; c < 16; ++c) w[c] = pack_half2(S[2 * c], S[2 * c + 1]);
+    tmem_st16(lane_addr + COL_S16 + 16 * quarter, w);
   };
   // Store the fp32 state to a pool row with coalesced 16-byte stores, staging
   // 32 state rows (16 KB) at a time in the U tile (free whenever this runs).
@@ -336,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t id_mnB64 = idesc_f16(128, 64, false, false, false, true);
   const uint32_t id_kk64 = idesc_f16(128, 64, false, false, false, false);
   const uint32_t id_mnB128 = idesc_f16(128, 128, false, false, false, true);
+  const uint32_t id_kk128 = idesc_f16(128, 128, false, false, false, false);
 
   // Geometry of chunk ch: absolute position of row 0, valid rows [lo, hi),
   // packed token index of row 0.
@@ -414,40 +418,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     cvt8_store(sm + dst + dblk + coff, sm + src + sblk + coff, sc, keep);
   };
   auto row_ok = [&](int ch) { return cr >= chunk_lo(ch) && cr < chunk_hi(ch); };
-  // A (fp32, AM) from K K^T rows, P (fp16 operand) from Q K^T rows; decay
-  // factors by running products exp(G_t - G_{j-1}) = exp(G_t - G_j) exp(g_j).
+  // The same conversion spread over warps 1-15 only (warp 0 is issuing MMAs).
+  auto cvt_tile_w = [&](int ch, uint32_t dst, uint32_t dblk, uint32_t src, uint32_t sblk, const float* rsc) {
+    if (warp == 0) return;
+    const int lo = chunk_lo(ch), hi = chunk_hi(ch);
+    for (int i = tid - 32; i < 1024; i += kThreads - 32) {
+      const int kb = i >> 9, r = (i & 511) >> 3;
+      const uint32_t o = static_cast<uint32_t>(i & 511) * 16u;
+      cvt8_store(sm + dst + kb * dblk + o, sm + src + kb * sblk + o, rsc ? rsc[r] : 1.f, r >= lo && r < hi);
+    }
+  };
+  // A from K K^T rows: the diagonal 16x16 blocks in fp32 (AM, for level 0 of
+  // the inverse), the strictly block-lower part as an fp16 operand (slot Q0,
+  // diagonal blocks zero); P (fp16 operand) from Q K^T rows.  Decay factors by
+  // running products exp(G_t - G_{j-1}) = exp(G_t - G_j) exp(g_j).
   auto build_AP = [&](int ch) {
     const int lo = chunk_lo(ch), hi = chunk_hi(ch);
     const int j0 = 16 * quarter;
-    float x[16], ev[16];
-    tmem_ld16(lane_addr + COL_D1 + j0, x);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 e4 = *reinterpret_cast<const float4*>(&sh.e[j0 + 4 * q]);
-      ev[4 * q] = e4.x;
-      ev[4 * q + 1] = e4.y;
-      ev[4 * q + 2] = e4.z;
-      ev[4 * q + 3] = e4.w;
-    }
     const int t = v_row & 63;
-    const bool vt = t >= lo && t < hi;
     const bool isA = v_row < 64;
+    float x[16];
+    tmem_ld16(lane_addr + COL_D1 + j0, x);
     const int jstart = min(j0 + 15, isA ? t - 1 : t);  // last column kept (j < t for A, j <= t for P)
-    float cur = 0.f;
-    if (vt && jstart >= j0) cur = (isA ? sh.bet[t] : 1.f) * expf(sh.G[t] - sh.G[jstart]);
     float out[16];
+    if (t >= lo && t < hi && jstart >= j0) {
+      float ev[16];
 #pragma unroll
-    for (int jj = 15; jj >= 0; --jj) {
-      const int j = j0 + jj;
-      const bool in = (j <= jstart) && (j >= lo);
-      out[jj] = in ? cur * x[jj] : 0.f;
-      if (j <= jstart) cur *= ev[jj];
+      for (int q = 0; q < 4; ++q) {
+        const float4 e4 = *reinterpret_cast<const float4*>(&sh.e[j0 + 4 * q]);
+        ev[4 * q] = e4.x;
+        ev[4 * q + 1] = e4.y;
+        ev[4 * q + 2] = e4.z;
+        ev[4 * q + 3] = e4.w;
+      }
+      float cur = (isA ? sh.bet[t] : 1.f) * expf(sh.G[t] - sh.G[jstart]);
+      if (jstart == j0 + 15 && lo <= j0) {  // whole block inside: no masks
+#pragma unroll
+        for (int jj = 15; jj >= 0; --jj) {
+          out[jj] = cur * x[jj];
+          cur *= ev[jj];
+        }
+      } else {
+#pragma unroll
+        for (int jj = 15; jj >= 0; --jj) {
+          const int j = j0 + jj;
+          const bool in = (j <= jstart) && (j >= lo);
+          out[jj] = in ? cur * x[jj] : 0.f;
+          if (j <= jstart) cur *= ev[jj];
+        }
+      }
+    } else {
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) out[jj] = 0.f;
     }
     if (isA) {
+      const bool diag = (t >> 4) == quarter;
+      if (diag) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<float4*>(am_chunk(AM, t, (j0 >> 2) + q)) =
-            make_float4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<float4*>(am_chunk(AM, t, (j0 >> 2) + q)) =
+              make_float4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+      }
+      uint8_t* ao = sm + slot_off(ch) + SL_Q0;
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        *reinterpret_cast<uint4*>(ao + swz(t, 2 * quarter + q)) =
+            diag ? make_uint4(0u, 0u, 0u, 0u) : pack8_half(&out[8 * q]);
     } else {
       uint8_t* pbuf = sm + OFF_P + (ch & 1) * kTile;
 #pragma unroll
@@ -455,165 +491,189 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(pbuf + swz(t, 2 * quarter + q)) = pack8_half(&out[8 * q]);
     }
   };
-  // Level 0 of the inverse (threads 0-63): 16x16 diagonal blocks of T = (I + A)^-1,
-  // one column per thread, written in place of A.
+  // Level 0 of the inverse (threads 0-63): T_d = the 16x16 diagonal blocks of
+  // (I + A)^-1, one column per thread by forward substitution; then T_d as an
+  // fp16 tile (rows t, zeros outside the diagonal blocks) at OFF_WT + 8 KB.
   auto inverse_l0 = [&]() {
     const int bb = tid >> 4, jj = tid & 15;
     float x[16];
 #pragma unroll
     for (int tt = 0; tt < 16; ++tt) {
       const int row = 16 * bb + tt;
-      float acc0 = 0.f, acc1 = 0.f;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         if (4 * m < tt) {
           const float4 a4 = *reinterpret_cast<const float4*>(am_chunk(AM, row, 4 * bb + m));
-          if (4 * m + 0 < tt) acc0 = fmaf(a4.x, x[4 * m + 0], acc0);
-          if (4 * m + 1 < tt) acc1 = fmaf(a4.y, x[4 * m + 1], acc1);
-          if (4 * m + 2 < tt) acc0 = fmaf(a4.z, x[4 * m + 2], acc0);
-          if (4 * m + 3 < tt) acc1 = fmaf(a4.w, x[4 * m + 3], acc1);
+          if (4 * m + 0 < tt) acc[0] = fmaf(a4.x, x[4 * m + 0], acc[0]);
+          if (4 * m + 1 < tt) acc[1] = fmaf(a4.y, x[4 * m + 1], acc[1]);
+          if (4 * m + 2 < tt) acc[2] = fmaf(a4.z, x[4 * m + 2], acc[2]);
+          if (4 * m + 3 < tt) acc[3] = fmaf(a4.w, x[4 * m + 3], acc[3]);
         }
       }
-      x[tt] = (tt == jj) ? 1.f : (tt > jj ? -(acc0 + acc1) : 0.f);
+      x[tt] = (tt == jj) ? 1.f : (tt > jj ? -((acc[0] + acc[1]) + (acc[2] + acc[3])) : 0.f);
     }
-    // every thread of this block read its rows of A before any column is written
-    asm volatile("bar.sync 1, 64;" ::: "memory");
+    asm volatile("bar.sync 1, 64;" ::: "memory");  // all of A's diagonal blocks read
 #pragma unroll
     for (int tt = 0; tt < 16; ++tt) am_at(AM, 16 * bb + tt, 16 * bb + jj) = x[tt];
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+    {
+      // Row t of T_d (its diagonal block) into registers first: the fp16 tile
+      // overlaps rows 32-63 of the fp32 scratch that other threads still read.
+      const int t = tid, blk = t >> 4;
+      float f[16];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float4 v4 = *reinterpret_cast<const float4*>(am_chunk(AM, t, 4 * blk + m));
+        f[4 * m] = v4.x;
+        f[4 * m + 1] = v4.y;
+        f[4 * m + 2] = v4.z;
+        f[4 * m + 3] = v4.w;
+      }
+      asm volatile("bar.sync 1, 64;" ::: "memory");
+      uint8_t* td = sm + OFF_WT + kTile;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if ((c >> 1) == blk) u = pack8_half(&f[8 * (c & 1)]);
+        *reinterpret_cast<uint4*>(td + swz(t, c)) = u;
+      }
+    }
+    fence_proxy_async();  // T_d is an MMA operand
   };
-  // Levels 1 and 2 of the inverse, then T' = T diag(beta gamma) and
-  // T'' = T diag(beta) as fp16 operands in the slot.
+  // Rest of the inverse on the tensor core.  With N = -T_d A_o (A_o = the
+  // strictly block-lower part of A; N^4 = 0):
+  //   T = (I + N + N^2 + N^3) T_d = Z + N^2 Z,   Z = (I + N) T_d.
+  // Round 1: N = -T_d A_o.  Round 2: [N^2 | N T_d] = N [N | T_d] -> Z, N^2.
+  // Round 3: T = Z + N^2 Z -> T' = T diag(beta gamma), T'' = T diag(beta).
+  // The 64-row products occupy TMEM lanes 0-63; warps 0,1,4,5,8,9,12,13 read
+  // them (16 columns each).  Tiles: T_d at OFF_WT + 8 KB, N at OFF_WT (so
+  // [N | T_d] is one MN-major operand), A_o / N^2 / T' at slot Q0, Z / T'' at
+  // slot Q1.
   auto inverse_rest = [&](int ch) -> bool {
     const uint32_t so = slot_off(ch);
     uint8_t* s = sm + so;
-    // Level 1: T[R][Cb] = -T[R][R] A[R][Cb] T[Cb][Cb] for (R, Cb) = (1, 0), (3, 2);
-    // one output per thread.  The product A[R][Cb] T[Cb][Cb] goes to the unused
-    // block (Cb, R) above the diagonal.
-    {
-      const int pp = tid >> 8, i = (tid >> 4) & 15, j = tid & 15;
-      const int R = 2 * pp + 1, Cb = 2 * pp;
-      const int rowA = 16 * R + i;
-      float y = 0.f;
-#pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
-        const float4 a4 = *reinterpret_cast<const float4*>(am_chunk(AM, rowA, 4 * Cb + k4));
-        y = fmaf(a4.x, am_at(AM, 16 * Cb + 4 * k4 + 0, 16 * Cb + j), y);
-        y = fmaf(a4.y, am_at(AM, 16 * Cb + 4 * k4 + 1, 16 * Cb + j), y);
-        y = fmaf(a4.z, am_at(AM, 16 * Cb + 4 * k4 + 2, 16 * Cb + j), y);
-        y = fmaf(a4.w, am_at(AM, 16 * Cb + 4 * k4 + 3, 16 * Cb + j), y);
-      }
-      __syncthreads();
-      am_at(AM, 16 * Cb + i, 16 * R + j) = y;
-      __syncthreads();
-      float z = 0.f;
-#pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
-        const float4 t4 = *reinterpret_cast<const float4*>(am_chunk(AM, rowA, 4 * R + k4));
-        z = fmaf(t4.x, am_at(AM, 16 * Cb + 4 * k4 + 0, 16 * R + j), z);
-        z = fmaf(t4.y, am_at(AM, 16 * Cb + 4 * k4 + 1, 16 * R + j), z);
-        z = fmaf(t4.z, am_at(AM, 16 * Cb + 4 * k4 + 2, 16 * R + j), z);
-        z = fmaf(t4.w, am_at(AM, 16 * Cb + 4 * k4 + 3, 16 * R + j), z);
-      }
-      am_at(AM, rowA, 16 * Cb + j) = -z;
-    }
-    __syncthreads();
-    // Level 2 on the tensor core: rows 32-63 of T (cols 0-31) = -T22 (A21 T11).
-    // M16 (slot Q0): rows 0-31 = [T11 | 0], rows 32-63 = [A21 | T22], fp16 K-major.
-    // Only the lower triangle (j <= r) is taken: the level-1 scratch blocks sit
-    // above the diagonal.
-    {
-      const int r = tid >> 3, c = tid & 7;
-      uint4 u = make_uint4(0u, 0u, 0u, 0u);
-      if (r >= 32 || c < 4) {
-        const float4 f0 = *reinterpret_cast<const float4*>(am_chunk(AM, r, 2 * c));
-        const float4 f1 = *reinterpret_cast<const float4*>(am_chunk(AM, r, 2 * c + 1));
-        float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (8 * c + e > r) f[e] = 0.f;
-        u = pack8_half(f);
-      }
-      *reinterpret_cast<uint4*>(s + SL_Q0 + swz(r, c)) = u;
-    }
-    fence_proxy_async();
-    __syncthreads();
+    const bool rt = (warp & 3) < 2;       // this thread reads TMEM lanes 0-63
+    const int t = v_row;                  // its row (valid when rt)
+    const uint32_t lrow = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    // Round 1.
     if (tid == 0) {
       tc_fence_after();
-      tc_mma2(tmem + COL_L2, dK(so + SL_Q0 + 32 * 128), 2, dMN(so + SL_Q0, kTile), 128, id_mnB64, 0);
+      tc_mma4(tmem + COL_D1, dK(OFF_WT + kTile), 2, dMN(so + SL_Q0, kTile), 128, id_mnB64, 0);
       tc_commit(&sh.bar_l2);
     }
     if (!wait_bar(&sh.bar_l2, ph_l2)) return false;
     ph_l2 ^= 1;
     tc_fence_after();
-    if ((warp & 3) == 0) {  // TMEM lanes 0-31 = rows of A21 T11; -Y -> Y16 rows k (MN-major B)
-      float y[16];
-      tmem_ld16(tmem + COL_L2 + 16 * quarter, y);
+    if (rt) {
+      float d[16];
+      tmem_ld16(lrow + COL_D1 + 16 * quarter, d);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) y[q] = -y[q];
+      for (int q = 0; q < 16; ++q) d[q] = -d[q];
 #pragma unroll
       for (int q = 0; q < 2; ++q)
-        *reinterpret_cast<uint4*>(s + SL_Q1 + swz(lane, 2 * quarter + q)) = pack8_half(&y[8 * q]);
+        *reinterpret_cast<uint4*>(sm + OFF_WT + swz(t, 2 * quarter + q)) = pack8_half(&d[8 * q]);
     }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
+    // Round 2.
     if (tid == 0) {
       tc_fence_after();
-      tc_mma2(tmem + COL_L2, dK(so + SL_Q0 + 32 * 128 + 64), 2, dMN(so + SL_Q1, kTile), 128, id_mnB64, 0);
+      tc_mma4(tmem + COL_D1, dK(OFF_WT), 2, dMN(OFF_WT, kTile), 128, id_mnB128, 0);
       tc_commit(&sh.bar_l2);
     }
     if (!wait_bar(&sh.bar_l2, ph_l2)) return false;
     ph_l2 ^= 1;
     tc_fence_after();
-    if ((warp & 3) == 0 && quarter < 2) {
-      float d[16];
-      tmem_ld16(tmem + COL_L2 + 16 * quarter, d);
+    float z[16];
+    if (rt) {
+      float n2[16], nt[16];
+      tmem_ld16(lrow + COL_D1 + 16 * quarter, n2);
+      tmem_ld16(lrow + COL_D1 + 64 + 16 * quarter, nt);
+      const uint8_t* td = sm + OFF_WT + kTile;
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<float4*>(am_chunk(AM, 32 + lane, 4 * quarter + q)) =
-            make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
-    }
-    tc_fence_before();
-    __syncthreads();
-    // T' and T'' (lower triangle incl. diagonal; zeros above): 8 columns per thread.
-    {
-      const int t = tid >> 3, q8 = tid & 7;
-      float tv[8], s1[8], s2[8];
+      for (int q = 0; q < 2; ++q) {
+        const uint4 u = *reinterpret_cast<const uint4*>(td + swz(t, 2 * quarter + q));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        const float4 f = *reinterpret_cast<const float4*>(am_chunk(AM, t, 2 * q8 + m));
-        const float4 a1 = *reinterpret_cast<const float4*>(&sh.sT1[8 * q8 + 4 * m]);
-        const float4 a2 = *reinterpret_cast<const float4*>(&sh.bet[8 * q8 + 4 * m]);
-        tv[4 * m] = f.x; tv[4 * m + 1] = f.y; tv[4 * m + 2] = f.z; tv[4 * m + 3] = f.w;
-        s1[4 * m] = a1.x; s1[4 * m + 1] = a1.y; s1[4 * m + 2] = a1.z; s1[4 * m + 3] = a1.w;
-        s2[4 * m] = a2.x; s2[4 * m + 1] = a2.y; s2[4 * m + 2] = a2.z; s2[4 * m + 3] = a2.w;
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+          z[8 * q + 2 * e] = f.x + nt[8 * q + 2 * e];
+          z[8 * q + 2 * e + 1] = f.y + nt[8 * q + 2 * e + 1];
+        }
       }
-      float o1[8], o2[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const bool keep = (8 * q8 + e) <= t;
-        o1[e] = keep ? tv[e] * s1[e] : 0.f;
-        o2[e] = keep ? tv[e] * s2[e] : 0.f;
+      for (int q = 0; q < 2; ++q) {
+        *reinterpret_cast<uint4*>(s + SL_Q0 + swz(t, 2 * quarter + q)) = pack8_half(&n2[8 * q]);
+        *reinterpret_cast<uint4*>(s + SL_Q1 + swz(t, 2 * quarter + q)) = pack8_half(&z[8 * q]);
       }
-      *reinterpret_cast<uint4*>(s + SL_Q0 + swz(t, q8)) = pack8_half(o1);
-      *reinterpret_cast<uint4*>(s + SL_Q1 + swz(t, q8)) = pack8_half(o2);
     }
     fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    // Round 3.
+    if (tid == 0) {
+      tc_fence_after();
+      tc_mma4(tmem + COL_D1, dK(so + SL_Q0), 2, dMN(so + SL_Q1, kTile), 128, id_mnB64, 0);
+      tc_commit(&sh.bar_l2);
+    }
+    if (!wait_bar(&sh.bar_l2, ph_l2)) return false;
+    ph_l2 ^= 1;
+    tc_fence_after();
+    if (rt) {
+      float d[16], o1[16], o2[16];
+      tmem_ld16(lrow + COL_D1 + 16 * quarter, d);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 a1 = *reinterpret_cast<const float4*>(&sh.sT1[16 * quarter + 4 * q]);
+        const float4 a2 = *reinterpret_cast<const float4*>(&sh.bet[16 * quarter + 4 * q]);
+        const float s1[4] = {a1.x, a1.y, a1.z, a1.w}, s2[4] = {a2.x, a2.y, a2.z, a2.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float tv = z[4 * q + e] + d[4 * q + e];
+          o1[4 * q + e] = tv * s1[e];
+          o2[4 * q + e] = tv * s2[e];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        *reinterpret_cast<uint4*>(s + SL_Q0 + swz(t, 2 * quarter + q)) = pack8_half(&o1[8 * q]);
+        *reinterpret_cast<uint4*>(s + SL_Q1 + swz(t, 2 * quarter + q)) = pack8_half(&o2[8 * q]);
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
     __syncthreads();
     return true;
   };
-  // K~ = diag(exp(G_C - G)) K from the fp16 K of the slot.
-  auto build_kt = [&](int ch) {
-    const uint8_t* src = sm + slot_off(ch) + SL_K0;
-    const float sc = sh.ksc[cr];
+  // W (rows t, K-major) from W^T in TMEM (lane k): element (t, k) of this
+  // thread's 16 columns t goes to block k / 64 of the [W | Q~] operand.
+  auto write_w = [&]() {
+    float x[16];
+    tmem_ld16(lane_addr + COL_WT + 16 * quarter, x);
+    const int k = v_row, kb = k >> 6, kk = k & 63;
+    __half* wb = reinterpret_cast<__half*>(sm + OFF_XB + kb * 16384);
 #pragma unroll
-    for (int kb = 0; kb < 2; ++kb) {
-      uint4 u = *reinterpret_cast<const uint4*>(src + kb * 16384 + coff);
+    for (int i = 0; i < 16; ++i) {
+      const int t = 16 * quarter + i;
+      wb[(swz(t, kk >> 3) >> 1) + (kk & 7)] = __float2half_rn(x[i]);
+    }
+  };
+  // K~ = diag(exp(G_C - G)) K from the fp16 K of the slot.
+  auto build_kt = [&](int ch) {  // warps 1-15 (warp 0 is issuing MMA2)
+    if (warp == 0) return;
+    const uint8_t* src = sm + slot_off(ch) + SL_K0;
+    for (int i = tid - 32; i < 1024; i += kThreads - 32) {
+      const int kb = i >> 9, r = (i & 511) >> 3;
+      const uint32_t o = static_cast<uint32_t>(i & 511) * 16u;
+      const float sc = sh.ksc[r];
+      uint4 u = *reinterpret_cast<const uint4*>(src + kb * 16384 + o);
       u.x = scale_half2(u.x, sc);
       u.y = scale_half2(u.y, sc);
       u.z = scale_half2(u.z, sc);
       u.w = scale_half2(u.w, sc);
-      *reinterpret_cast<uint4*>(sm + OFF_KT + kb * kTile + coff) = u;
+      *reinterpret_cast<uint4*>(sm + OFF_KT + kb * kTile + o) = u;
     }
   };
 
@@ -630,18 +690,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_mma4(tmem + COL_UT, dMN(so + SL_V0, kTile), 128, dK(so + SL_Q1), 2, id_mnA, 0);
     tc_commit(&sh.bar_2);
   };
-  auto issue_x = [&]() {  // X1 = S0 W^T, O = S0 Q~^T
-    const uint64_t aS = dK(OFF_S);
-    tc_mma4(tmem + COL_X1, aS, 2, dMN(OFF_WT, kTile), 128, id_mnB64, 0);
-    tc_mma4(tmem + COL_X1, aS + 1024, 2, dMN(OFF_WT + 8192, kTile), 128, id_mnB64, 1);
-    tc_mma4(tmem + COL_O, aS, 2, dK(OFF_QT), 2, id_kk64, 0);
-    tc_mma4(tmem + COL_O, aS + 1024, 2, dK(OFF_QT + kTile), 2, id_kk64, 1);
+  auto issue_x = [&]() {  // [X1 | O] = S0 [W; Q~]^T  (A = S0 from TMEM)
+    tc_mma4_ts(tmem + COL_X1, tmem + COL_S16, 8, dK(OFF_XB), 2, id_kk128, 0);
+    tc_mma4_ts(tmem + COL_X1, tmem + COL_S16 + 32, 8, dK(OFF_XB + 16384), 2, id_kk128, 1);
     tc_commit(&sh.bar_x);
   };
-  auto issue_su = [&](int c) {  // SU = U^T K~, O += U^T P^T
-    const uint64_t aU = dK(OFF_U);
-    tc_mma4(tmem + COL_SU, aU, 2, dMN(OFF_KT, kTile), 128, id_mnB128, 0);
-    tc_mma4(tmem + COL_O, aU, 2, dK(OFF_P + (c & 1) * kTile), 2, id_kk64, 1);
+  auto issue_su = [&](int c) {  // SU = U^T K~, O += U^T P^T  (A = U from TMEM)
+    tc_mma4_ts(tmem + COL_SU, tmem + COL_U, 8, dMN(OFF_KT, kTile), 128, id_mnB128, 0);
+    tc_mma4_ts(tmem + COL_O, tmem + COL_U, 8, dK(OFF_P + (c & 1) * kTile), 2, id_kk64, 1);
     tc_commit(&sh.bar_s);
   };
 
@@ -661,12 +717,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       issue_mma1(0);
     }
     __syncthreads();
-    cvt_tile(OFF_QT, kTile, SL_Q0, 16384, sh.gam[cr], row_ok(0));
+    cvt_tile(OFF_XB + kTile, 16384, SL_Q0, 16384, sh.gam[cr], row_ok(0));
     if (!wait_bar(&sh.bar_1, ph_1)) { failed = true; break; }
     ph_1 ^= 1;
     tc_fence_after();
     build_AP(0);
     cvt_tile(SL_K0, 16384, SL_K0, 16384, 1.f, row_ok(0));
+    fence_proxy_async();
     tc_fence_before();
     __syncthreads();
     if (tid < 64) inverse_l0();
@@ -681,11 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ph_2 ^= 1;
     tc_fence_after();
     {
-      float x[16];
-      tmem_ld16(lane_addr + COL_WT + 16 * quarter, x);
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-        *reinterpret_cast<uint4*>(sm + OFF_WT + swz(v_row, 2 * quarter + q)) = pack8_half(&x[8 * q]);
+      write_w();
     }
     gamC = sh.gam[63];
     fence_proxy_async();
@@ -712,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (has_p) {
       if (!wait_bar(&sh.bar_tma[p & 1], (p >> 1) & 1)) { failed = true; break; }
       gates();
-      cvt_tile(sop + SL_V0, kTile, sop + SL_V0, kTile, 1.f, row_ok(p));
+      cvt_tile_w(p, sop + SL_V0, kTile, sop + SL_V0, kTile, nullptr);
       __syncthreads();
     }
     // [C] chain c: U = U~ - X1; then SU = U^T K~, O += U^T P^T and MMA1 of p.
@@ -723,11 +776,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       float xu[16], xw[16];
       tmem_ld16(lane_addr + COL_UT + 16 * quarter, xu);
       tmem_ld16(lane_addr + COL_X1 + 16 * quarter, xw);
+      uint32_t w[8];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) xu[q] -= xw[q];
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-        *reinterpret_cast<uint4*>(sm + OFF_U + swz(v_row, 2 * quarter + q)) = pack8_half(&xu[8 * q]);
+      for (int q = 0; q < 8; ++q) w[q] = pack_half2(xu[2 * q] - xw[2 * q], xu[2 * q + 1] - xw[2 * q + 1]);
+      tmem_st8(lane_addr + COL_U + 8 * quarter, w);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -738,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (has_p) issue_mma1(p);
     }
     // [C'] prep p (shared memory only, X(c) has finished reading Q~): Q~ of p.
-    if (has_p) cvt_tile(OFF_QT, kTile, sop + SL_Q0, 16384, sh.gam[cr], row_ok(p));
+    if (has_p) cvt_tile_w(p, OFF_XB + kTile, 16384, sop + SL_Q0, 16384, sh.gam);
     // [F1] chain c: S <- gamma_C S + SU (registers), outputs into the U tile.
     if (!wait_bar(&sh.bar_s, ph_s)) { failed = true; break; }
     ph_s ^= 1;
@@ -761,6 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       build_AP(p);
       cvt_tile(sop + SL_K0, 16384, sop + SL_K0, 16384, 1.f, row_ok(p));
+      fence_proxy_async();
     }
     tc_fence_before();
     __syncthreads();
@@ -782,7 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncthreads();
-    stage_state();  // S16 for chunk c+1 (X(c) finished reading it)
+    stage_state();  // S0 of chunk c+1 into TMEM (X(c) finished reading it)
     // [E] prep p: inverse levels 1-2, T', T''; then MMA2.
     if (has_p) {
       if (!inverse_rest(p)) { failed = true; break; }
@@ -806,11 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_bar(&sh.bar_2, ph_2)) { failed = true; break; }
       ph_2 ^= 1;
       tc_fence_after();
-      float x[16];
-      tmem_ld16(lane_addr + COL_WT + 16 * quarter, x);
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-        *reinterpret_cast<uint4*>(sm + OFF_WT + swz(v_row, 2 * quarter + q)) = pack8_half(&x[8 * q]);
+      write_w();
       gamC_next = sh.gam[63];
     }
     fence_proxy_async();
