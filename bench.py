@@ -68,7 +68,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
         return self
@@ -161,6 +161,10 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
     prefill_flops = T * H * FLOP_PER_TOKEN_HEAD
     slot_out = gdn.gdn_paged_prefill_slots(pre.cu_seqlens, pre.page_indptr, pre.page_indices, pre.last_page_len,
                                            pre.page_size)
+    # Workspace of the chunk-local phase (one 64 x 64 fp16 tile per chunk and
+    # head), allocated once outside the timed region like any caller would.
+    ws = torch.empty(gdn.gdn_prefill_workspace_bytes(pre.cu_seqlens.numel() - 1, T, H), dtype=torch.uint8,
+                     device=dev)
 
     def prefill_step(ev=None):
         gdn.gdn_paged_prefill_slots(pre.cu_seqlens, pre.page_indptr, pre.page_indices, pre.last_page_len,
@@ -169,7 +173,7 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
             ev[0].record(stream)
         gdn.gdn_chunk_gated_delta_rule_paged(pre.q, pre.k, pre.v, pre.g, pre.beta, pre.cu_seqlens, pool,
                                              pre.page_indices, pre.page_indptr, pre.page_size, pre.last_page_len,
-                                             scale=SCALE, slots=slot_out, o=o)
+                                             scale=SCALE, slots=slot_out, o=o, workspace=ws)
         if ev is not None:
             ev[1].record(stream)
 
@@ -190,7 +194,7 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
     ms_prefill = max_over_ranks(start.elapsed_time(stop) / args.steps)
     kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
     clocks = clk.summary()
-    launches = 2 * args.steps
+    launches = 4 * args.steps  # slots, slot map, chunk-local inverse, state chain
 
     # ---- e2e: host buffers, copies inside the timed region ----
     e2e = None
@@ -206,7 +210,7 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
                 dbuf[n].copy_(t, non_blocking=True)
             gdn.gdn_chunk_gated_delta_rule_paged(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"],
                                                  pre.cu_seqlens, pool, pre.page_indices, pre.page_indptr,
-                                                 pre.page_size, pre.last_page_len, scale=SCALE, o=o)
+                                                 pre.page_size, pre.last_page_len, scale=SCALE, o=o, workspace=ws)
             host_o.copy_(o, non_blocking=True)
 
         e2e_step()
@@ -223,7 +227,7 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
         ms_e2e = max_over_ranks(start.elapsed_time(stop) / e2e_steps)
         e2e = {"value": T * world / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
-        launches += e2e_steps + 1
+        launches += 3 * (e2e_steps + 1)  # slot map, chunk-local inverse, state chain
         del host, host_o, dbuf
 
     value = T * world / (ms_prefill * 1e-3)
@@ -249,7 +253,8 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
                    "tokens_per_step": T, "l2": "inputs larger than L2 (streamed q/k/v/o per step), no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": None, "kernel": "prefill_kernel", "kernel_ms": kernel_ms,
+                     "traffic": None, "kernel": "paged prefill call (slot map + chunk-local inverse + state chain)",
+                     "kernel_ms": kernel_ms,
                      "algorithmic_bytes": prefill_bytes, "peak_kind": peak_kind},
         "tensor": {"achieved_tflops": prefill_flops / (kernel_ms * 1e-3) / 1e12, "peak_tflops": bf16,
                    "frac": prefill_flops / (kernel_ms * 1e-3) / 1e12 / bf16, "flops_per_launch": prefill_flops},
@@ -279,7 +284,7 @@ def _bench_decode(args, gdn, workloads, dev, stream, barrier, max_over_ranks, ra
         if ev is not None:
             ev[1].record(stream)
 
-    dsteps = max(args.steps, 20)
+    dsteps = max(args.steps, 200)
     for _ in range(max(args.warmup, 3)):
         decode_step()
     dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(dsteps)]
@@ -390,7 +395,7 @@ def run_reference(args, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)

@@ -64,14 +64,14 @@ def library():
                 except Exception as e:  # no silent fallback: the CUDA library is the product
                     raise RuntimeError("libgdn_paged.so is missing or stale and could not be built: %s" % e)
             lib = ctypes.CDLL(LIB_PATH)
-            P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+            P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
             sig = {
                 "gdn_paged_prefill_slots": [P, P, P, P, i32, i32, P, P, P, P, P],
                 "gdn_paged_decode_slots": [P, P, P, i32, P, P, P],
                 "gdn_chunk_gated_delta_rule": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32,
-                                               P, P, P, P, P, P, P, P, i32, i64, P, P],
+                                               P, P, P, P, P, P, P, P, i32, i64, P, sz, P, P],
                 "gdn_chunk_gated_delta_rule_paged": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32,
-                                                     P, i32, P, P, i32, P, P, P, P],
+                                                     P, i32, P, P, i32, P, P, P, sz, P, P],
                 "gdn_gated_delta_rule_decode_paged": [P, P, P, P, P, P, i32, i32, i32, i32, f32,
                                                       P, i32, P, P, P, P, P, P],
             }
@@ -161,6 +161,18 @@ def gdn_paged_decode_slots(page_indptr, page_indices, last_page_len, out=None):
     return out
 
 
+def _workspace(workspace, num_seqs, T, H, device):
+    """The prefill workspace: the caller's uint8 tensor (checked for size) or a
+    fresh one from the torch caching allocator."""
+    need = gdn_prefill_workspace_bytes(num_seqs, T, H)
+    if workspace is None:
+        return torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+    _need(workspace, torch.uint8, "workspace")
+    if workspace.numel() < need:
+        raise ValueError("workspace holds %d bytes, the call needs %d" % (workspace.numel(), need))
+    return workspace
+
+
 def _tokens(q, k, v, g, beta):
     _need(q, torch.bfloat16, "q", 3)
     _need(k, torch.bfloat16, "k", 3)
@@ -178,9 +190,11 @@ def gdn_chunk_gated_delta_rule(q, k, v, g, beta, cu_seqlens, *, scale=0.0, initi
                                state_indices=None, output_state=None, output_state_indices=None,
                                state_checkpoints=None, checkpoint_state_indices=None,
                                checkpoint_cu_starts=None, prefix_lens=None, checkpoint_every_n_tokens=0,
-                               o=None, err_word=None):
+                               o=None, err_word=None, workspace=None):
     """Chunked prefill with slot arguments (explicit read / final / checkpoint
-    rows).  Returns o (bf16 [T, H, V]); pools are updated in place."""
+    rows).  Returns o (bf16 [T, H, V]); pools are updated in place.
+    ``workspace``: optional uint8 device tensor of at least
+    gdn_prefill_workspace_bytes(num_seqs, T, H) bytes."""
     T, H, K, V = _tokens(q, k, v, g, beta)
     _need(cu_seqlens, torch.int32, "cu_seqlens")
     f32, i32 = torch.float32, torch.int32
@@ -193,20 +207,24 @@ def gdn_chunk_gated_delta_rule(q, k, v, g, beta, cu_seqlens, *, scale=0.0, initi
     if o is None:
         o = torch.empty(T, H, V, dtype=torch.bfloat16, device=q.device)
     _need(o, torch.bfloat16, "o", 3)
+    ws = _workspace(workspace, cu_seqlens.numel() - 1, T, H, q.device)
     _check("gdn_chunk_gated_delta_rule", library().gdn_chunk_gated_delta_rule(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(o), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, H,
         K, V, float(scale), _ptr(pools[0]), _ptr(_opt(state_indices, i32, "state_indices")), _ptr(pools[1]),
         _ptr(_opt(output_state_indices, i32, "output_state_indices")), _ptr(pools[2]),
         _ptr(_opt(checkpoint_state_indices, i32, "checkpoint_state_indices")),
         _ptr(_opt(checkpoint_cu_starts, i32, "checkpoint_cu_starts")), _ptr(_opt(prefix_lens, i32, "prefix_lens")),
-        int(checkpoint_every_n_tokens), stride, _ptr(_opt(err_word, i32, "err_word")), _stream(q)))
+        int(checkpoint_every_n_tokens), stride, _ptr(ws), ws.numel(), _ptr(_opt(err_word, i32, "err_word")),
+        _stream(q)))
     return o
 
 
 def gdn_chunk_gated_delta_rule_paged(q, k, v, g, beta, cu_seqlens, state_pool, page_indices, page_indptr,
-                                     page_size, last_page_len, *, scale=0.0, slots=None, o=None, err_word=None):
+                                     page_size, last_page_len, *, scale=0.0, slots=None, o=None, err_word=None,
+                                     workspace=None):
     """Paged chunked prefill over state_pool [num_pages, H, V, K].  ``slots``:
-    the dict returned by gdn_paged_prefill_slots (optional).  Returns o."""
+    the dict returned by gdn_paged_prefill_slots (optional).  ``workspace``:
+    optional uint8 device tensor (see gdn_prefill_workspace_bytes).  Returns o."""
     T, H, K, V = _tokens(q, k, v, g, beta)
     i32 = torch.int32
     _need(cu_seqlens, i32, "cu_seqlens")
@@ -216,6 +234,7 @@ def gdn_chunk_gated_delta_rule_paged(q, k, v, g, beta, cu_seqlens, state_pool, p
     if o is None:
         o = torch.empty(T, H, V, dtype=torch.bfloat16, device=q.device)
     _need(o, torch.bfloat16, "o", 3)
+    ws = _workspace(workspace, cu_seqlens.numel() - 1, T, H, q.device)
     sl = None
     if slots is not None:
         sl = _PrefillSlots(*[_ptr(_need(slots[n], i32, n)) for n in
@@ -223,7 +242,7 @@ def gdn_chunk_gated_delta_rule_paged(q, k, v, g, beta, cu_seqlens, state_pool, p
     _check("gdn_chunk_gated_delta_rule_paged", library().gdn_chunk_gated_delta_rule_paged(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(o), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, H,
         K, V, float(scale), _ptr(state_pool), state_pool.shape[0], _ptr(page_indices), _ptr(page_indptr),
-        int(page_size), _ptr(last_page_len), None if sl is None else ctypes.byref(sl),
+        int(page_size), _ptr(last_page_len), None if sl is None else ctypes.byref(sl), _ptr(ws), ws.numel(),
         _ptr(_opt(err_word, i32, "err_word")), _stream(q)))
     return o
 

@@ -54,9 +54,20 @@ int encode_tokens_map(CUtensorMap* map, const void* base, int64_t T, int64_t H, 
   return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_CUDA;
 }
 
-}  // namespace gdn_host
+int encode_tiles_map_f16(CUtensorMap* map, const void* base, int64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return GDN_ERR_CUDA;
+  cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_CUDA;
+}
 
-extern "C" size_t gdn_prefill_workspace_bytes(int32_t, int32_t, int32_t) { return 0; }
+}  // namespace gdn_host
 
 extern "C" const char* gdn_status_string(int status) {
   switch (status) {

@@ -1,4 +1,5 @@
-// prefill.cu -- chunked paged GDN prefill on tcgen05 tensor cores.
+// prefill.cu -- chunked paged GDN prefill on tcgen05 tensor cores: the state
+// chain, plus the C-ABI entry points of the prefill.
 //
 // "flashinfer.gdn_paged": chunk_gated_delta_rule_paged, the prefill bullets,
 // the 64-token left-padding paragraph, and "Slot arguments of
@@ -8,141 +9,92 @@
 // Method (gated delta rule, chunked).  Per (sequence, head) chain and 64-token
 // chunk with rows t = 0..63, cumulative gate G_t = g_0 + ... + g_t (rows outside
 // the sequence have g = beta = 0 and k = v = 0, so they are the identity),
-// gamma_t = exp(G_t), S0 the V x K state at the chunk start:
-//   A[t][j] = beta_t exp(G_t - G_j) (k_t . k_j)      j < t   (strictly lower)
-//   T       = (I + A)^-1
-//   W       = T diag(beta gamma) K,   U~ = T diag(beta) V
-//   U       = U~ - W S0^T                            (the chunk's new values)
-//   O[t]    = scale (gamma_t S0 q_t + sum_{j<=t} exp(G_t - G_j)(q_t . k_j) U[j])
-//   S1      = gamma_C S0 + U^T diag(exp(G_C - G_j)) K
+// gamma_t = exp(G_t), S0 the V x K state at the chunk start and
+// T'' = (I + A)^-1 diag(beta) from the chunk-local kernel (ut.cu):
+//   W     = T'' diag(gamma) K,  U~ = T'' V
+//   U     = U~ - W S0^T                            (the chunk's new values)
+//   O[t]  = scale (gamma_t S0 q_t + sum_{j<=t} exp(G_t - G_j)(q_t . k_j) U[j])
+//   S1    = gamma_C S0 + U^T diag(exp(G_C - G_j)) K
 // which equals the token-by-token recurrence up to rounding.
 //
-// Mapping.  One CTA (512 threads) per chain, chains ordered by decreasing
-// length.  Per chunk the work splits into a state-independent "prep" (TMA of
-// Q/K/V, gates, [K;Q]K^T, A and P, the inverse T, W^T and U~^T) and the state
-// "chain" (S0 W^T and S0 Q~^T, U, U^T K~ and U^T P^T, the state update and the
-// outputs).  The loop runs chain(c) and prep(c+1) in one software-pipelined
-// instruction stream: every tcgen05.mma is followed by CUDA-core work that does
-// not depend on it, so MMA latency hides behind the other half.  TMA runs two
-// chunks ahead into a pair of slots.
-//   - MMAs (M = 128, fp32 accumulators in TMEM): [K;Q]K^T on bf16 straight from
-//     TMA; everything else on fp16 operands (11-bit significand keeps written
-//     states within 1e-3 relative error; bf16 would not).
-//   - decay factors exp(G_t - G_j) come from running products of exp(g).
-//   - T = (I + A)^-1: the 16x16 diagonal blocks T_d by forward substitution on
-//     CUDA cores, the rest as three MMAs: N = -T_d A_o (A_o the block-lower
-//     part of A, N^4 = 0), T = (I + N)(I + N^2) T_d = Z + N^2 Z with
-//     Z = (I + N) T_d.
-//   - beta gamma and beta fold into the columns of T (T', T''), gamma into Q~
-//     and exp(G_C - G) into K~, so O = scale (S0 Q~^T + U P^T) is one
-//     accumulator and S1 = gamma_C S0 + U^T K~.
-//   - the fp32 state lives in registers (thread = state row v, 32 columns) and is
-//     restaged as the fp16 MMA operand every chunk; page-boundary and final
-//     states go from registers to the pool.
+// Mapping.  One CTA (16 warps) per chain, chains ordered by decreasing length;
+// the warps are specialised and hand work to each other through mbarriers:
+//   - warps 0-7, "chain": the fp32 state in registers (thread = state row v,
+//     64 columns), U read back from TMEM, the state update, the outputs and
+//     the page-boundary / final state stores;
+//   - warps 8-14, "prep": everything of chunk c+1 that does not depend on the
+//     state, while the chain works on chunk c: TMA of Q, K, V, T'', gates,
+//     P (decayed, masked Q K^T), W, Q~ = diag(gamma) Q, K~ = diag(exp(G_C - G)) K;
+//   - warp 15, "issuer": every tcgen05.mma, in whatever order the two streams
+//     become ready (chain first).  A thread's MMA issue runs almost in step with
+//     the tensor core, so no warp that has other work issues.
+// Per chunk the MMAs are (M = 128, fp32 accumulators in TMEM):
+//   prep : D_X  = [Q; .] K^T                  (bf16 from TMA; P from rows 0-63)
+//          D_X  = [0; T''] V  or [T''; 0] V   (U~ into the chunk's U rows)
+//          D_W  = [T'; .] K,  T' = T'' diag(gamma)
+//   chain: D_X += [Q~; -W] S0^T or [-W; Q~] S0^T   (U rows: U~ - W S0^T = U;
+//                                                   O rows: Q~ S0^T)
+//          D_SU = U^T K~;  D_X += [P_even; P_odd] U (O rows += P U)
+// D_X alternates between two TMEM buffers and its U / O row halves swap with
+// the chunk parity, so one zero tile serves both forms of [0; T''].  Operands
+// are fp16 (an 11-bit significand keeps written states within 1e-3 relative
+// error; bf16 would not) except Q K^T, which uses the bf16 tiles as loaded.
 #include <math.h>
 
-#include "common.cuh"
+#include "prefill_common.cuh"
 
 namespace {
 
 using namespace gdn;
 
 constexpr int kThreads = 512;
+constexpr int kPrepThreads = 224;  // warps 8-14
+constexpr int kIssuerWarp = 15;
 constexpr uint32_t kTile = 8192;  // 64 rows x 128 B
 
-// Slot: the raw TMA tiles of one chunk (two slots), converted in place.
-constexpr uint32_t SLOT_BYTES = 49152;
-constexpr uint32_t SL_K0 = 0;      // K cols 0-63   -> K fp16 (MN-major A of W^T)
-constexpr uint32_t SL_Q0 = 8192;   // Q cols 0-63   -> A_o, N^2 (inverse operands) -> T' fp16
-constexpr uint32_t SL_K1 = 16384;  // K cols 64-127 -> K fp16
-constexpr uint32_t SL_Q1 = 24576;  // Q cols 64-127 -> Z (inverse operand) -> T'' fp16
-constexpr uint32_t SL_V0 = 32768;  // V cols 0-63   -> V fp16 (MN-major A of U~^T)
-constexpr uint32_t SL_V1 = 40960;  // V cols 64-127 -> V fp16
-// Other tiles (byte offsets from the 1024-aligned base).
-constexpr uint32_t OFF_FREE = 2 * SLOT_BYTES;  // 16 KB scratch (sequence ranking at start-up)
-constexpr uint32_t OFF_KT = OFF_FREE + 16384;  // K~ = diag(exp(G_C - G)) K fp16 [kb0 | kb1], rows t
-constexpr uint32_t OFF_P = OFF_KT + 16384;     // P fp16, two buffers, rows t
-constexpr uint32_t OFF_WT = OFF_P + 16384;     // inverse scratch: fp32 A / T_d, then N | T_d (fp16)
-constexpr uint32_t OFF_U = OFF_WT + 16384;     // output / state staging for coalesced stores
-constexpr uint32_t OFF_XB = OFF_U + 16384;     // [W | Q~] fp16 per 64-column block: the B operand of S0 [W; Q~]^T
-constexpr uint32_t OFF_SMALL = OFF_XB + 32768;
-constexpr uint32_t SMEM_USED = OFF_SMALL + 2048;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
+// Shared memory (byte offsets from the 1024-aligned base).
+constexpr uint32_t OFF_Q = 0;         // Q bf16 [kb0 | kb1] (one chunk)
+constexpr uint32_t OFF_K = 16384;     // 3 x K [kb0 | kb1]: bf16 -> fp16 -> K~, in place
+constexpr uint32_t OFF_V = 65536;     // 2 x V [kb0 | kb1]: bf16 -> fp16, in place
+constexpr uint32_t OFF_TZT = 98304;   // T''(odd chunk) | zero tile | T''(even chunk)
+constexpr uint32_t OFF_P = 122880;    // P (even chunk) | P (odd chunk), rows t, K-major
+constexpr uint32_t OFF_TP = 139264;   // T' = T'' diag(gamma)
+constexpr uint32_t OFF_XA = 147456;   // [Q~; -W] or [-W; Q~], K-major, [kb0 | kb1]
+constexpr uint32_t OFF_S16 = 180224;  // S0 fp16, K-major B (rows v), [kb0 | kb1]
+constexpr uint32_t OFF_U16 = 212992;  // U fp16 [t][v], MN-major, [v 0-63 | v 64-127]
+constexpr uint32_t OFF_SMALL = 229376;
 
-// TMEM columns (fp32, 128 lanes).
-constexpr uint32_t COL_D1 = 0;     // [K;Q]K^T, then the inverse's products (cols 0-127)
-constexpr uint32_t COL_WT = 64;    // W^T   (lane = k)
-constexpr uint32_t COL_U = 64;     // U^T as the fp16 A operand (32 cols; free between W^T uses)
-constexpr uint32_t COL_UT = 128;   // U~^T  (lane = v)
-constexpr uint32_t COL_X1 = 192;   // S0 W^T       } one N = 128 product
-constexpr uint32_t COL_O = 256;    // S0 Q~^T      } + U^T P^T accumulated later
-constexpr uint32_t COL_SU = 320;   // U^T K~ (128 cols)
-constexpr uint32_t COL_S16 = 448;  // S0 as the fp16 A operand (64 cols)
+// TMEM columns.
+constexpr uint32_t COL_DX = 0;     // two 128-column accumulators, by chunk parity
+constexpr uint32_t COL_DW = 256;   // W (rows 0-63)
+constexpr uint32_t COL_DSU = 384;  // U^T K~
 constexpr uint32_t TMEM_COLS = 512;
 
-struct PrefillArgs {
-  const float* g;
-  const float* beta;
-  __nv_bfloat16* o;
-  const int32_t* cu_seqlens;
-  int32_t num_seqs;
-  int32_t T;
-  int32_t H;
-  float scale;
-  const float* initial_state;
-  const int32_t* state_indices;
-  float* output_state;
-  const int32_t* output_state_indices;
-  float* state_checkpoints;
-  const int32_t* checkpoint_state_indices;
-  const int32_t* checkpoint_cu_starts;
-  const int32_t* prefix_lens;
-  int32_t N;
-  int64_t row_stride;
-  // Paged mode without precomputed slots: rows come from the page table.
-  const int32_t* indptr;
-  const int32_t* pages;
-  const int32_t* last_len;
-  int32_t page_size;
-  int32_t num_pages;
-  int32_t* err_word;
+struct Gates {
+  float G[64];  // cumulative gate
+  float e[64];  // exp(g)
 };
 
-// Per-chunk scalars of the chunk being prepared.
 struct Small {
-  float G[64];    // cumulative gate
-  float e[64];    // exp(g)
-  float gam[64];  // exp(G)
-  float bet[64];  // beta (0 outside the sequence)
-  float sT1[64];  // beta * gamma  (column scale of T')
-  float ksc[64];  // exp(G_C - G)  (row scale of K~)
-  uint64_t bar_tma[2];
-  uint64_t bar_x, bar_1, bar_s, bar_2, bar_l2;
+  Gates gates[3];  // ring over chunks
+  // TMA completion
+  uint64_t bar_q, bar_v[2], bar_t[2], bar_k[3];
+  // MMA completion (tcgen05.commit)
+  uint64_t bar_p, bar_m2, bar_x, bar_su, bar_o[2];
+  // hand-offs between warp groups
+  uint64_t xa_full, mp_ready, m2_ready, u_ready, s16_ready, o_read[2];
   uint32_t tmem_base;
   int seq;
   int flag;
+  int abort;
 };
+constexpr uint32_t SMALL_BYTES = ((sizeof(Small) + 127) / 128) * 128;
+// Dynamic shared memory requested: the tiles, the small block and slack to
+// align the base to 1024 B.  Stays below the 227 KB a CTA may use.
+constexpr uint32_t SMEM_BYTES = OFF_SMALL + SMALL_BYTES + 1024;
+static_assert(SMEM_BYTES <= 232448, "prefill shared memory above the per-CTA limit");
 
-__device__ __forceinline__ void cvt8_store(uint8_t* dst, const uint8_t* src_bf16, float sc, bool keep) {
-  uint4 out = make_uint4(0u, 0u, 0u, 0u);
-  if (keep) {
-    const uint4 in = *reinterpret_cast<const uint4*>(src_bf16);
-    float2 f0 = unpack_bf162(in.x), f1 = unpack_bf162(in.y), f2 = unpack_bf162(in.z), f3 = unpack_bf162(in.w);
-    out.x = pack_half2(f0.x * sc, f0.y * sc);
-    out.y = pack_half2(f1.x * sc, f1.y * sc);
-    out.z = pack_half2(f2.x * sc, f2.y * sc);
-    out.w = pack_half2(f3.x * sc, f3.y * sc);
-  }
-  *reinterpret_cast<uint4*>(dst) = out;
-}
-
-__device__ __forceinline__ uint32_t scale_half2(uint32_t u, float sc) {
-  __half2 h = *reinterpret_cast<__half2*>(&u);
-  const float2 f = __half22float2(h);
-  return pack_half2(f.x * sc, f.y * sc);
-}
-
-__device__ __forceinline__ uint4 pack8_half(const float* x) {
+__device__ __forceinline__ uint4 pack8h(const float* x) {
   uint4 u;
   u.x = pack_half2(x[0], x[1]);
   u.y = pack_half2(x[2], x[3]);
@@ -151,20 +103,44 @@ __device__ __forceinline__ uint4 pack8_half(const float* x) {
   return u;
 }
 
-// fp32 64 x 64 matrix, 16-byte chunk cj of row r stored at chunk cj ^ (r % 16).
-__device__ __forceinline__ float* am_chunk(float* AM, int r, int cj) { return AM + r * 64 + ((cj ^ (r & 15)) << 2); }
-__device__ __forceinline__ float& am_at(float* AM, int r, int j) {
-  return AM[r * 64 + ((((j >> 2) ^ (r & 15)) << 2) | (j & 3))];
+__device__ __forceinline__ void unpack8h(uint4 u, float* x) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+
+__device__ __forceinline__ uint32_t scale_half2(uint32_t u, float sc) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u));
+  return pack_half2(f.x * sc, f.y * sc);
+}
+
+// bf16 x 8 -> fp16 x 8 times sc (zeros unless keep); src may equal dst.
+__device__ __forceinline__ void cvt8(uint8_t* dst, const uint8_t* src, float sc, bool keep) {
+  uint4 out = make_uint4(0u, 0u, 0u, 0u);
+  if (keep) {
+    const uint4 in = *reinterpret_cast<const uint4*>(src);
+    const float2 f0 = unpack_bf162(in.x), f1 = unpack_bf162(in.y), f2 = unpack_bf162(in.z), f3 = unpack_bf162(in.w);
+    out.x = pack_half2(f0.x * sc, f0.y * sc);
+    out.y = pack_half2(f1.x * sc, f1.y * sc);
+    out.z = pack_half2(f2.x * sc, f2.y * sc);
+    out.w = pack_half2(f3.x * sc, f3.y * sc);
+  }
+  *reinterpret_cast<uint4*>(dst) = out;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
+                   const PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
   Small& sh = *reinterpret_cast<Small*>(sm + OFF_SMALL);
-  float* AM = reinterpret_cast<float*>(sm + OFF_WT);
+  volatile int* abort_flag = &sh.abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.H;
@@ -172,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- pick the sequence: rank-th longest (ties by index) ----
   if (a.num_seqs > 1 && a.num_seqs < 4096) {
-    int* cu_s = reinterpret_cast<int*>(sm + OFF_FREE);
+    int* cu_s = reinterpret_cast<int*>(sm + OFF_XA);
     for (int i = tid; i <= a.num_seqs; i += kThreads) cu_s[i] = a.cu_seqlens[i];
     if (tid == 0) sh.seq = -1;
     __syncthreads();
@@ -206,11 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n = i1 - i0;
     const int lpl = a.last_len[b];
     const long long tot = static_cast<long long>(n - 1) * a.page_size + lpl;
-    P = static_cast<int>(tot - L);
-    if (n < 1 || lpl < 1 || lpl > a.page_size || tot < L) {
+    if (n < 1 || lpl < 1 || lpl > a.page_size || tot < L || tot > 0x3FFFFFFFLL) {
       if (tid == 0) record_error(a.err_word, GDN_DEVERR_PAGE_TABLE, b);
       return;
     }
+    P = static_cast<int>(tot - L);
     in_row = P > 0 ? a.pages[i0 + (P - 1) / a.page_size] : -1;
     out_row = a.pages[i1 - 1];
     ck_rows = a.pages + i0 + P / a.page_size;
@@ -233,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     in_row = a.state_indices ? a.state_indices[b] : -1;
     out_row = a.output_state_indices ? a.output_state_indices[b] : -1;
     if (a.state_checkpoints) ck_rows = a.checkpoint_state_indices + a.checkpoint_cu_starts[b];
-    if (P < 0) {
+    if (P < 0 || static_cast<long long>(P) + L > 0x3FFFFFFFLL) {
       if (tid == 0) record_error(a.err_word, GDN_DEVERR_PAGE_TABLE, b);
       return;
     }
@@ -248,98 +224,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!init_pool) in_row = -1;
   if (!out_pool) out_row = -1;
 
-  // ---- set-up: barriers, TMEM ----
+  const int end_pos = P + L;
+  const int first_pos = (P / kChunk) * kChunk;
+  const int nch = chunk_count(P, L);
+  const int first_ck = (ck_rows && N > 0) ? P / N : 0;
+  const int slot0 = slot_base(cu_b, b);
+
+  // ---- set-up: barriers, TMEM, the zero tile ----
   if (tid == 0) {
-    mbar_init(&sh.bar_tma[0], 1);
-    mbar_init(&sh.bar_tma[1], 1);
+    mbar_init(&sh.bar_q, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.bar_v[i], 1);
+      mbar_init(&sh.bar_t[i], 1);
+      mbar_init(&sh.bar_o[i], 1);
+      mbar_init(&sh.o_read[i], 128);
+    }
+    for (int i = 0; i < 3; ++i) mbar_init(&sh.bar_k[i], 1);
+    mbar_init(&sh.bar_p, 1);
+    mbar_init(&sh.bar_m2, 1);
     mbar_init(&sh.bar_x, 1);
-    mbar_init(&sh.bar_1, 1);
-    mbar_init(&sh.bar_s, 1);
-    mbar_init(&sh.bar_2, 1);
-    mbar_init(&sh.bar_l2, 1);
+    mbar_init(&sh.bar_su, 1);
+    mbar_init(&sh.xa_full, 1);
+    mbar_init(&sh.mp_ready, 1);
+    mbar_init(&sh.m2_ready, 1);
+    mbar_init(&sh.u_ready, 128);
+    mbar_init(&sh.s16_ready, 256);
+    sh.abort = 0;
     fence_mbar_init();
-    prefetch_tensormap(&tm_q);
-    prefetch_tensormap(&tm_k);
-    prefetch_tensormap(&tm_v);
   }
   if (warp == 0) {
     tmem_alloc(&sh.tmem_base, TMEM_COLS);
     tmem_relinquish();
   }
+  reinterpret_cast<uint4*>(sm + OFF_TZT + kTile)[tid] = make_uint4(0u, 0u, 0u, 0u);  // 512 x 16 B
+  fence_proxy_async();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
-
-  // Thread roles: v_row = state row / TMEM lane (0..127), quarter = which 32
-  // state columns (and which quarter of a 64-column accumulator) it handles.
-  // For tile conversions every thread owns row cr = tid / 8, 16-byte chunk
-  // tid % 8, in both 64-column blocks (byte offset tid * 16 in a block).
-  const int v_row = tid & 127;
-  const int quarter = tid >> 7;
-  const int cr = tid >> 3;
-  const uint32_t coff = static_cast<uint32_t>(tid) * 16u;
-  const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-  const int64_t head_off = static_cast<int64_t>(h) * kDimV * kDimK;
-
-  // ---- initial state: pool row or literal zeros (the pool is never scaled by 0) ----
-  float S[32];
-  if (in_row >= 0) {
-    const float4* src =
-        reinterpret_cast<const float4*>(init_pool + in_row * a.row_stride + head_off + v_row * kDimK + 32 * quarter);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float4 x = src[i];
-      S[4 * i] = x.x;
-      S[4 * i + 1] = x.y;
-      S[4 * i + 2] = x.z;
-      S[4 * i + 3] = x.w;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) S[i] = 0.f;
-  }
-  auto stage_state = [&]() {  // fp16 copy of S as the TMEM A operand
-    uint32_t w[16];
-#pragma unroll
-    for (int c = 0; c < 16; ++c) w[c] = pack_half2(S[2 * c], S[2 * c + 1]);
-    tmem_st16(lane_addr + COL_S16 + 16 * quarter, w);
-  };
-  // Store the fp32 state to a pool row with coalesced 16-byte stores, staging
-  // 32 state rows (16 KB) at a time in the U tile (free whenever this runs).
-  auto store_state = [&](float* pool, int row) {
-    float4* stg = reinterpret_cast<float4*>(sm + OFF_U);
-    float4* dst = reinterpret_cast<float4*>(pool + row * a.row_stride + head_off);
-#pragma unroll 1
-    for (int r = 0; r < 4; ++r) {
-      if ((warp & 3) == r) {
-        const int rr = v_row - 32 * r;
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          stg[rr * 32 + ((8 * quarter + i) ^ rr)] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
-      }
-      __syncthreads();
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int i = tid + k * kThreads;
-        dst[r * 1024 + i] = stg[(i >> 5) * 32 + ((i & 31) ^ (i >> 5))];
-      }
-      __syncthreads();
-    }
-  };
-  stage_state();
-
-  const int end_pos = P + L;
-  const int first_pos = (P / kChunk) * kChunk;
-  const int nchunks = (end_pos + kChunk - 1) / kChunk - P / kChunk;
-  const int first_ck = (ck_rows && N > 0) ? P / N : 0;
-
-  const uint32_t id_bf16_kk = idesc_f16(128, 64, true, true, false, false);
-  const uint32_t id_mnA = idesc_f16(128, 64, false, false, true, false);
-  const uint32_t id_mnB64 = idesc_f16(128, 64, false, false, false, true);
-  const uint32_t id_kk64 = idesc_f16(128, 64, false, false, false, false);
-  const uint32_t id_mnB128 = idesc_f16(128, 128, false, false, false, true);
-  const uint32_t id_kk128 = idesc_f16(128, 128, false, false, false, false);
 
   // Geometry of chunk ch: absolute position of row 0, valid rows [lo, hi),
   // packed token index of row 0.
@@ -347,547 +269,419 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto chunk_lo = [&](int ch) { return max(P - chunk_a0(ch), 0); };
   auto chunk_hi = [&](int ch) { return min(end_pos - chunk_a0(ch), kChunk); };
   auto chunk_tf = [&](int ch) { return cu_b + (chunk_a0(ch) - P); };
-  auto slot_off = [&](int ch) { return static_cast<uint32_t>(ch & 1) * SLOT_BYTES; };
-  // Shared-memory descriptors: K-major (8-row groups 1024 B apart) and MN-major.
+  auto kslot = [&](int ch) { return OFF_K + static_cast<uint32_t>(ch % 3) * 16384u; };
+  auto vslot = [&](int ch) { return OFF_V + static_cast<uint32_t>(ch & 1) * 16384u; };
+  auto tslot = [&](int ch) { return OFF_TZT + ((ch & 1) ? 0u : 16384u); };
   auto dK = [&](uint32_t off) { return sdesc(sbase + off, 16, 1024); };
   auto dMN = [&](uint32_t off, uint32_t lbo) { return sdesc(sbase + off, lbo, 1024); };
+  const int64_t head_off = static_cast<int64_t>(h) * kDimV * kDimK;
 
-  uint32_t ph_x = 0, ph_1 = 0, ph_s = 0, ph_2 = 0, ph_l2 = 0;
-  bool failed = false;
-  // One thread polls the mbarrier; everybody meets at a hardware barrier.
-  auto wait_bar = [&](uint64_t* bar, uint32_t parity) -> bool {
-    int bad = 0;
-    if (tid == 0) bad = mbar_wait(bar, parity) ? 0 : 1;
-    return __syncthreads_or(bad) == 0;
-  };
-
-  // ---------------------------------------------------------------- prep ----
-  auto issue_tma = [&](int ch) {  // one thread
-    const int tf = chunk_tf(ch);
-    uint8_t* s = sm + slot_off(ch);
-    uint64_t* bar = &sh.bar_tma[ch & 1];
-    mbar_arrive_expect_tx(bar, 6 * kTile);
-    tma_load_3d(s + SL_K0, &tm_k, bar, 0, h, tf);
-    tma_load_3d(s + SL_K1, &tm_k, bar, 64, h, tf);
-    tma_load_3d(s + SL_Q0, &tm_q, bar, 0, h, tf);
-    tma_load_3d(s + SL_Q1, &tm_q, bar, 64, h, tf);
-    tma_load_3d(s + SL_V0, &tm_v, bar, 0, h, tf);
-    tma_load_3d(s + SL_V1, &tm_v, bar, 64, h, tf);
-  };
-  float pg0 = 0.f, pg1 = 0.f, pb0 = 0.f, pb1 = 0.f;  // gates of rows 2*lane, 2*lane+1 (warp 1)
-  auto prefetch_gates = [&](int ch) {
-    if (warp == 1) {
-      const int lo = chunk_lo(ch), hi = chunk_hi(ch);
-      const int64_t tf = chunk_tf(ch);
-      const int r0 = 2 * lane, r1 = 2 * lane + 1;
-      const bool v0 = r0 >= lo && r0 < hi, v1 = r1 >= lo && r1 < hi;
-      pg0 = v0 ? a.g[(tf + r0) * H + h] : 0.f;
-      pb0 = v0 ? a.beta[(tf + r0) * H + h] : 0.f;
-      pg1 = v1 ? a.g[(tf + r1) * H + h] : 0.f;
-      pb1 = v1 ? a.beta[(tf + r1) * H + h] : 0.f;
-    }
-  };
-  auto gates = [&]() {  // warp 1: cumulative gate and the per-row scalars
-    if (warp == 1) {
-      float s = pg0 + pg1;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, s, off);
-        if (lane >= off) s += y;
+  if (warp == kIssuerWarp) {
+    // ================================================================ issuer
+    const uint32_t id_kk = idesc_f16(128, 128, false, false, false, false);
+    const uint32_t id_mnmn = idesc_f16(128, 128, false, false, true, true);
+    const uint32_t id_kmn = idesc_f16(128, 128, false, false, false, true);
+    const uint32_t id_qk = idesc_f16(128, 64, true, true, false, false);
+    int cx = 0, px = 0;  // next op of each stream, two per chunk
+    uint64_t t_last = globaltimer_ns();
+    while (cx < 2 * nch || px < 2 * nch) {
+      bool did = false;
+      if (cx < 2 * nch) {
+        const int c = cx >> 1;
+        const uint32_t e = c & 1;
+        bool ready = ((cx & 1) == 0) ? (mbar_test(&sh.xa_full, e) && mbar_test(&sh.s16_ready, e))
+                                     : mbar_test(&sh.u_ready, e);
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        if (ready) {
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t d = tmem + COL_DX + 128 * e;
+            if ((cx & 1) == 0) {  // D_X += XA S0^T
+              tc_mma4(d, dK(OFF_XA), 2, dK(OFF_S16), 2, id_kk, 1);
+              tc_mma4(d, dK(OFF_XA + 16384), 2, dK(OFF_S16 + 16384), 2, id_kk, 1);
+              tc_commit(&sh.bar_x);
+            } else {  // D_SU = U^T K~;  O rows += P U
+              tc_mma4(tmem + COL_DSU, dMN(OFF_U16, kTile), 128, dMN(kslot(c), kTile), 128, id_mnmn, 0);
+              tc_commit(&sh.bar_su);
+              tc_mma4(d, dK(OFF_P), 2, dMN(OFF_U16, kTile), 128, id_kmn, 1);
+              tc_commit(&sh.bar_o[e]);
+            }
+          }
+          __syncwarp();
+          ++cx;
+          did = true;
+        }
       }
-      const float G0 = s - pg1, G1 = s;
-      const float GC = __shfl_sync(0xffffffffu, s, 31);
-      const float gm0 = expf(G0), gm1 = expf(G1);
-      sh.G[2 * lane] = G0;
-      sh.G[2 * lane + 1] = G1;
-      sh.e[2 * lane] = expf(pg0);
-      sh.e[2 * lane + 1] = expf(pg1);
-      sh.gam[2 * lane] = gm0;
-      sh.gam[2 * lane + 1] = gm1;
-      sh.bet[2 * lane] = pb0;
-      sh.bet[2 * lane + 1] = pb1;
-      sh.sT1[2 * lane] = pb0 * gm0;
-      sh.sT1[2 * lane + 1] = pb1 * gm1;
-      sh.ksc[2 * lane] = expf(GC - G0);
-      sh.ksc[2 * lane + 1] = expf(GC - G1);
-    }
-  };
-  // Convert this thread's chunk of both 64-column blocks of a bf16 tile.
-  auto cvt_tile = [&](uint32_t dst, uint32_t dblk, uint32_t src, uint32_t sblk, float sc, bool keep) {
-    cvt8_store(sm + dst + coff, sm + src + coff, sc, keep);
-    cvt8_store(sm + dst + dblk + coff, sm + src + sblk + coff, sc, keep);
-  };
-  auto row_ok = [&](int ch) { return cr >= chunk_lo(ch) && cr < chunk_hi(ch); };
-  // The same conversion spread over warps 1-15 only (warp 0 is issuing MMAs).
-  auto cvt_tile_w = [&](int ch, uint32_t dst, uint32_t dblk, uint32_t src, uint32_t sblk, const float* rsc) {
-    if (warp == 0) return;
-    const int lo = chunk_lo(ch), hi = chunk_hi(ch);
-    for (int i = tid - 32; i < 1024; i += kThreads - 32) {
-      const int kb = i >> 9, r = (i & 511) >> 3;
-      const uint32_t o = static_cast<uint32_t>(i & 511) * 16u;
-      cvt8_store(sm + dst + kb * dblk + o, sm + src + kb * sblk + o, rsc ? rsc[r] : 1.f, r >= lo && r < hi);
-    }
-  };
-  // A from K K^T rows: the diagonal 16x16 blocks in fp32 (AM, for level 0 of
-  // the inverse), the strictly block-lower part as an fp16 operand (slot Q0,
-  // diagonal blocks zero); P (fp16 operand) from Q K^T rows.  Decay factors by
-  // running products exp(G_t - G_{j-1}) = exp(G_t - G_j) exp(g_j).
-  auto build_AP = [&](int ch) {
-    const int lo = chunk_lo(ch), hi = chunk_hi(ch);
-    const int j0 = 16 * quarter;
-    const int t = v_row & 63;
-    const bool isA = v_row < 64;
-    float x[16];
-    tmem_ld16(lane_addr + COL_D1 + j0, x);
-    const int jstart = min(j0 + 15, isA ? t - 1 : t);  // last column kept (j < t for A, j <= t for P)
-    float out[16];
-    if (t >= lo && t < hi && jstart >= j0) {
-      float ev[16];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 e4 = *reinterpret_cast<const float4*>(&sh.e[j0 + 4 * q]);
-        ev[4 * q] = e4.x;
-        ev[4 * q + 1] = e4.y;
-        ev[4 * q + 2] = e4.z;
-        ev[4 * q + 3] = e4.w;
+      if (!did && px < 2 * nch) {
+        const int p = px >> 1;
+        const uint32_t e = p & 1;
+        bool ready = ((px & 1) == 0) ? mbar_test(&sh.mp_ready, e) : mbar_test(&sh.m2_ready, e);
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        if (ready) {
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t d = tmem + COL_DX + 128 * e;
+            if ((px & 1) == 0) {  // Q K^T (bf16) into columns 0-63 of the chunk's D_X
+              tc_mma4(d, dK(OFF_Q), 2, dK(kslot(p)), 2, id_qk, 0);
+              tc_mma4(d, dK(OFF_Q + kTile), 2, dK(kslot(p) + kTile), 2, id_qk, 1);
+              tc_commit(&sh.bar_p);
+            } else {  // U~ into the U rows of D_X (zeros in the O rows); W into D_W
+              const uint32_t at = e ? OFF_TZT : OFF_TZT + kTile;
+              tc_mma4(d, dK(at), 2, dMN(vslot(p), kTile), 128, id_kmn, 0);
+              tc_mma4(tmem + COL_DW, dK(OFF_TP), 2, dMN(kslot(p), kTile), 128, id_kmn, 0);
+              tc_commit(&sh.bar_m2);
+            }
+          }
+          __syncwarp();
+          ++px;
+          did = true;
+        }
       }
-      float cur = (isA ? sh.bet[t] : 1.f) * expf(sh.G[t] - sh.G[jstart]);
-      if (jstart == j0 + 15 && lo <= j0) {  // whole block inside: no masks
+      if (did) {
+        t_last = globaltimer_ns();
+      } else if (*abort_flag || globaltimer_ns() - t_last > 2000000000ull) {
+        *abort_flag = 1;
+        break;
+      } else {
+        __nanosleep(32);  // give the issue slots to the working warps
+      }
+    }
+  } else if (warp >= 8) {
+    // ================================================================== prep
+    const int pt = tid - 256, pw = warp - 8;
+    const int wq = warp & 3, ph = pw >> 2;
+    const bool tm_reader = wq < 2;                      // warps 8, 9, 12, 13: TMEM lanes 0-63
+    const int cw = (pw == 2) ? 0 : (pw == 3 ? 1 : 2);  // warps 10, 11, 14 among the others
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * wq) << 16);
+    auto psync = [&]() { asm volatile("bar.sync 2, %0;" ::"r"(kPrepThreads) : "memory"); };
+    // One thread waits; the whole group learns the outcome at once.
+    auto pwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      uint32_t bad = 0;
+      if (pt == 0 && !mbar_wait_or_abort(bar, parity, abort_flag)) {
+        bad = 1;
+        *abort_flag = 1;
+      }
+      uint32_t any;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+          "bar.red.or.pred q, 2, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}\n"
+          : "=r"(any)
+          : "r"(bad), "r"(kPrepThreads)
+          : "memory");
+      tc_fence_after();
+      return any == 0;
+    };
+    auto tma_rows = [&](const CUtensorMap* map, uint32_t dst, uint64_t* bar, int ch) {
+      tma_load_3d(sm + dst, map, bar, 0, h, chunk_tf(ch));
+      tma_load_3d(sm + dst + kTile, map, bar, 64, h, chunk_tf(ch));
+    };
+    auto tma_q = [&](int ch) {
+      mbar_arrive_expect_tx(&sh.bar_q, 16384);
+      tma_rows(&tm_q, OFF_Q, &sh.bar_q, ch);
+    };
+    auto tma_k = [&](int ch) {
+      mbar_arrive_expect_tx(&sh.bar_k[ch % 3], 16384);
+      tma_rows(&tm_k, kslot(ch), &sh.bar_k[ch % 3], ch);
+    };
+    auto tma_v = [&](int ch) {
+      mbar_arrive_expect_tx(&sh.bar_v[ch & 1], 16384);
+      tma_rows(&tm_v, vslot(ch), &sh.bar_v[ch & 1], ch);
+    };
+    auto tma_t = [&](int ch) {
+      mbar_arrive_expect_tx(&sh.bar_t[ch & 1], kTinvBytes);
+      tma_load_2d(sm + tslot(ch), &tm_t, &sh.bar_t[ch & 1], 0, ((slot0 + ch) * H + h) * 64);
+    };
+    if (pt == 0) {
+      prefetch_tensormap(&tm_q);
+      prefetch_tensormap(&tm_k);
+      prefetch_tensormap(&tm_v);
+      prefetch_tensormap(&tm_t);
+      tma_q(0);
+      tma_k(0);
+      tma_v(0);
+      tma_t(0);
+      if (nch > 1) {
+        tma_k(1);
+        tma_v(1);
+        tma_t(1);
+      }
+    }
+    // Gates: warp 8 holds g of rows 2 lane and 2 lane + 1 of the next chunk.
+    float pg0 = 0.f, pg1 = 0.f;
+    auto prefetch_g = [&](int ch) {
+      if (pw == 0 && ch < nch) {
+        const int lo = chunk_lo(ch), hi = chunk_hi(ch);
+        const int64_t tf = chunk_tf(ch);
+        const int r0 = 2 * lane, r1 = 2 * lane + 1;
+        pg0 = (r0 >= lo && r0 < hi) ? a.g[(tf + r0) * H + h] : 0.f;
+        pg1 = (r1 >= lo && r1 < hi) ? a.g[(tf + r1) * H + h] : 0.f;
+      }
+    };
+    prefetch_g(0);
+    for (int p = 0; p < nch; ++p) {
+      const uint32_t e = p & 1;
+      const int lo = chunk_lo(p), hi = chunk_hi(p);
+      Gates& gs = sh.gates[p % 3];
+      // 1. cumulative gate of chunk p
+      if (pw == 0) {
+        float s = pg0 + pg1;
 #pragma unroll
-        for (int jj = 15; jj >= 0; --jj) {
-          out[jj] = cur * x[jj];
-          cur *= ev[jj];
+        for (int off = 1; off < 32; off <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, s, off);
+          if (lane >= off) s += y;
+        }
+        gs.G[2 * lane] = s - pg1;
+        gs.G[2 * lane + 1] = s;
+        gs.e[2 * lane] = __expf(pg0);
+        gs.e[2 * lane + 1] = __expf(pg1);
+        prefetch_g(p + 1);
+      }
+      psync();
+      // 2. T' = T'' diag(gamma)
+      if (!pwait(&sh.bar_t[e], (p >> 1) & 1)) break;
+      for (int i = pt; i < 512; i += kPrepThreads) {
+        const int c = (i & 7) ^ ((i >> 3) & 7);  // logical 16-byte chunk of this slot
+        float f[8];
+        unpack8h(*reinterpret_cast<const uint4*>(sm + tslot(p) + i * 16), f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] *= __expf(gs.G[8 * c + k]);
+        *reinterpret_cast<uint4*>(sm + OFF_TP + i * 16) = pack8h(f);
+      }
+      // 3. V -> fp16 in place
+      if (!pwait(&sh.bar_v[e], (p >> 1) & 1)) break;
+      for (int i = pt; i < 1024; i += kPrepThreads) {
+        const int row = (i & 511) >> 3;
+        uint8_t* ptr = sm + vslot(p) + (i >> 9) * kTile + (i & 511) * 16;
+        cvt8(ptr, ptr, 1.f, row >= lo && row < hi);
+      }
+      // 4. Q K^T may start once Q and K are in and the chunk's D_X is free
+      if (!pwait(&sh.bar_q, e)) break;
+      if (!pwait(&sh.bar_k[p % 3], (p / 3) & 1)) break;
+      if (p >= 2 && !pwait(&sh.o_read[e], ((p - 2) >> 1) & 1)) break;
+      if (pt == 0) mbar_arrive(&sh.mp_ready);
+      // 5. P = decayed, masked Q K^T (TMEM lanes 0-63)  ||  K -> fp16 in place
+      if (!pwait(&sh.bar_p, e)) break;
+      if (tm_reader) {
+        const int t = 32 * wq + lane;
+        float x[32];
+        tmem_ld32(lane_addr + COL_DX + 128 * e + 32 * ph, x);
+        float out[32];
+        const int j0 = 32 * ph;
+        const int jmax = min(j0 + 31, t);
+        if (t >= lo && t < hi && jmax >= j0) {
+          float cur = __expf(gs.G[t] - gs.G[jmax]);
+#pragma unroll
+          for (int jj = 31; jj >= 0; --jj) {
+            const int j = j0 + jj;
+            out[jj] = (j <= jmax && j >= lo) ? cur * x[jj] : 0.f;
+            if (j <= jmax) cur *= gs.e[j];
+          }
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) out[jj] = 0.f;
+        }
+        uint8_t* pb = sm + OFF_P + e * kTile;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(pb + swz(t, 4 * ph + c)) = pack8h(&out[8 * c]);
+      } else {
+        for (int i = 32 * cw + lane; i < 1024; i += 96) {
+          const int row = (i & 511) >> 3;
+          uint8_t* ptr = sm + kslot(p) + (i >> 9) * kTile + (i & 511) * 16;
+          cvt8(ptr, ptr, 1.f, row >= lo && row < hi);
+        }
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      psync();
+      if (pt == 0) mbar_arrive(&sh.m2_ready);
+      // 6. Q~ = diag(gamma) Q into the Q~ rows of XA (free once X of chunk p-1 is done)
+      if (p >= 1 && !pwait(&sh.bar_x, (p - 1) & 1)) break;
+      for (int i = pt; i < 1024; i += kPrepThreads) {
+        const int kb = i >> 9, rc = i & 511, row = rc >> 3;
+        cvt8(sm + OFF_XA + kb * 16384 + e * kTile + rc * 16, sm + OFF_Q + kb * kTile + rc * 16, __expf(gs.G[row]),
+             row >= lo && row < hi);
+      }
+      fence_proxy_async();
+      psync();
+      if (pt == 0 && p + 1 < nch) tma_q(p + 1);
+      // 7. -W (TMEM lanes 0-63) into the W rows of XA  ||  K~ = diag(exp(G_C - G)) K in place
+      if (!pwait(&sh.bar_m2, e)) break;
+      if (tm_reader) {
+        const int t = 32 * wq + lane;
+        const uint32_t wrow = t + 64 * (1 - e);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float w[32];
+          tmem_ld32(lane_addr + COL_DW + 64 * ph + 32 * hh, w);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = -w[i];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(sm + OFF_XA + ph * 16384 + swz(wrow, 4 * hh + c)) = pack8h(&w[8 * c]);
         }
       } else {
-#pragma unroll
-        for (int jj = 15; jj >= 0; --jj) {
-          const int j = j0 + jj;
-          const bool in = (j <= jstart) && (j >= lo);
-          out[jj] = in ? cur * x[jj] : 0.f;
-          if (j <= jstart) cur *= ev[jj];
+        const float GC = gs.G[63];
+        for (int i = 32 * cw + lane; i < 1024; i += 96) {
+          const int row = (i & 511) >> 3;
+          uint4* ptr = reinterpret_cast<uint4*>(sm + kslot(p) + (i >> 9) * kTile + (i & 511) * 16);
+          const float sc = __expf(GC - gs.G[row]);
+          uint4 u = *ptr;
+          u.x = scale_half2(u.x, sc);
+          u.y = scale_half2(u.y, sc);
+          u.z = scale_half2(u.z, sc);
+          u.w = scale_half2(u.w, sc);
+          *ptr = u;
         }
       }
-    } else {
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj) out[jj] = 0.f;
-    }
-    if (isA) {
-      const bool diag = (t >> 4) == quarter;
-      if (diag) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<float4*>(am_chunk(AM, t, (j0 >> 2) + q)) =
-              make_float4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
-      }
-      uint8_t* ao = sm + slot_off(ch) + SL_Q0;
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-        *reinterpret_cast<uint4*>(ao + swz(t, 2 * quarter + q)) =
-            diag ? make_uint4(0u, 0u, 0u, 0u) : pack8_half(&out[8 * q]);
-    } else {
-      uint8_t* pbuf = sm + OFF_P + (ch & 1) * kTile;
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-        *reinterpret_cast<uint4*>(pbuf + swz(t, 2 * quarter + q)) = pack8_half(&out[8 * q]);
-    }
-  };
-  // Level 0 of the inverse (threads 0-63): T_d = the 16x16 diagonal blocks of
-  // (I + A)^-1, one column per thread by forward substitution; then T_d as an
-  // fp16 tile (rows t, zeros outside the diagonal blocks) at OFF_WT + 8 KB.
-  auto inverse_l0 = [&]() {
-    const int bb = tid >> 4, jj = tid & 15;
-    float x[16];
-#pragma unroll
-    for (int tt = 0; tt < 16; ++tt) {
-      const int row = 16 * bb + tt;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        if (4 * m < tt) {
-          const float4 a4 = *reinterpret_cast<const float4*>(am_chunk(AM, row, 4 * bb + m));
-          if (4 * m + 0 < tt) acc[0] = fmaf(a4.x, x[4 * m + 0], acc[0]);
-          if (4 * m + 1 < tt) acc[1] = fmaf(a4.y, x[4 * m + 1], acc[1]);
-          if (4 * m + 2 < tt) acc[2] = fmaf(a4.z, x[4 * m + 2], acc[2]);
-          if (4 * m + 3 < tt) acc[3] = fmaf(a4.w, x[4 * m + 3], acc[3]);
-        }
-      }
-      x[tt] = (tt == jj) ? 1.f : (tt > jj ? -((acc[0] + acc[1]) + (acc[2] + acc[3])) : 0.f);
-    }
-    asm volatile("bar.sync 1, 64;" ::: "memory");  // all of A's diagonal blocks read
-#pragma unroll
-    for (int tt = 0; tt < 16; ++tt) am_at(AM, 16 * bb + tt, 16 * bb + jj) = x[tt];
-    asm volatile("bar.sync 1, 64;" ::: "memory");
-    {
-      // Row t of T_d (its diagonal block) into registers first: the fp16 tile
-      // overlaps rows 32-63 of the fp32 scratch that other threads still read.
-      const int t = tid, blk = t >> 4;
-      float f[16];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float4 v4 = *reinterpret_cast<const float4*>(am_chunk(AM, t, 4 * blk + m));
-        f[4 * m] = v4.x;
-        f[4 * m + 1] = v4.y;
-        f[4 * m + 2] = v4.z;
-        f[4 * m + 3] = v4.w;
-      }
-      asm volatile("bar.sync 1, 64;" ::: "memory");
-      uint8_t* td = sm + OFF_WT + kTile;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint4 u = make_uint4(0u, 0u, 0u, 0u);
-        if ((c >> 1) == blk) u = pack8_half(&f[8 * (c & 1)]);
-        *reinterpret_cast<uint4*>(td + swz(t, c)) = u;
-      }
-    }
-    fence_proxy_async();  // T_d is an MMA operand
-  };
-  // Rest of the inverse on the tensor core.  With N = -T_d A_o (A_o = the
-  // strictly block-lower part of A; N^4 = 0):
-  //   T = (I + N + N^2 + N^3) T_d = Z + N^2 Z,   Z = (I + N) T_d.
-  // Round 1: N = -T_d A_o.  Round 2: [N^2 | N T_d] = N [N | T_d] -> Z, N^2.
-  // Round 3: T = Z + N^2 Z -> T' = T diag(beta gamma), T'' = T diag(beta).
-  // The 64-row products occupy TMEM lanes 0-63; warps 0,1,4,5,8,9,12,13 read
-  // them (16 columns each).  Tiles: T_d at OFF_WT + 8 KB, N at OFF_WT (so
-  // [N | T_d] is one MN-major operand), A_o / N^2 / T' at slot Q0, Z / T'' at
-  // slot Q1.
-  auto inverse_rest = [&](int ch) -> bool {
-    const uint32_t so = slot_off(ch);
-    uint8_t* s = sm + so;
-    const bool rt = (warp & 3) < 2;       // this thread reads TMEM lanes 0-63
-    const int t = v_row;                  // its row (valid when rt)
-    const uint32_t lrow = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-    // Round 1.
-    if (tid == 0) {
-      tc_fence_after();
-      tc_mma4(tmem + COL_D1, dK(OFF_WT + kTile), 2, dMN(so + SL_Q0, kTile), 128, id_mnB64, 0);
-      tc_commit(&sh.bar_l2);
-    }
-    if (!wait_bar(&sh.bar_l2, ph_l2)) return false;
-    ph_l2 ^= 1;
-    tc_fence_after();
-    if (rt) {
-      float d[16];
-      tmem_ld16(lrow + COL_D1 + 16 * quarter, d);
-#pragma unroll
-      for (int q = 0; q < 16; ++q) d[q] = -d[q];
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-        *reinterpret_cast<uint4*>(sm + OFF_WT + swz(t, 2 * quarter + q)) = pack8_half(&d[8 * q]);
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    // Round 2.
-    if (tid == 0) {
-      tc_fence_after();
-      tc_mma4(tmem + COL_D1, dK(OFF_WT), 2, dMN(OFF_WT, kTile), 128, id_mnB128, 0);
-      tc_commit(&sh.bar_l2);
-    }
-    if (!wait_bar(&sh.bar_l2, ph_l2)) return false;
-    ph_l2 ^= 1;
-    tc_fence_after();
-    float z[16];
-    if (rt) {
-      float n2[16], nt[16];
-      tmem_ld16(lrow + COL_D1 + 16 * quarter, n2);
-      tmem_ld16(lrow + COL_D1 + 64 + 16 * quarter, nt);
-      const uint8_t* td = sm + OFF_WT + kTile;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const uint4 u = *reinterpret_cast<const uint4*>(td + swz(t, 2 * quarter + q));
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-          z[8 * q + 2 * e] = f.x + nt[8 * q + 2 * e];
-          z[8 * q + 2 * e + 1] = f.y + nt[8 * q + 2 * e + 1];
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        *reinterpret_cast<uint4*>(s + SL_Q0 + swz(t, 2 * quarter + q)) = pack8_half(&n2[8 * q]);
-        *reinterpret_cast<uint4*>(s + SL_Q1 + swz(t, 2 * quarter + q)) = pack8_half(&z[8 * q]);
-      }
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    // Round 3.
-    if (tid == 0) {
-      tc_fence_after();
-      tc_mma4(tmem + COL_D1, dK(so + SL_Q0), 2, dMN(so + SL_Q1, kTile), 128, id_mnB64, 0);
-      tc_commit(&sh.bar_l2);
-    }
-    if (!wait_bar(&sh.bar_l2, ph_l2)) return false;
-    ph_l2 ^= 1;
-    tc_fence_after();
-    if (rt) {
-      float d[16], o1[16], o2[16];
-      tmem_ld16(lrow + COL_D1 + 16 * quarter, d);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 a1 = *reinterpret_cast<const float4*>(&sh.sT1[16 * quarter + 4 * q]);
-        const float4 a2 = *reinterpret_cast<const float4*>(&sh.bet[16 * quarter + 4 * q]);
-        const float s1[4] = {a1.x, a1.y, a1.z, a1.w}, s2[4] = {a2.x, a2.y, a2.z, a2.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float tv = z[4 * q + e] + d[4 * q + e];
-          o1[4 * q + e] = tv * s1[e];
-          o2[4 * q + e] = tv * s2[e];
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        *reinterpret_cast<uint4*>(s + SL_Q0 + swz(t, 2 * quarter + q)) = pack8_half(&o1[8 * q]);
-        *reinterpret_cast<uint4*>(s + SL_Q1 + swz(t, 2 * quarter + q)) = pack8_half(&o2[8 * q]);
-      }
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    return true;
-  };
-  // W (rows t, K-major) from W^T in TMEM (lane k): element (t, k) of this
-  // thread's 16 columns t goes to block k / 64 of the [W | Q~] operand.
-  auto write_w = [&]() {
-    float x[16];
-    tmem_ld16(lane_addr + COL_WT + 16 * quarter, x);
-    const int k = v_row, kb = k >> 6, kk = k & 63;
-    __half* wb = reinterpret_cast<__half*>(sm + OFF_XB + kb * 16384);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int t = 16 * quarter + i;
-      wb[(swz(t, kk >> 3) >> 1) + (kk & 7)] = __float2half_rn(x[i]);
-    }
-  };
-  // K~ = diag(exp(G_C - G)) K from the fp16 K of the slot.
-  auto build_kt = [&](int ch) {  // warps 1-15 (warp 0 is issuing MMA2)
-    if (warp == 0) return;
-    const uint8_t* src = sm + slot_off(ch) + SL_K0;
-    for (int i = tid - 32; i < 1024; i += kThreads - 32) {
-      const int kb = i >> 9, r = (i & 511) >> 3;
-      const uint32_t o = static_cast<uint32_t>(i & 511) * 16u;
-      const float sc = sh.ksc[r];
-      uint4 u = *reinterpret_cast<const uint4*>(src + kb * 16384 + o);
-      u.x = scale_half2(u.x, sc);
-      u.y = scale_half2(u.y, sc);
-      u.z = scale_half2(u.z, sc);
-      u.w = scale_half2(u.w, sc);
-      *reinterpret_cast<uint4*>(sm + OFF_KT + kb * kTile + o) = u;
-    }
-  };
-
-  // ---- MMA batches (thread 0) ----
-  auto issue_mma1 = [&](int ch) {  // D1 = [K;Q] K^T (bf16 from TMA)
-    const uint32_t so = slot_off(ch);
-    tc_mma4(tmem + COL_D1, dK(so), 2, dK(so), 2, id_bf16_kk, 0);
-    tc_mma4(tmem + COL_D1, dK(so + 16384), 2, dK(so + 16384), 2, id_bf16_kk, 1);
-    tc_commit(&sh.bar_1);
-  };
-  auto issue_mma2 = [&](int ch) {  // W^T = K^T T'^T, U~^T = V^T T''^T
-    const uint32_t so = slot_off(ch);
-    tc_mma4(tmem + COL_WT, dMN(so + SL_K0, 16384), 128, dK(so + SL_Q0), 2, id_mnA, 0);
-    tc_mma4(tmem + COL_UT, dMN(so + SL_V0, kTile), 128, dK(so + SL_Q1), 2, id_mnA, 0);
-    tc_commit(&sh.bar_2);
-  };
-  auto issue_x = [&]() {  // [X1 | O] = S0 [W; Q~]^T  (A = S0 from TMEM)
-    tc_mma4_ts(tmem + COL_X1, tmem + COL_S16, 8, dK(OFF_XB), 2, id_kk128, 0);
-    tc_mma4_ts(tmem + COL_X1, tmem + COL_S16 + 32, 8, dK(OFF_XB + 16384), 2, id_kk128, 1);
-    tc_commit(&sh.bar_x);
-  };
-  auto issue_su = [&](int c) {  // SU = U^T K~, O += U^T P^T  (A = U from TMEM)
-    tc_mma4_ts(tmem + COL_SU, tmem + COL_U, 8, dMN(OFF_KT, kTile), 128, id_mnB128, 0);
-    tc_mma4_ts(tmem + COL_O, tmem + COL_U, 8, dK(OFF_P + (c & 1) * kTile), 2, id_kk64, 1);
-    tc_commit(&sh.bar_s);
-  };
-
-  // ------------------------------------------------------------ prologue ----
-  if (tid == 0) {
-    issue_tma(0);
-    if (nchunks > 1) issue_tma(1);
-  }
-  prefetch_gates(0);
-  float gamC = 1.f;
-  do {
-    if (!wait_bar(&sh.bar_tma[0], 0)) { failed = true; break; }
-    gates();
-    cvt_tile(SL_V0, kTile, SL_V0, kTile, 1.f, row_ok(0));
-    if (tid == 0) {
-      tc_fence_after();
-      issue_mma1(0);
-    }
-    __syncthreads();
-    cvt_tile(OFF_XB + kTile, 16384, SL_Q0, 16384, sh.gam[cr], row_ok(0));
-    if (!wait_bar(&sh.bar_1, ph_1)) { failed = true; break; }
-    ph_1 ^= 1;
-    tc_fence_after();
-    build_AP(0);
-    cvt_tile(SL_K0, 16384, SL_K0, 16384, 1.f, row_ok(0));
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    if (tid < 64) inverse_l0();
-    __syncthreads();
-    if (!inverse_rest(0)) { failed = true; break; }
-    if (tid == 0) {
-      tc_fence_after();
-      issue_mma2(0);
-    }
-    build_kt(0);
-    if (!wait_bar(&sh.bar_2, ph_2)) { failed = true; break; }
-    ph_2 ^= 1;
-    tc_fence_after();
-    {
-      write_w();
-    }
-    gamC = sh.gam[63];
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-  } while (0);
-
-  // ---------------------------------------------------------------- loop ----
-  // Iteration c runs the state chain of chunk c and the prep of chunk p = c+1.
-  // A tcgen05.ld waits for every MMA issued before it, so each TMEM read comes
-  // right after the batch it needs, with shared-memory-only work in between.
-  for (int c = 0; c < nchunks && !failed; ++c) {
-    const int p = c + 1;
-    const bool has_p = p < nchunks;
-    const uint32_t sop = slot_off(p);
-    // [A] TMA two chunks ahead; chain MMAs X1 = S0 W^T, O = S0 Q~^T.
-    if (tid == 0) {
-      if (c + 2 < nchunks) issue_tma(c + 2);
-      tc_fence_after();
-      issue_x();
-    }
-    if (has_p) prefetch_gates(p);
-    // [B] prep p (shared memory only): gates, V -> fp16, K~ source rows.
-    if (has_p) {
-      if (!wait_bar(&sh.bar_tma[p & 1], (p >> 1) & 1)) { failed = true; break; }
-      gates();
-      cvt_tile_w(p, sop + SL_V0, kTile, sop + SL_V0, kTile, nullptr);
-      __syncthreads();
-    }
-    // [C] chain c: U = U~ - X1; then SU = U^T K~, O += U^T P^T and MMA1 of p.
-    if (!wait_bar(&sh.bar_x, ph_x)) { failed = true; break; }
-    ph_x ^= 1;
-    tc_fence_after();
-    {
-      float xu[16], xw[16];
-      tmem_ld16(lane_addr + COL_UT + 16 * quarter, xu);
-      tmem_ld16(lane_addr + COL_X1 + 16 * quarter, xw);
-      uint32_t w[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) w[q] = pack_half2(xu[2 * q] - xw[2 * q], xu[2 * q + 1] - xw[2 * q + 1]);
-      tmem_st8(lane_addr + COL_U + 8 * quarter, w);
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-      issue_su(c);
-      if (has_p) issue_mma1(p);
-    }
-    // [C'] prep p (shared memory only, X(c) has finished reading Q~): Q~ of p.
-    if (has_p) cvt_tile_w(p, OFF_XB + kTile, 16384, sop + SL_Q0, 16384, sh.gam);
-    // [F1] chain c: S <- gamma_C S + SU (registers), outputs into the U tile.
-    if (!wait_bar(&sh.bar_s, ph_s)) { failed = true; break; }
-    ph_s ^= 1;
-    tc_fence_after();
-    {
-      float x[32];
-      tmem_ld32(lane_addr + COL_SU + 32 * quarter, x);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) S[i] = fmaf(gamC, S[i], x[i]);
-      float y[16];
-      tmem_ld16(lane_addr + COL_O + 16 * quarter, y);
-      __nv_bfloat16* ost = reinterpret_cast<__nv_bfloat16*>(sm + OFF_U);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) ost[(16 * quarter + i) * 128 + v_row] = __float2bfloat16_rn(a.scale * y[i]);
-    }
-    // [D] prep p: A and P from MMA1, K -> fp16 in place.
-    if (has_p) {
-      if (!wait_bar(&sh.bar_1, ph_1)) { failed = true; break; }
-      ph_1 ^= 1;
-      tc_fence_after();
-      build_AP(p);
-      cvt_tile(sop + SL_K0, 16384, sop + SL_K0, 16384, 1.f, row_ok(p));
       fence_proxy_async();
-    }
-    tc_fence_before();
-    __syncthreads();
-    // [E0] inverse level 0 (threads 0-63) || output rows of chunk c (the others).
-    {
-      if (has_p && tid < 64) {
-        inverse_l0();
-      } else if (tid >= 64) {
-        const int lo = chunk_lo(c), hi = chunk_hi(c);
-        const int64_t tstride = static_cast<int64_t>(H) * kDimV;
-        __nv_bfloat16* obase = a.o + (static_cast<int64_t>(chunk_tf(c)) * H + h) * kDimV;
-        const __nv_bfloat16* ost = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_U);
-        for (int i = tid - 64; i < 1024; i += kThreads - 64) {
-          const int r = i >> 4, part = i & 15;
-          if (r >= lo && r < hi)
-            *reinterpret_cast<uint4*>(obase + r * tstride + part * 8) =
-                *reinterpret_cast<const uint4*>(ost + r * 128 + part * 8);
+      tc_fence_before();
+      psync();
+      if (pt == 0) {
+        if (p + 2 < nch) {
+          tma_v(p + 2);
+          tma_t(p + 2);
+          // The K slot of chunk p+2 held K~ of chunk p-1 until its U^T K~ finished.
+          if (p >= 1 && !mbar_wait_or_abort(&sh.bar_su, (p - 1) & 1, abort_flag)) *abort_flag = 1;
+          tma_k(p + 2);
         }
+        mbar_arrive(&sh.xa_full);
       }
     }
-    __syncthreads();
-    stage_state();  // S0 of chunk c+1 into TMEM (X(c) finished reading it)
-    // [E] prep p: inverse levels 1-2, T', T''; then MMA2.
-    if (has_p) {
-      if (!inverse_rest(p)) { failed = true; break; }
-      if (tid == 0) {
-        tc_fence_after();
-        issue_mma2(p);
+  } else {
+    // ================================================================= chain
+    const int wq = warp & 3, hc = warp >> 2;
+    const int v = 32 * wq + lane;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * wq) << 16);
+    bool ok = true;
+    auto cwait = [&](uint64_t* bar, uint32_t parity) {
+      if (ok && !mbar_wait_or_abort(bar, parity, abort_flag)) {
+        ok = false;
+        *abort_flag = 1;
       }
+      tc_fence_after();
+      return ok;
+    };
+    float S[64];
+    if (in_row >= 0) {
+      const float4* src =
+          reinterpret_cast<const float4*>(init_pool + in_row * a.row_stride + head_off + v * kDimK + 64 * hc);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float4 x = src[i];
+        S[4 * i] = x.x;
+        S[4 * i + 1] = x.y;
+        S[4 * i + 2] = x.z;
+        S[4 * i + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) S[i] = 0.f;
     }
-    // [G1] while MMA2 runs: checkpoint of chunk c, K~ of p (SU(c) has finished).
-    {
+    uint8_t* s16 = sm + OFF_S16 + hc * 16384;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(s16 + swz(v, c)) = pack8h(&S[8 * c]);
+    fence_proxy_async();
+    mbar_arrive(&sh.s16_ready);
+    auto store_state = [&](float* pool, int row) {
+      float4* dst = reinterpret_cast<float4*>(pool + row * a.row_stride + head_off + v * kDimK + 64 * hc);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
+    };
+    for (int c = 0; c < nch; ++c) {
+      const uint32_t e = c & 1;
+      // U rows of D_X: 64-127 for even chunks, 0-63 for odd ones; the O rows are the others.
+      const bool isU = (wq >> 1) != static_cast<int>(e);
+      const int t = v & 63;
+      const uint32_t dx = lane_addr + COL_DX + 128 * e + 64 * hc;
+      if (isU) {  // U -> U16[t][v] (fp16): A of U^T K~ and B of P U
+        if (!cwait(&sh.bar_x, e)) break;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float u[32];
+          tmem_ld32(dx + 32 * hh, u);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            *reinterpret_cast<uint4*>(sm + OFF_U16 + hc * kTile + swz(t, 4 * hh + cc)) = pack8h(&u[8 * cc]);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        mbar_arrive(&sh.u_ready);
+      }
+      // S1 = gamma_C S0 + U^T K~, and its fp16 copy for the next chunk
+      if (!cwait(&sh.bar_su, e)) break;
+      const float gamC = __expf(sh.gates[c % 3].G[63]);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float su[32];
+        tmem_ld32(lane_addr + COL_DSU + 64 * hc + 32 * hh, su);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) S[32 * hh + i] = fmaf(gamC, S[32 * hh + i], su[i]);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          *reinterpret_cast<uint4*>(s16 + swz(v, 4 * hh + cc)) = pack8h(&S[32 * hh + 8 * cc]);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(&sh.s16_ready);
       const int a_end = chunk_a0(c) + kChunk;
       if (ck_rows && ck_pool && a_end % N == 0 && a_end <= end_pos) {
         const int row = ck_rows[a_end / N - 1 - first_ck];
         if (row >= 0) store_state(ck_pool, row);
       }
+      if (!isU) {  // outputs of chunk c from the O rows
+        if (!cwait(&sh.bar_o[e], (c >> 1) & 1)) break;
+        const int lo = chunk_lo(c), hi = chunk_hi(c);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float o[32];
+          tmem_ld32(dx + 32 * hh, o);
+          if (t >= lo && t < hi) {
+            uint4* dst = reinterpret_cast<uint4*>(a.o + (static_cast<int64_t>(chunk_tf(c) + t) * H + h) * kDimV +
+                                                  64 * hc + 32 * hh);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              uint4 w;
+              w.x = pack_bf162(a.scale * o[8 * cc], a.scale * o[8 * cc + 1]);
+              w.y = pack_bf162(a.scale * o[8 * cc + 2], a.scale * o[8 * cc + 3]);
+              w.z = pack_bf162(a.scale * o[8 * cc + 4], a.scale * o[8 * cc + 5]);
+              w.w = pack_bf162(a.scale * o[8 * cc + 6], a.scale * o[8 * cc + 7]);
+              dst[cc] = w;
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&sh.o_read[e]);
+      }
     }
-    float gamC_next = gamC;
-    if (has_p) {
-      build_kt(p);
-      // [G2] W^T of p -> fp16 rows k.
-      if (!wait_bar(&sh.bar_2, ph_2)) { failed = true; break; }
-      ph_2 ^= 1;
-      tc_fence_after();
-      write_w();
-      gamC_next = sh.gam[63];
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    gamC = gamC_next;
+    if (ok && out_row >= 0) store_state(out_pool, out_row);
   }
 
-  if (failed) {
-    if (tid == 0) record_error(a.err_word, GDN_DEVERR_TIMEOUT, b);
-  } else if (out_row >= 0) {
-    store_state(out_pool, out_row);
-  }
   tc_fence_before();
   __syncthreads();
+  if (tid == 0 && sh.abort) record_error(a.err_word, GDN_DEVERR_TIMEOUT, b);
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
-int launch(const PrefillArgs& a, const void* q, const void* k, const void* v, cudaStream_t stream) {
+int launch(PrefillArgs& a, const void* q, const void* k, const void* v, void* workspace, size_t workspace_bytes,
+           cudaStream_t stream) {
+  const int64_t ns = num_chunk_slots(a.T, a.num_seqs);
+  if (!workspace || workspace_bytes < gdn::workspace_bytes(a.T, a.num_seqs, a.H) || !gdn_host::aligned16(workspace))
+    return GDN_ERR_INVALID_ARGUMENT;
   int rc = gdn_host::check_device(nullptr);
   if (rc != GDN_OK) return rc;
-  CUtensorMap mq, mk, mv;
+  a.num_slots = static_cast<int32_t>(ns);
+  a.slot_seq = static_cast<int32_t*>(workspace);
+  a.tinv = reinterpret_cast<__half*>(static_cast<uint8_t*>(workspace) + workspace_map_bytes(ns));
+  rc = host::launch_chunk_inverse(a, k, stream);
+  if (rc != GDN_OK) return rc;
+  CUtensorMap mq, mk, mv, mt;
   if (gdn_host::encode_tokens_map(&mq, q, a.T, a.H, kDimK) != GDN_OK ||
       gdn_host::encode_tokens_map(&mk, k, a.T, a.H, kDimK) != GDN_OK ||
-      gdn_host::encode_tokens_map(&mv, v, a.T, a.H, kDimV) != GDN_OK)
+      gdn_host::encode_tokens_map(&mv, v, a.T, a.H, kDimV) != GDN_OK ||
+      gdn_host::encode_tiles_map_f16(&mt, a.tinv, ns * a.H * 64) != GDN_OK)
     return GDN_ERR_CUDA;
   if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
       cudaSuccess) {
@@ -895,7 +689,7 @@ int launch(const PrefillArgs& a, const void* q, const void* k, const void* v, cu
     return GDN_ERR_CUDA;
   }
   const long long grid = static_cast<long long>(a.num_seqs) * a.H;
-  prefill_kernel<<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, stream>>>(mq, mk, mv, a);
+  prefill_kernel<<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, stream>>>(mq, mk, mv, mt, a);
   return gdn_host::launch_status();
 }
 
@@ -904,7 +698,8 @@ int check_common(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const 
                  int32_t K, int32_t V) {
   if (num_seqs < 0 || total_tokens < 0 || H < 1) return GDN_ERR_INVALID_ARGUMENT;
   if (K != kDimK || V != kDimV) return GDN_ERR_UNSUPPORTED;
-  if (static_cast<long long>(num_seqs) * H > 0x7FFFFFFFLL) return GDN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_seqs) * H > 0x7FFFFFFFLL || H > 65535) return GDN_ERR_UNSUPPORTED;
+  if (num_chunk_slots(total_tokens, num_seqs) * H * 64 > 0x7FFFFFFFLL) return GDN_ERR_UNSUPPORTED;
   if (num_seqs > 0 && !cu_seqlens) return GDN_ERR_INVALID_ARGUMENT;
   if (total_tokens > 0) {
     using gdn_host::aligned16;
@@ -932,6 +727,11 @@ void fill_common(PrefillArgs& a, const float* g, const float* beta, gdn_bf16* o,
 
 }  // namespace
 
+extern "C" size_t gdn_prefill_workspace_bytes(int32_t num_seqs, int32_t total_tokens, int32_t H) {
+  if (num_seqs < 0 || total_tokens < 0 || H < 1) return 0;
+  return gdn::workspace_bytes(total_tokens, num_seqs, H);
+}
+
 extern "C" int gdn_chunk_gated_delta_rule(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const float* g,
                                           const float* beta, gdn_bf16* o, const int32_t* cu_seqlens,
                                           int32_t num_seqs, int32_t total_tokens, int32_t H, int32_t K, int32_t V,
@@ -940,7 +740,8 @@ extern "C" int gdn_chunk_gated_delta_rule(const gdn_bf16* q, const gdn_bf16* k, 
                                           float* state_checkpoints, const int32_t* checkpoint_state_indices,
                                           const int32_t* checkpoint_cu_starts, const int32_t* prefix_lens,
                                           int32_t checkpoint_every_n_tokens, int64_t pool_row_stride,
-                                          int32_t* err_word, void* stream) {
+                                          void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                          void* stream) {
   int rc = check_common(q, k, v, g, beta, o, cu_seqlens, num_seqs, total_tokens, H, K, V);
   if (rc != GDN_OK) return rc;
   if ((state_indices != nullptr) != (initial_state != nullptr)) return GDN_ERR_INVALID_ARGUMENT;
@@ -971,7 +772,7 @@ extern "C" int gdn_chunk_gated_delta_rule(const gdn_bf16* q, const gdn_bf16* k, 
   a.prefix_lens = prefix_lens;
   a.N = nck ? checkpoint_every_n_tokens : 0;
   a.row_stride = any_pool ? pool_row_stride : 0;
-  return launch(a, q, k, v, static_cast<cudaStream_t>(stream));
+  return launch(a, q, k, v, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int gdn_chunk_gated_delta_rule_paged(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
@@ -981,7 +782,8 @@ extern "C" int gdn_chunk_gated_delta_rule_paged(const gdn_bf16* q, const gdn_bf1
                                                 int32_t num_pages, const int32_t* page_indices,
                                                 const int32_t* page_indptr, int32_t page_size,
                                                 const int32_t* last_page_len, const gdn_prefill_slots* slots,
-                                                int32_t* err_word, void* stream) {
+                                                void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                                void* stream) {
   int rc = check_common(q, k, v, g, beta, o, cu_seqlens, num_seqs, total_tokens, H, K, V);
   if (rc != GDN_OK) return rc;
   if (page_size <= 0 || page_size % kChunk != 0 || num_pages < 1) return GDN_ERR_INVALID_ARGUMENT;
@@ -1012,5 +814,5 @@ extern "C" int gdn_chunk_gated_delta_rule_paged(const gdn_bf16* q, const gdn_bf1
     a.pages = page_indices;
     a.last_len = last_page_len;
   }
-  return launch(a, q, k, v, static_cast<cudaStream_t>(stream));
+  return launch(a, q, k, v, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }

@@ -1,0 +1,93 @@
+// prefill_common.cuh -- what the prefill kernels share: the call's arguments,
+// the per-sequence geometry (prefix, chunks) and the workspace layout.
+//
+// "flashinfer.gdn_paged": chunk_gated_delta_rule_paged and "Slot arguments of
+// chunk_gated_delta_rule".  Chunks are 64 tokens aligned to ABSOLUTE positions:
+// the first chunk of a sequence with prefix P starts at 64 floor(P / 64), its
+// rows before P are left padding (the identity step), so page / checkpoint
+// boundaries (multiples of 64) always fall on chunk ends.
+#pragma once
+
+#include "common.cuh"
+
+namespace gdn {
+
+struct PrefillArgs {
+  const float* g;
+  const float* beta;
+  __nv_bfloat16* o;
+  const int32_t* cu_seqlens;
+  int32_t num_seqs;
+  int32_t T;
+  int32_t H;
+  float scale;
+  const float* initial_state;
+  const int32_t* state_indices;
+  float* output_state;
+  const int32_t* output_state_indices;
+  float* state_checkpoints;
+  const int32_t* checkpoint_state_indices;
+  const int32_t* checkpoint_cu_starts;
+  const int32_t* prefix_lens;
+  int32_t N;
+  int64_t row_stride;
+  // Paged mode without precomputed slots: rows come from the page table.
+  const int32_t* indptr;
+  const int32_t* pages;
+  const int32_t* last_len;
+  int32_t page_size;
+  int32_t num_pages;
+  int32_t* err_word;
+  // Workspace: chunk slot -> sequence map, then one 64 x 64 fp16 tile per
+  // (chunk slot, head) holding T'' = (I + A)^-1 diag(beta).
+  int32_t* slot_seq;
+  __half* tinv;
+  int32_t num_slots;
+};
+
+// Workspace chunk slots.  Chunk c of sequence b lives in slot
+//   base_b + c,  base_b = floor(cu_seqlens[b] / 64) + 2 b.
+// A sequence has at most floor(L / 64) + 2 chunks and base_{b+1} - base_b >=
+// floor(L_b / 64) + 2, so slots of different sequences never meet, and every
+// slot is below floor(T / 64) + 2 S + 2.
+__host__ __device__ inline int64_t num_chunk_slots(int64_t T, int64_t num_seqs) { return T / 64 + 2 * num_seqs + 2; }
+__device__ inline int slot_base(int cu_b, int b) { return cu_b / 64 + 2 * b; }
+
+constexpr uint32_t kTinvBytes = 64 * 64 * 2;  // one T'' tile
+
+__host__ __device__ inline size_t workspace_map_bytes(int64_t num_slots) {
+  return static_cast<size_t>((num_slots * 4 + 1023) / 1024 * 1024);
+}
+__host__ __device__ inline size_t workspace_bytes(int64_t T, int64_t num_seqs, int64_t H) {
+  const int64_t ns = num_chunk_slots(T, num_seqs);
+  return workspace_map_bytes(ns) + static_cast<size_t>(ns) * H * kTinvBytes;
+}
+
+// Prefix length P, start cu_b and new length L of sequence b.  Returns false
+// for a zero-length sequence or arguments no kernel may act on (the chain
+// kernel reports those in err_word).
+__device__ inline bool seq_extent(const PrefillArgs& a, int b, int& cu_b, int& L, int& P) {
+  cu_b = a.cu_seqlens[b];
+  L = a.cu_seqlens[b + 1] - cu_b;
+  if (L <= 0 || cu_b < 0 || static_cast<long long>(cu_b) + L > a.T) return false;
+  if (a.indptr) {
+    const int n = a.indptr[b + 1] - a.indptr[b];
+    const int lpl = a.last_len[b];
+    const long long tot = static_cast<long long>(n - 1) * a.page_size + lpl;
+    if (n < 1 || lpl < 1 || lpl > a.page_size || tot < L || tot > 0x3FFFFFFFLL) return false;
+    P = static_cast<int>(tot - L);
+  } else {
+    P = a.prefix_lens ? a.prefix_lens[b] : 0;
+    if (P < 0 || static_cast<long long>(P) + L > 0x3FFFFFFFLL) return false;
+  }
+  return true;
+}
+
+__device__ inline int chunk_count(int P, int L) { return (P + L + 63) / 64 - P / 64; }
+
+namespace host {
+// Enqueue the slot map and the chunk-local inverse kernels (ut.cu).
+int launch_chunk_inverse(const PrefillArgs& a, const void* k, cudaStream_t stream);
+}  // namespace host
+
+}  // namespace gdn

@@ -131,7 +131,12 @@ int gdn_paged_decode_slots(const int32_t *page_indptr, const int32_t *page_indic
  * when given, prefix_lens is required and N must be a positive multiple of 64.
  * initial_state, output_state and state_checkpoints may be the same pool;
  * pool_row_stride (elements) is >= H*V*K and a multiple of 4.
- * total_tokens is T, the first dimension of q/k/v/o. */
+ * total_tokens is T, the first dimension of q/k/v/o.
+ * workspace: caller-owned device memory of at least
+ * gdn_prefill_workspace_bytes(num_seqs, total_tokens, H) bytes, 16-byte
+ * aligned (GDN_ERR_INVALID_ARGUMENT otherwise).  The call overwrites it; its
+ * contents need no initialisation and mean nothing afterwards, and two calls
+ * in flight at once need two workspaces. */
 int gdn_chunk_gated_delta_rule(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
                                const float *g, const float *beta, gdn_bf16 *o,
                                const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens,
@@ -141,7 +146,8 @@ int gdn_chunk_gated_delta_rule(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_b
                                float *state_checkpoints, const int32_t *checkpoint_state_indices,
                                const int32_t *checkpoint_cu_starts, const int32_t *prefix_lens,
                                int32_t checkpoint_every_n_tokens, int64_t pool_row_stride,
-                               int32_t *err_word, void *stream);
+                               void *workspace, size_t workspace_bytes, int32_t *err_word,
+                               void *stream);
 
 /* gdn_chunk_gated_delta_rule_paged -- "chunk_gated_delta_rule_paged(q, k, v,
  * ...)": chunked prefill over a paged pool state_pool[num_pages, H, V, K].  It
@@ -151,9 +157,9 @@ int gdn_chunk_gated_delta_rule(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_b
  * page that ends at or before the prefix.  It is the slot-argument call above
  * with state_pool as all three pools, page_indices as checkpoint rows and
  * N = page_size.  slots (nullable): rows from gdn_paged_prefill_slots, e.g.
- * computed once per step and shared by all layers; when NULL the kernel
- * derives them itself from the page table (no extra launch, no workspace).
- * page_size must be a positive multiple of 64. */
+ * computed once per step and shared by all layers; when NULL the kernels
+ * derive them from the page table.  page_size must be a positive multiple of
+ * 64.  workspace / workspace_bytes: as for gdn_chunk_gated_delta_rule. */
 int gdn_chunk_gated_delta_rule_paged(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
                                      const float *g, const float *beta, gdn_bf16 *o,
                                      const int32_t *cu_seqlens, int32_t num_seqs,
@@ -161,8 +167,8 @@ int gdn_chunk_gated_delta_rule_paged(const gdn_bf16 *q, const gdn_bf16 *k, const
                                      float scale, float *state_pool, int32_t num_pages,
                                      const int32_t *page_indices, const int32_t *page_indptr,
                                      int32_t page_size, const int32_t *last_page_len,
-                                     const gdn_prefill_slots *slots, int32_t *err_word,
-                                     void *stream);
+                                     const gdn_prefill_slots *slots, void *workspace,
+                                     size_t workspace_bytes, int32_t *err_word, void *stream);
 
 /* gdn_gated_delta_rule_decode_paged -- "gated_delta_rule_decode_paged(q, k, v,
  * ...)": one token per sequence.  When the token opens a new page
@@ -180,8 +186,14 @@ int gdn_gated_delta_rule_decode_paged(const gdn_bf16 *q, const gdn_bf16 *k, cons
                                       const int32_t *last_page_len, const gdn_decode_slots *slots,
                                       int32_t *err_word, void *stream);
 
-/* Bytes of device workspace a prefill call needs: always 0 (the calls take no
- * workspace; kept so callers can size one uniformly). */
+/* Bytes of device workspace a prefill call over num_seqs sequences,
+ * total_tokens new tokens and H heads needs (0 for invalid arguments).  The
+ * prefill runs in two phases: a chunk-local phase computes, for every 64-token
+ * chunk and head in parallel, T'' = (I + A)^-1 diag(beta) of the chunked delta
+ * rule (A[t][j] = beta_t exp(G_t - G_j) k_t . k_j, j < t) and stores it as a
+ * 64 x 64 fp16 tile; the sequential state chain then reads it back.  The
+ * workspace holds one int32 per chunk slot and one 8 KB tile per (chunk slot,
+ * head), with total_tokens / 64 + 2 num_seqs + 2 chunk slots. */
 size_t gdn_prefill_workspace_bytes(int32_t num_seqs, int32_t total_tokens, int32_t H);
 
 /* Static text for a status code. */

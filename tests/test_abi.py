@@ -36,7 +36,11 @@ def test_status_strings_and_workspace():
     for code in (0, -1, -2, -3):
         assert lib.gdn_status_string(code) and lib.gdn_status_string(code) != b"unknown status"
     assert lib.gdn_status_string(-99) == b"unknown status"
-    assert lib.gdn_prefill_workspace_bytes(64, 100000, 32) == 0
+    # one int32 per chunk slot (padded to 1 KB) + one 64 x 64 fp16 tile per (slot, head);
+    # slots = T / 64 + 2 S + 2
+    slots = 100000 // 64 + 2 * 64 + 2
+    assert lib.gdn_prefill_workspace_bytes(64, 100000, 32) == (slots * 4 + 1023) // 1024 * 1024 + slots * 32 * 8192
+    assert lib.gdn_prefill_workspace_bytes(-1, 10, 2) == 0
 
 
 FAKE = 0x10000  # a 16-byte aligned non-null address; never dereferenced by the host checks below
@@ -57,12 +61,12 @@ def test_slot_calls_reject_bad_arguments():
 def _chunk(lib, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, o=FAKE, cu=FAKE, S=2, T=10, H=2, K=128, V=128, scale=0.0,
              init=None, si=None, out=None, osi=None, ck=None, cki=None, ccs=None, pl=None, N=0, stride=0,
-             err=None)
+             ws=FAKE, wsb=1 << 40, err=None)
     a.update(kw)
     return lib.gdn_chunk_gated_delta_rule(a["q"], a["k"], a["v"], a["g"], a["beta"], a["o"], a["cu"], a["S"],
                                           a["T"], a["H"], a["K"], a["V"], a["scale"], a["init"], a["si"],
                                           a["out"], a["osi"], a["ck"], a["cki"], a["ccs"], a["pl"], a["N"],
-                                          a["stride"], a["err"], None)
+                                          a["stride"], a["ws"], a["wsb"], a["err"], None)
 
 
 def test_prefill_rejects_bad_arguments():
@@ -81,16 +85,22 @@ def test_prefill_rejects_bad_arguments():
     assert _chunk(lib, **dict(ck, stride=100), pl=FAKE, N=128) == -1  # stride < H*V*K
     assert _chunk(lib, S=0) == 0                               # nothing to do
     assert _chunk(lib, T=0) == 0
+    need = lib.gdn_prefill_workspace_bytes(2, 10, 2)
+    assert _chunk(lib, ws=None) == -1                          # workspace required
+    assert _chunk(lib, wsb=need - 1) == -1                     # too small
+    assert _chunk(lib, ws=FAKE + 8, wsb=need) == -1            # not 16-byte aligned
 
 
 def test_paged_calls_reject_bad_arguments():
     lib = gdn.library()
     p = FAKE
     f = lib.gdn_chunk_gated_delta_rule_paged
-    assert f(p, p, p, p, p, p, p, 1, 10, 2, 128, 128, 0.0, p, 8, p, p, 96, p, None, None, None) == -1
-    assert f(p, p, p, p, p, p, p, 1, 10, 2, 128, 128, 0.0, None, 8, p, p, 64, p, None, None, None) == -1
-    assert f(p, p, p, p, p, p, p, 1, 10, 2, 128, 64, 0.0, p, 8, p, p, 64, p, None, None, None) == -2
-    assert f(p, p, p, p, p, p, p, 1, 10, 2, 128, 128, 0.0, p, 0, p, p, 64, p, None, None, None) == -1
+    big = 1 << 40
+    assert f(p, p, p, p, p, p, p, 1, 10, 2, 128, 128, 0.0, p, 8, p, p, 96, p, None, p, big, None, None) == -1
+    assert f(p, p, p, p, p, p, p, 1, 10, 2, 128, 128, 0.0, None, 8, p, p, 64, p, None, p, big, None, None) == -1
+    assert f(p, p, p, p, p, p, p, 1, 10, 2, 128, 64, 0.0, p, 8, p, p, 64, p, None, p, big, None, None) == -2
+    assert f(p, p, p, p, p, p, p, 1, 10, 2, 128, 128, 0.0, p, 0, p, p, 64, p, None, p, big, None, None) == -1
+    assert f(p, p, p, p, p, p, p, 1, 10, 2, 128, 128, 0.0, p, 8, p, p, 64, p, None, None, 0, None, None) == -1
     d = lib.gdn_gated_delta_rule_decode_paged
     assert d(p, p, p, p, p, p, 4, 2, 128, 128, 0.0, p, 8, None, p, p, None, None, None) == -1
     assert d(p, p, p, p, p, p, 4, 2, 96, 128, 0.0, p, 8, p, p, p, None, None, None) == -2
