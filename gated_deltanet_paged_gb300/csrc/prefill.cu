@@ -41,6 +41,8 @@
 // error; bf16 would not) except Q K^T, which uses the bf16 tiles as loaded.
 #include <math.h>
 
+#include <mutex>
+
 #include "prefill_common.cuh"
 
 namespace {
@@ -815,4 +817,61 @@ extern "C" int gdn_chunk_gated_delta_rule_paged(const gdn_bf16* q, const gdn_bf1
     a.last_len = last_page_len;
   }
   return launch(a, q, k, v, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// Paged prefill without a caller-provided workspace.
+//
+// Some callers cannot call cudaMalloc: a runtime whose device memory is all
+// handed out by its own pool, a plugin host that forbids device allocations,
+// or a serving loop that cannot afford the device synchronisation an
+// allocation may trigger.  For them the workspace of the chunk-local phase
+// lives in a fixed array in the library's own device image, reserved on every
+// GPU that loads the library for as long as the process runs.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kStaticWorkspaceBytes = size_t(64) << 20;  // 64 MiB
+static __device__ __align__(256) uint8_t g_static_workspace[kStaticWorkspaceBytes];
+
+// The array's device address, looked up once per device (with that device
+// current) on the first call made on it.
+void* static_workspace() {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" int gdn_chunk_gated_delta_rule_paged_static_workspace(
+    const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const float* g, const float* beta, gdn_bf16* o,
+    const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens, int32_t H, int32_t K, int32_t V, float scale,
+    float* state_pool, int32_t num_pages, const int32_t* page_indices, const int32_t* page_indptr, int32_t page_size,
+    const int32_t* last_page_len, const gdn_prefill_slots* slots, int32_t* err_word, void* stream) {
+  if (num_seqs >= 0 && total_tokens >= 0 && H >= 1 &&
+      gdn::workspace_bytes(total_tokens, num_seqs, H) > kStaticWorkspaceBytes)
+    return GDN_ERR_UNSUPPORTED;
+  void* ws = nullptr;
+  if (num_seqs > 0 && total_tokens > 0) {
+    ws = static_workspace();
+    if (!ws) return GDN_ERR_CUDA;
+  }
+  return gdn_chunk_gated_delta_rule_paged(q, k, v, g, beta, o, cu_seqlens, num_seqs, total_tokens, H, K, V, scale,
+                                          state_pool, num_pages, page_indices, page_indptr, page_size, last_page_len,
+                                          slots, ws, kStaticWorkspaceBytes, err_word, stream);
 }

@@ -170,6 +170,30 @@ int gdn_chunk_gated_delta_rule_paged(const gdn_bf16 *q, const gdn_bf16 *k, const
                                      const gdn_prefill_slots *slots, void *workspace,
                                      size_t workspace_bytes, int32_t *err_word, void *stream);
 
+/* gdn_chunk_gated_delta_rule_paged_static_workspace -- no counterpart in the
+ * method's published API; it exists for callers that cannot allocate device
+ * memory (a runtime whose memory all belongs to its own pool, a plugin host
+ * that forbids device allocations, a serving loop that cannot take the device
+ * synchronisation an allocation may cause).  Same arguments and result as
+ * gdn_chunk_gated_delta_rule_paged without workspace / workspace_bytes: the
+ * workspace is a fixed 64 MiB array in the library's device image, which every
+ * GPU that loads the library holds until the process exits.  The call
+ * allocates nothing; it returns GDN_ERR_UNSUPPORTED when
+ * gdn_prefill_workspace_bytes(num_seqs, total_tokens, H) exceeds 64 MiB
+ * (roughly total_tokens * H <= 500,000).  The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call outside any stream capture.  All calls share
+ * the one array: nothing in it needs to start at zero (each call writes what
+ * it reads), but calls whose executions overlap on the GPU (other streams,
+ * other host threads) race on it and must be serialised by the caller. */
+int gdn_chunk_gated_delta_rule_paged_static_workspace(
+    const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v, const float *g, const float *beta,
+    gdn_bf16 *o, const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens, int32_t H,
+    int32_t K, int32_t V, float scale, float *state_pool, int32_t num_pages,
+    const int32_t *page_indices, const int32_t *page_indptr, int32_t page_size,
+    const int32_t *last_page_len, const gdn_prefill_slots *slots, int32_t *err_word,
+    void *stream);
+
 /* gdn_gated_delta_rule_decode_paged -- "gated_delta_rule_decode_paged(q, k, v,
  * ...)": one token per sequence.  When the token opens a new page
  * (last_page_len[b] == 1) the state is read from the previous page and written
