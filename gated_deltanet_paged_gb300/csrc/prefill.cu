@@ -72,19 +72,23 @@ constexpr uint32_t COL_DW = 256;   // W (rows 0-63)
 constexpr uint32_t COL_DSU = 384;  // U^T K~
 constexpr uint32_t TMEM_COLS = 512;
 
-struct Gates {
-  float G[64];  // cumulative gate
-  float e[64];  // exp(g)
+struct Gates {    // of the chunk being prepared
+  float G[64];    // cumulative gate
+  float e[64];    // exp(g)
+  float gam[64];  // exp(G)
+  float ksc[64];  // exp(G_C - G)
 };
 
 struct Small {
-  Gates gates[3];  // ring over chunks
+  Gates gates;
+  float gamC[4];  // exp(G_C) by chunk, ring of 3 (read by the chain)
   // TMA completion
   uint64_t bar_q, bar_v[2], bar_t[2], bar_k[3];
   // MMA completion (tcgen05.commit)
   uint64_t bar_p, bar_m2, bar_x, bar_su, bar_o[2];
   // hand-offs between warp groups
   uint64_t xa_full, mp_ready, m2_ready, u_ready, s16_ready, o_read[2];
+  uint64_t o_staged, stg_free;  // output staging in the U16 tile
   uint32_t tmem_base;
   int seq;
   int flag;
@@ -137,7 +141,7 @@ __device__ __forceinline__ void cvt8(uint8_t* dst, const uint8_t* src, float sc,
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
-                   const PrefillArgs a) {
+                   const __grid_constant__ CUtensorMap tm_o, const PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
@@ -251,6 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.m2_ready, 1);
     mbar_init(&sh.u_ready, 128);
     mbar_init(&sh.s16_ready, 256);
+    mbar_init(&sh.o_staged, 128);
+    mbar_init(&sh.stg_free, 1);
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -394,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_2d(sm + tslot(ch), &tm_t, &sh.bar_t[ch & 1], 0, ((slot0 + ch) * H + h) * 64);
     };
     if (pt == 0) {
+      prefetch_tensormap(&tm_o);
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
@@ -423,8 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int p = 0; p < nch; ++p) {
       const uint32_t e = p & 1;
       const int lo = chunk_lo(p), hi = chunk_hi(p);
-      Gates& gs = sh.gates[p % 3];
-      // 1. cumulative gate of chunk p
+      Gates& gs = sh.gates;
+      // 1. cumulative gate of chunk p and its tables
       if (pw == 0) {
         float s = pg0 + pg1;
 #pragma unroll
@@ -432,37 +439,56 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float y = __shfl_up_sync(0xffffffffu, s, off);
           if (lane >= off) s += y;
         }
-        gs.G[2 * lane] = s - pg1;
-        gs.G[2 * lane + 1] = s;
+        const float G0 = s - pg1, G1 = s;
+        const float GC = __shfl_sync(0xffffffffu, s, 31);
+        gs.G[2 * lane] = G0;
+        gs.G[2 * lane + 1] = G1;
         gs.e[2 * lane] = __expf(pg0);
         gs.e[2 * lane + 1] = __expf(pg1);
+        gs.gam[2 * lane] = __expf(G0);
+        gs.gam[2 * lane + 1] = __expf(G1);
+        gs.ksc[2 * lane] = __expf(GC - G0);
+        gs.ksc[2 * lane + 1] = __expf(GC - G1);
+        if (lane == 0) sh.gamC[p % 3] = __expf(GC);
         prefetch_g(p + 1);
       }
-      psync();
-      // 2. T' = T'' diag(gamma)
+      // 2. Q K^T may start at once: Q and K are in, the chunk's D_X is free
+      if (!pwait(&sh.bar_q, e)) break;
+      if (!pwait(&sh.bar_k[p % 3], (p / 3) & 1)) break;
+      if (p >= 2 && !pwait(&sh.o_read[e], ((p - 2) >> 1) & 1)) break;
+      if (pt == 0) mbar_arrive(&sh.mp_ready);
+      // 3. T' = T'' diag(gamma)  (the gate tables are visible after the waits above)
       if (!pwait(&sh.bar_t[e], (p >> 1) & 1)) break;
       for (int i = pt; i < 512; i += kPrepThreads) {
         const int c = (i & 7) ^ ((i >> 3) & 7);  // logical 16-byte chunk of this slot
         float f[8];
         unpack8h(*reinterpret_cast<const uint4*>(sm + tslot(p) + i * 16), f);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) f[k] *= __expf(gs.G[8 * c + k]);
+        const float4 g0 = *reinterpret_cast<const float4*>(&gs.gam[8 * c]);
+        const float4 g1 = *reinterpret_cast<const float4*>(&gs.gam[8 * c + 4]);
+        f[0] *= g0.x;
+        f[1] *= g0.y;
+        f[2] *= g0.z;
+        f[3] *= g0.w;
+        f[4] *= g1.x;
+        f[5] *= g1.y;
+        f[6] *= g1.z;
+        f[7] *= g1.w;
         *reinterpret_cast<uint4*>(sm + OFF_TP + i * 16) = pack8h(f);
       }
-      // 3. V -> fp16 in place
+      // 4. V -> fp16 in place
       if (!pwait(&sh.bar_v[e], (p >> 1) & 1)) break;
       for (int i = pt; i < 1024; i += kPrepThreads) {
         const int row = (i & 511) >> 3;
         uint8_t* ptr = sm + vslot(p) + (i >> 9) * kTile + (i & 511) * 16;
         cvt8(ptr, ptr, 1.f, row >= lo && row < hi);
       }
-      // 4. Q K^T may start once Q and K are in and the chunk's D_X is free
-      if (!pwait(&sh.bar_q, e)) break;
-      if (!pwait(&sh.bar_k[p % 3], (p / 3) & 1)) break;
-      if (p >= 2 && !pwait(&sh.o_read[e], ((p - 2) >> 1) & 1)) break;
-      if (pt == 0) mbar_arrive(&sh.mp_ready);
-      // 5. P = decayed, masked Q K^T (TMEM lanes 0-63)  ||  K -> fp16 in place
+      // 5. once Q K^T is done: K -> fp16 in place (all warps), then P (TMEM lanes 0-63)
       if (!pwait(&sh.bar_p, e)) break;
+      for (int i = pt; i < 1024; i += kPrepThreads) {
+        const int row = (i & 511) >> 3;
+        uint8_t* ptr = sm + kslot(p) + (i >> 9) * kTile + (i & 511) * 16;
+        cvt8(ptr, ptr, 1.f, row >= lo && row < hi);
+      }
       if (tm_reader) {
         const int t = 32 * wq + lane;
         float x[32];
@@ -485,12 +511,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* pb = sm + OFF_P + e * kTile;
 #pragma unroll
         for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(pb + swz(t, 4 * ph + c)) = pack8h(&out[8 * c]);
-      } else {
-        for (int i = 32 * cw + lane; i < 1024; i += 96) {
-          const int row = (i & 511) >> 3;
-          uint8_t* ptr = sm + kslot(p) + (i >> 9) * kTile + (i & 511) * 16;
-          cvt8(ptr, ptr, 1.f, row >= lo && row < hi);
-        }
       }
       fence_proxy_async();
       tc_fence_before();
@@ -500,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p >= 1 && !pwait(&sh.bar_x, (p - 1) & 1)) break;
       for (int i = pt; i < 1024; i += kPrepThreads) {
         const int kb = i >> 9, rc = i & 511, row = rc >> 3;
-        cvt8(sm + OFF_XA + kb * 16384 + e * kTile + rc * 16, sm + OFF_Q + kb * kTile + rc * 16, __expf(gs.G[row]),
+        cvt8(sm + OFF_XA + kb * 16384 + e * kTile + rc * 16, sm + OFF_Q + kb * kTile + rc * 16, gs.gam[row],
              row >= lo && row < hi);
       }
       fence_proxy_async();
@@ -522,11 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(sm + OFF_XA + ph * 16384 + swz(wrow, 4 * hh + c)) = pack8h(&w[8 * c]);
         }
       } else {
-        const float GC = gs.G[63];
         for (int i = 32 * cw + lane; i < 1024; i += 96) {
           const int row = (i & 511) >> 3;
           uint4* ptr = reinterpret_cast<uint4*>(sm + kslot(p) + (i >> 9) * kTile + (i & 511) * 16);
-          const float sc = __expf(GC - gs.G[row]);
+          const float sc = gs.ksc[row];
           uint4 u = *ptr;
           u.x = scale_half2(u.x, sc);
           u.y = scale_half2(u.y, sc);
@@ -597,6 +616,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t dx = lane_addr + COL_DX + 128 * e + 64 * hc;
       if (isU) {  // U -> U16[t][v] (fp16): A of U^T K~ and B of P U
         if (!cwait(&sh.bar_x, e)) break;
+        // the previous chunk's outputs were staged in this tile
+        if (c >= 1 && !cwait(&sh.stg_free, (c - 1) & 1)) break;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           float u[32];
@@ -611,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // S1 = gamma_C S0 + U^T K~, and its fp16 copy for the next chunk
       if (!cwait(&sh.bar_su, e)) break;
-      const float gamC = __expf(sh.gates[c % 3].G[63]);
+      const float gamC = sh.gamC[c % 3];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         float su[32];
@@ -630,31 +651,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = ck_rows[a_end / N - 1 - first_ck];
         if (row >= 0) store_state(ck_pool, row);
       }
-      if (!isU) {  // outputs of chunk c from the O rows
+      if (!isU) {
+        // Outputs of chunk c from the O rows.  A full chunk goes through a bf16
+        // staging copy in the U16 tile (free once P U is done) and two TMA
+        // stores; a partial one (first / last of a sequence) row by row, so
+        // that no row of another sequence is touched.
         if (!cwait(&sh.bar_o[e], (c >> 1) & 1)) break;
         const int lo = chunk_lo(c), hi = chunk_hi(c);
+        const bool full = lo == 0 && hi == kChunk;
+        uint8_t* stg = sm + OFF_U16 + hc * kTile;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           float o[32];
           tmem_ld32(dx + 32 * hh, o);
-          if (t >= lo && t < hi) {
+          uint4 w[4];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            w[cc].x = pack_bf162(a.scale * o[8 * cc], a.scale * o[8 * cc + 1]);
+            w[cc].y = pack_bf162(a.scale * o[8 * cc + 2], a.scale * o[8 * cc + 3]);
+            w[cc].z = pack_bf162(a.scale * o[8 * cc + 4], a.scale * o[8 * cc + 5]);
+            w[cc].w = pack_bf162(a.scale * o[8 * cc + 6], a.scale * o[8 * cc + 7]);
+          }
+          if (full) {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint4*>(stg + swz(t, 4 * hh + cc)) = w[cc];
+          } else if (t >= lo && t < hi) {
             uint4* dst = reinterpret_cast<uint4*>(a.o + (static_cast<int64_t>(chunk_tf(c) + t) * H + h) * kDimV +
                                                   64 * hc + 32 * hh);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              uint4 w;
-              w.x = pack_bf162(a.scale * o[8 * cc], a.scale * o[8 * cc + 1]);
-              w.y = pack_bf162(a.scale * o[8 * cc + 2], a.scale * o[8 * cc + 3]);
-              w.z = pack_bf162(a.scale * o[8 * cc + 4], a.scale * o[8 * cc + 5]);
-              w.w = pack_bf162(a.scale * o[8 * cc + 6], a.scale * o[8 * cc + 7]);
-              dst[cc] = w;
-            }
+            for (int cc = 0; cc < 4; ++cc) dst[cc] = w[cc];
           }
         }
         tc_fence_before();
         mbar_arrive(&sh.o_read[e]);
+        fence_proxy_async();
+        mbar_arrive(&sh.o_staged);
+        bool bad = false;
+        if (lane == 0 && (wq & 1) == 0 && hc == 0) {  // one thread of the group (warp 0 or 2)
+          bad = !mbar_wait_or_abort(&sh.o_staged, c & 1, abort_flag);
+          if (!bad) {
+            if (full) {
+              tma_store_3d(&tm_o, sm + OFF_U16, 0, h, chunk_tf(c));
+              tma_store_3d(&tm_o, sm + OFF_U16 + kTile, 64, h, chunk_tf(c));
+              bulk_commit();
+              bulk_wait_read();
+            }
+            mbar_arrive(&sh.stg_free);
+          }
+        }
+        if (__shfl_sync(0xffffffffu, bad, 0)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
       }
     }
+    bulk_wait_all();
     if (ok && out_row >= 0) store_state(out_pool, out_row);
   }
 
@@ -679,10 +731,11 @@ int launch(PrefillArgs& a, const void* q, const void* k, const void* v, void* wo
   a.tinv = reinterpret_cast<__half*>(static_cast<uint8_t*>(workspace) + workspace_map_bytes(ns));
   rc = host::launch_chunk_inverse(a, k, stream);
   if (rc != GDN_OK) return rc;
-  CUtensorMap mq, mk, mv, mt;
+  CUtensorMap mq, mk, mv, mt, mo;
   if (gdn_host::encode_tokens_map(&mq, q, a.T, a.H, kDimK) != GDN_OK ||
       gdn_host::encode_tokens_map(&mk, k, a.T, a.H, kDimK) != GDN_OK ||
       gdn_host::encode_tokens_map(&mv, v, a.T, a.H, kDimV) != GDN_OK ||
+      gdn_host::encode_tokens_map(&mo, a.o, a.T, a.H, kDimV) != GDN_OK ||
       gdn_host::encode_tiles_map_f16(&mt, a.tinv, ns * a.H * 64) != GDN_OK)
     return GDN_ERR_CUDA;
   if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
@@ -691,7 +744,7 @@ int launch(PrefillArgs& a, const void* q, const void* k, const void* v, void* wo
     return GDN_ERR_CUDA;
   }
   const long long grid = static_cast<long long>(a.num_seqs) * a.H;
-  prefill_kernel<<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, stream>>>(mq, mk, mv, mt, a);
+  prefill_kernel<<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, stream>>>(mq, mk, mv, mt, mo, a);
   return gdn_host::launch_status();
 }
 
