@@ -99,7 +99,7 @@ __global__ void slot_map_kernel(const PrefillArgs a) {
 }
 
 __global__ void __launch_bounds__(kUtThreads, 3)
-    ut_kernel(const __grid_constant__ CUtensorMap tm_k, const PrefillArgs a) {
+    ut_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_t, const PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
@@ -351,17 +351,25 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     tc_commit(&sh.bar_mma);
   }
   ok = ok && wait_all(&sh.bar_mma, 1);
-  if (ok && hi > lo) {
+  if (ok) {  // T'' rows into a staging tile per chunk (R2 is free again), then TMA stores
     float d[64];
     tmem_ld64(lane_addr + r0, d);
-    uint4* dst = reinterpret_cast<uint4*>(a.tinv + (static_cast<int64_t>(sh.slot[half]) * H + h) * 4096 + t * 64);
+    uint8_t* stg = sm + UT_R2 + half * kTile;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       float o[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[i] = (z[8 * c + i] + d[8 * c + i]) * sh.bet[r0 + 8 * c + i];
-      dst[c] = pack8h(o);
+      *reinterpret_cast<uint4*>(stg + swz(t, c)) = pack8h(o);
     }
+  }
+  fence_proxy_async();
+  __syncthreads();
+  if (ok && tid == 0) {
+    for (int hh = 0; hh < 2; ++hh)
+      if (sh.hi[hh] > sh.lo[hh]) tma_store_2d(&tm_t, sm + UT_R2 + hh * kTile, 0, (sh.slot[hh] * H + h) * 64);
+    bulk_commit();
+    bulk_wait_all();
   }
   if (!ok && tid == 0) record_error(a.err_word, GDN_DEVERR_TIMEOUT, 0);
   tc_fence_before();
@@ -380,14 +388,16 @@ namespace host {
 int launch_chunk_inverse(const PrefillArgs& a, const void* k, cudaStream_t stream) {
   if (a.num_seqs == 0 || a.num_slots == 0) return GDN_OK;
   slot_map_kernel<<<(a.num_slots + 255) / 256, 256, 0, stream>>>(a);
-  CUtensorMap mk;
-  if (gdn_host::encode_tokens_map(&mk, k, a.T, a.H, kDimK) != GDN_OK) return GDN_ERR_CUDA;
+  CUtensorMap mk, mt;
+  if (gdn_host::encode_tokens_map(&mk, k, a.T, a.H, kDimK) != GDN_OK ||
+      gdn_host::encode_tiles_map_f16(&mt, a.tinv, static_cast<int64_t>(a.num_slots) * a.H * 64) != GDN_OK)
+    return GDN_ERR_CUDA;
   if (cudaFuncSetAttribute(ut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, UT_SMEM) != cudaSuccess) {
     cudaGetLastError();
     return GDN_ERR_CUDA;
   }
   const dim3 grid(static_cast<unsigned>((a.num_slots + 1) / 2), static_cast<unsigned>(a.H));
-  ut_kernel<<<grid, kUtThreads, UT_SMEM, stream>>>(mk, a);
+  ut_kernel<<<grid, kUtThreads, UT_SMEM, stream>>>(mk, mt, a);
   return gdn_host::launch_status();
 }
 
