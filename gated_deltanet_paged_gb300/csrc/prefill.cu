@@ -72,11 +72,11 @@ constexpr uint32_t COL_DW = 256;   // W (rows 0-63)
 constexpr uint32_t COL_DSU = 384;  // U^T K~
 constexpr uint32_t TMEM_COLS = 512;
 
-struct Gates {    // of the chunk being prepared
-  float G[64];    // cumulative gate
-  float e[64];    // exp(g)
-  float gam[64];  // exp(G)
-  float ksc[64];  // exp(G_C - G)
+struct Gates {       // of the chunk being prepared
+  float G[64];       // cumulative gate
+  float e[64];       // exp(g)
+  float gam[2][64];  // exp(G), by chunk parity
+  float ksc[2][64];  // exp(G_C - G), by chunk parity
 };
 
 struct Small {
@@ -87,7 +87,7 @@ struct Small {
   // MMA completion (tcgen05.commit)
   uint64_t bar_p, bar_m2, bar_x, bar_su, bar_o[2];
   // hand-offs between warp groups
-  uint64_t xa_full, mp_ready, m2_ready, u_ready, s16_ready, o_read[2];
+  uint64_t xa_full, mp_ready, m2_ready, u_ready, s16_ready, gates_ready, qt_done, o_read[2];
   uint64_t o_staged, stg_free;  // output staging in the U16 tile
   uint32_t tmem_base;
   int seq;
@@ -250,7 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.bar_m2, 1);
     mbar_init(&sh.bar_x, 1);
     mbar_init(&sh.bar_su, 1);
-    mbar_init(&sh.xa_full, 1);
+    mbar_init(&sh.xa_full, 1 + 256);  // the prep's leader and every chain thread
+    mbar_init(&sh.gates_ready, 1);
+    mbar_init(&sh.qt_done, 256);
     mbar_init(&sh.mp_ready, 1);
     mbar_init(&sh.m2_ready, 1);
     mbar_init(&sh.u_ready, 128);
@@ -283,6 +285,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto dK = [&](uint32_t off) { return sdesc(sbase + off, 16, 1024); };
   auto dMN = [&](uint32_t off, uint32_t lbo) { return sdesc(sbase + off, lbo, 1024); };
   const int64_t head_off = static_cast<int64_t>(h) * kDimV * kDimK;
+
+  auto tma_rows = [&](const CUtensorMap* map, uint32_t dst, uint64_t* bar, int ch) {
+    tma_load_3d(sm + dst, map, bar, 0, h, chunk_tf(ch));
+    tma_load_3d(sm + dst + kTile, map, bar, 64, h, chunk_tf(ch));
+  };
+  auto tma_q = [&](int ch) {
+    mbar_arrive_expect_tx(&sh.bar_q, 16384);
+    tma_rows(&tm_q, OFF_Q, &sh.bar_q, ch);
+  };
 
   if (warp == kIssuerWarp) {
     // ================================================================ issuer
@@ -379,14 +390,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       return any == 0;
     };
-    auto tma_rows = [&](const CUtensorMap* map, uint32_t dst, uint64_t* bar, int ch) {
-      tma_load_3d(sm + dst, map, bar, 0, h, chunk_tf(ch));
-      tma_load_3d(sm + dst + kTile, map, bar, 64, h, chunk_tf(ch));
-    };
-    auto tma_q = [&](int ch) {
-      mbar_arrive_expect_tx(&sh.bar_q, 16384);
-      tma_rows(&tm_q, OFF_Q, &sh.bar_q, ch);
-    };
     auto tma_k = [&](int ch) {
       mbar_arrive_expect_tx(&sh.bar_k[ch % 3], 16384);
       tma_rows(&tm_k, kslot(ch), &sh.bar_k[ch % 3], ch);
@@ -445,10 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         gs.G[2 * lane + 1] = G1;
         gs.e[2 * lane] = __expf(pg0);
         gs.e[2 * lane + 1] = __expf(pg1);
-        gs.gam[2 * lane] = __expf(G0);
-        gs.gam[2 * lane + 1] = __expf(G1);
-        gs.ksc[2 * lane] = __expf(GC - G0);
-        gs.ksc[2 * lane + 1] = __expf(GC - G1);
+        gs.gam[e][2 * lane] = __expf(G0);
+        gs.gam[e][2 * lane + 1] = __expf(G1);
+        gs.ksc[e][2 * lane] = __expf(GC - G0);
+        gs.ksc[e][2 * lane + 1] = __expf(GC - G1);
         if (lane == 0) sh.gamC[p % 3] = __expf(GC);
         prefetch_g(p + 1);
       }
@@ -456,15 +459,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!pwait(&sh.bar_q, e)) break;
       if (!pwait(&sh.bar_k[p % 3], (p / 3) & 1)) break;
       if (p >= 2 && !pwait(&sh.o_read[e], ((p - 2) >> 1) & 1)) break;
-      if (pt == 0) mbar_arrive(&sh.mp_ready);
+      if (pt == 0) {
+        mbar_arrive(&sh.mp_ready);
+        mbar_arrive(&sh.gates_ready);
+      }
       // 3. T' = T'' diag(gamma)  (the gate tables are visible after the waits above)
       if (!pwait(&sh.bar_t[e], (p >> 1) & 1)) break;
       for (int i = pt; i < 512; i += kPrepThreads) {
         const int c = (i & 7) ^ ((i >> 3) & 7);  // logical 16-byte chunk of this slot
         float f[8];
         unpack8h(*reinterpret_cast<const uint4*>(sm + tslot(p) + i * 16), f);
-        const float4 g0 = *reinterpret_cast<const float4*>(&gs.gam[8 * c]);
-        const float4 g1 = *reinterpret_cast<const float4*>(&gs.gam[8 * c + 4]);
+        const float4 g0 = *reinterpret_cast<const float4*>(&gs.gam[e][8 * c]);
+        const float4 g1 = *reinterpret_cast<const float4*>(&gs.gam[e][8 * c + 4]);
         f[0] *= g0.x;
         f[1] *= g0.y;
         f[2] *= g0.z;
@@ -516,17 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       psync();
       if (pt == 0) mbar_arrive(&sh.m2_ready);
-      // 6. Q~ = diag(gamma) Q into the Q~ rows of XA (free once X of chunk p-1 is done)
+      // 6. -W (TMEM lanes 0-63) into the W rows of XA (free once X of chunk p-1 is done).
+      //    Q~ and K~ of this chunk are converted by the chain warps (see there).
       if (p >= 1 && !pwait(&sh.bar_x, (p - 1) & 1)) break;
-      for (int i = pt; i < 1024; i += kPrepThreads) {
-        const int kb = i >> 9, rc = i & 511, row = rc >> 3;
-        cvt8(sm + OFF_XA + kb * 16384 + e * kTile + rc * 16, sm + OFF_Q + kb * kTile + rc * 16, gs.gam[row],
-             row >= lo && row < hi);
-      }
-      fence_proxy_async();
-      psync();
-      if (pt == 0 && p + 1 < nch) tma_q(p + 1);
-      // 7. -W (TMEM lanes 0-63) into the W rows of XA  ||  K~ = diag(exp(G_C - G)) K in place
       if (!pwait(&sh.bar_m2, e)) break;
       if (tm_reader) {
         const int t = 32 * wq + lane;
@@ -540,18 +538,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             *reinterpret_cast<uint4*>(sm + OFF_XA + ph * 16384 + swz(wrow, 4 * hh + c)) = pack8h(&w[8 * c]);
-        }
-      } else {
-        for (int i = 32 * cw + lane; i < 1024; i += 96) {
-          const int row = (i & 511) >> 3;
-          uint4* ptr = reinterpret_cast<uint4*>(sm + kslot(p) + (i >> 9) * kTile + (i & 511) * 16);
-          const float sc = gs.ksc[row];
-          uint4 u = *ptr;
-          u.x = scale_half2(u.x, sc);
-          u.y = scale_half2(u.y, sc);
-          u.z = scale_half2(u.z, sc);
-          u.w = scale_half2(u.w, sc);
-          *ptr = u;
         }
       }
       fence_proxy_async();
@@ -603,12 +589,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(s16 + swz(v, c)) = pack8h(&S[8 * c]);
     fence_proxy_async();
     mbar_arrive(&sh.s16_ready);
+    // The chain warps' share of chunk q's preparation, done while they would
+    // otherwise wait for it: Q~ = diag(gamma) Q into the Q~ rows of XA (free:
+    // X of chunk q-1 has finished), the next Q load, and K~ = diag(exp(G_C - G)) K
+    // in place once W = T' K has read the fp16 K.
+    const int ci = tid;  // 0..255
+    auto help_prep = [&](int q) -> bool {
+      const uint32_t eq = q & 1;
+      const int lo = chunk_lo(q), hi = chunk_hi(q);
+      if (!cwait(&sh.bar_q, eq) || !cwait(&sh.gates_ready, eq)) return false;
+      const float* gam = sh.gates.gam[eq];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = ci + 256 * k;
+        const int kb = i >> 9, rc = i & 511, row = rc >> 3;
+        cvt8(sm + OFF_XA + kb * 16384 + eq * kTile + rc * 16, sm + OFF_Q + kb * kTile + rc * 16, gam[row],
+             row >= lo && row < hi);
+      }
+      fence_proxy_async();
+      mbar_arrive(&sh.qt_done);
+      if (ci == 0 && q + 1 < nch) {  // the Q buffer is free once Q~ and Q K^T have read it
+        if (!mbar_wait_or_abort(&sh.qt_done, eq, abort_flag) || !mbar_wait_or_abort(&sh.bar_p, eq, abort_flag)) {
+          *abort_flag = 1;
+          ok = false;
+        } else {
+          tma_q(q + 1);
+        }
+      }
+      if (!cwait(&sh.bar_m2, eq)) return false;  // W has read the fp16 K
+      const float* ksc = sh.gates.ksc[eq];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = ci + 256 * k;
+        const int row = (i & 511) >> 3;
+        uint4* ptr = reinterpret_cast<uint4*>(sm + kslot(q) + (i >> 9) * kTile + (i & 511) * 16);
+        const float sc = ksc[row];
+        uint4 u = *ptr;
+        u.x = scale_half2(u.x, sc);
+        u.y = scale_half2(u.y, sc);
+        u.z = scale_half2(u.z, sc);
+        u.w = scale_half2(u.w, sc);
+        *ptr = u;
+      }
+      fence_proxy_async();
+      mbar_arrive(&sh.xa_full);
+      return true;
+    };
     auto store_state = [&](float* pool, int row) {
       float4* dst = reinterpret_cast<float4*>(pool + row * a.row_stride + head_off + v * kDimK + 64 * hc);
 #pragma unroll
       for (int i = 0; i < 16; ++i) dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
     };
-    for (int c = 0; c < nch; ++c) {
+    if (!help_prep(0)) ok = false;
+    for (int c = 0; c < nch && ok; ++c) {
       const uint32_t e = c & 1;
       // U rows of D_X: 64-127 for even chunks, 0-63 for odd ones; the O rows are the others.
       const bool isU = (wq >> 1) != static_cast<int>(e);
@@ -705,6 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
+      if (c + 1 < nch && !help_prep(c + 1)) break;
     }
     bulk_wait_all();
     if (ok && out_row >= 0) store_state(out_pool, out_row);
