@@ -54,11 +54,11 @@ int encode_tokens_map(CUtensorMap* map, const void* base, int64_t T, int64_t H, 
   return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_CUDA;
 }
 
-int encode_tiles_map_f16(CUtensorMap* map, const void* base, int64_t rows) {
+int encode_tiles_map_f16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
   auto fn = encode_fn();
   if (!fn) return GDN_ERR_CUDA;
-  cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {128};
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
   cuuint32_t box[2] = {64, 64};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,

@@ -10,7 +10,7 @@
 // chunk with rows t = 0..63, cumulative gate G_t = g_0 + ... + g_t (rows outside
 // the sequence have g = beta = 0 and k = v = 0, so they are the identity),
 // gamma_t = exp(G_t), S0 the V x K state at the chunk start and
-// T'' = (I + A)^-1 diag(beta) from the chunk-local kernel (ut.cu):
+// T'' = (I + A)^-1 diag(beta) and -W from the chunk-local kernel (ut.cu):
 //   W     = T'' diag(gamma) K,  U~ = T'' V
 //   U     = U~ - W S0^T                            (the chunk's new values)
 //   O[t]  = scale (gamma_t S0 q_t + sum_{j<=t} exp(G_t - G_j)(q_t . k_j) U[j])
@@ -23,20 +23,22 @@
 //     64 columns), U read back from TMEM, the state update, the outputs and
 //     the page-boundary / final state stores;
 //   - warps 8-14, "prep": everything of chunk c+1 that does not depend on the
-//     state, while the chain works on chunk c: TMA of Q, K, V, T'', gates,
-//     P (decayed, masked Q K^T), W, Q~ = diag(gamma) Q, K~ = diag(exp(G_C - G)) K;
+//     state, while the chain works on chunk c: TMA of Q, K, V, T'' and -W,
+//     gates, V -> fp16, P (decayed, masked Q K^T); the chain warps convert
+//     Q~ = diag(gamma) Q and K~ = diag(exp(G_C - G)) K in their idle time;
 //   - warp 15, "issuer": every tcgen05.mma, in whatever order the two streams
 //     become ready (chain first).  A thread's MMA issue runs almost in step with
 //     the tensor core, so no warp that has other work issues.
 // Per chunk the MMAs are (M = 128, fp32 accumulators in TMEM):
-//   prep : D_X  = [Q; .] K^T                  (bf16 from TMA; P from rows 0-63)
+//   prep : D_P  = [Q; .] K^T                  (bf16 from TMA; P from rows 0-63)
 //          D_X  = [0; T''] V  or [T''; 0] V   (U~ into the chunk's U rows)
-//          D_W  = [T'; .] K,  T' = T'' diag(gamma)
 //   chain: D_X += [Q~; -W] S0^T or [-W; Q~] S0^T   (U rows: U~ - W S0^T = U;
 //                                                   O rows: Q~ S0^T)
 //          D_SU = U^T K~;  D_X += [P_even; P_odd] U (O rows += P U)
 // D_X alternates between two TMEM buffers and its U / O row halves swap with
-// the chunk parity, so one zero tile serves both forms of [0; T''].  Operands
+// the chunk parity (U rows 0-63 for even chunks), so one zero tile serves both
+// [T''; 0] and [0; T''], one Q~ tile sits between the two -W buffers of the
+// X operand, and one P tile serves both [P; .] and [.; P].  Operands
 // are fp16 (an 11-bit significand keeps written states within 1e-3 relative
 // error; bf16 would not) except Q K^T, which uses the bf16 tiles as loaded.
 #include <math.h>
@@ -58,17 +60,16 @@ constexpr uint32_t kTile = 8192;  // 64 rows x 128 B
 constexpr uint32_t OFF_Q = 0;         // Q bf16 [kb0 | kb1] (one chunk)
 constexpr uint32_t OFF_K = 16384;     // 3 x K [kb0 | kb1]: bf16 -> fp16 -> K~, in place
 constexpr uint32_t OFF_V = 65536;     // 2 x V [kb0 | kb1]: bf16 -> fp16, in place
-constexpr uint32_t OFF_TZT = 98304;   // T''(odd chunk) | zero tile | T''(even chunk)
-constexpr uint32_t OFF_P = 122880;    // P (even chunk) | P (odd chunk), rows t, K-major
-constexpr uint32_t OFF_TP = 139264;   // T' = T'' diag(gamma)
-constexpr uint32_t OFF_XA = 147456;   // [Q~; -W] or [-W; Q~], K-major, [kb0 | kb1]
+constexpr uint32_t OFF_TZT = 98304;   // T''(even chunk) | zero tile | T''(odd chunk)
+constexpr uint32_t OFF_P = 122880;    // P, rows t, K-major
+constexpr uint32_t OFF_XA = 131072;   // per K block (24 KB apart): -W (even) | Q~ | -W (odd)
 constexpr uint32_t OFF_S16 = 180224;  // S0 fp16, K-major B (rows v), [kb0 | kb1]
 constexpr uint32_t OFF_U16 = 212992;  // U fp16 [t][v], MN-major, [v 0-63 | v 64-127]
 constexpr uint32_t OFF_SMALL = 229376;
 
 // TMEM columns.
 constexpr uint32_t COL_DX = 0;     // two 128-column accumulators, by chunk parity
-constexpr uint32_t COL_DW = 256;   // W (rows 0-63)
+constexpr uint32_t COL_DP = 256;   // Q K^T of the chunk being prepared (rows 0-63, 64 columns)
 constexpr uint32_t COL_DSU = 384;  // U^T K~
 constexpr uint32_t TMEM_COLS = 512;
 
@@ -83,7 +84,7 @@ struct Small {
   Gates gates;
   float gamC[4];  // exp(G_C) by chunk, ring of 3 (read by the chain)
   // TMA completion
-  uint64_t bar_q, bar_v[2], bar_t[2], bar_k[3];
+  uint64_t bar_q, bar_v[2], bar_t[2], bar_k[3], bar_w[2];
   // MMA completion (tcgen05.commit)
   uint64_t bar_p, bar_m2, bar_x, bar_su, bar_o[2];
   // hand-offs between warp groups
@@ -109,21 +110,6 @@ __device__ __forceinline__ uint4 pack8h(const float* x) {
   return u;
 }
 
-__device__ __forceinline__ void unpack8h(uint4 u, float* x) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-    x[2 * i] = f.x;
-    x[2 * i + 1] = f.y;
-  }
-}
-
-__device__ __forceinline__ uint32_t scale_half2(uint32_t u, float sc) {
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u));
-  return pack_half2(f.x * sc, f.y * sc);
-}
-
 // bf16 x 8 -> fp16 x 8 times sc (zeros unless keep); src may equal dst.
 __device__ __forceinline__ void cvt8(uint8_t* dst, const uint8_t* src, float sc, bool keep) {
   uint4 out = make_uint4(0u, 0u, 0u, 0u);
@@ -141,7 +127,8 @@ __device__ __forceinline__ void cvt8(uint8_t* dst, const uint8_t* src, float sc,
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
-                   const __grid_constant__ CUtensorMap tm_o, const PrefillArgs a) {
+                   const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_w,
+                   const PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
@@ -239,6 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- set-up: barriers, TMEM, the zero tile ----
   if (tid == 0) {
     mbar_init(&sh.bar_q, 1);
+    mbar_init(&sh.bar_w[0], 1);
+    mbar_init(&sh.bar_w[1], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.bar_v[i], 1);
       mbar_init(&sh.bar_t[i], 1);
@@ -281,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto chunk_tf = [&](int ch) { return cu_b + (chunk_a0(ch) - P); };
   auto kslot = [&](int ch) { return OFF_K + static_cast<uint32_t>(ch % 3) * 16384u; };
   auto vslot = [&](int ch) { return OFF_V + static_cast<uint32_t>(ch & 1) * 16384u; };
-  auto tslot = [&](int ch) { return OFF_TZT + ((ch & 1) ? 0u : 16384u); };
+  auto tslot = [&](int ch) { return OFF_TZT + static_cast<uint32_t>(ch & 1) * 16384u; };
   auto dK = [&](uint32_t off) { return sdesc(sbase + off, 16, 1024); };
   auto dMN = [&](uint32_t off, uint32_t lbo) { return sdesc(sbase + off, lbo, 1024); };
   const int64_t head_off = static_cast<int64_t>(h) * kDimV * kDimK;
@@ -316,13 +305,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             const uint32_t d = tmem + COL_DX + 128 * e;
             if ((cx & 1) == 0) {  // D_X += XA S0^T
-              tc_mma4(d, dK(OFF_XA), 2, dK(OFF_S16), 2, id_kk, 1);
-              tc_mma4(d, dK(OFF_XA + 16384), 2, dK(OFF_S16 + 16384), 2, id_kk, 1);
+              tc_mma4(d, dK(OFF_XA + kTile * e), 2, dK(OFF_S16), 2, id_kk, 1);
+              tc_mma4(d, dK(OFF_XA + 24576 + kTile * e), 2, dK(OFF_S16 + 16384), 2, id_kk, 1);
               tc_commit(&sh.bar_x);
             } else {  // D_SU = U^T K~;  O rows += P U
               tc_mma4(tmem + COL_DSU, dMN(OFF_U16, kTile), 128, dMN(kslot(c), kTile), 128, id_mnmn, 0);
               tc_commit(&sh.bar_su);
-              tc_mma4(d, dK(OFF_P), 2, dMN(OFF_U16, kTile), 128, id_kmn, 1);
+              tc_mma4(d, dK(OFF_P - kTile * (1 - e)), 2, dMN(OFF_U16, kTile), 128, id_kmn, 1);
               tc_commit(&sh.bar_o[e]);
             }
           }
@@ -340,14 +329,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (lane == 0) {
             const uint32_t d = tmem + COL_DX + 128 * e;
-            if ((px & 1) == 0) {  // Q K^T (bf16) into columns 0-63 of the chunk's D_X
-              tc_mma4(d, dK(OFF_Q), 2, dK(kslot(p)), 2, id_qk, 0);
-              tc_mma4(d, dK(OFF_Q + kTile), 2, dK(kslot(p) + kTile), 2, id_qk, 1);
+            if ((px & 1) == 0) {  // Q K^T (bf16)
+              tc_mma4(tmem + COL_DP, dK(OFF_Q), 2, dK(kslot(p)), 2, id_qk, 0);
+              tc_mma4(tmem + COL_DP, dK(OFF_Q + kTile), 2, dK(kslot(p) + kTile), 2, id_qk, 1);
               tc_commit(&sh.bar_p);
-            } else {  // U~ into the U rows of D_X (zeros in the O rows); W into D_W
-              const uint32_t at = e ? OFF_TZT : OFF_TZT + kTile;
+            } else {  // U~ into the U rows of D_X (zeros in the O rows)
+              const uint32_t at = OFF_TZT + kTile * e;
               tc_mma4(d, dK(at), 2, dMN(vslot(p), kTile), 128, id_kmn, 0);
-              tc_mma4(tmem + COL_DW, dK(OFF_TP), 2, dMN(kslot(p), kTile), 128, id_kmn, 0);
               tc_commit(&sh.bar_m2);
             }
           }
@@ -370,7 +358,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pt = tid - 256, pw = warp - 8;
     const int wq = warp & 3, ph = pw >> 2;
     const bool tm_reader = wq < 2;                      // warps 8, 9, 12, 13: TMEM lanes 0-63
-    const int cw = (pw == 2) ? 0 : (pw == 3 ? 1 : 2);  // warps 10, 11, 14 among the others
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * wq) << 16);
     auto psync = [&]() { asm volatile("bar.sync 2, %0;" ::"r"(kPrepThreads) : "memory"); };
     // One thread waits; the whole group learns the outcome at once.
@@ -402,20 +389,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&sh.bar_t[ch & 1], kTinvBytes);
       tma_load_2d(sm + tslot(ch), &tm_t, &sh.bar_t[ch & 1], 0, ((slot0 + ch) * H + h) * 64);
     };
+    // -W of chunk ch straight into its -W buffer of the X operand (by chunk parity).
+    auto tma_w = [&](int ch) {
+      const uint32_t dst = OFF_XA + static_cast<uint32_t>(ch & 1) * 16384u;
+      const int row = ((slot0 + ch) * H + h) * 64;
+      uint64_t* bar = &sh.bar_w[ch & 1];
+      mbar_arrive_expect_tx(bar, kWBytes);
+      tma_load_2d(sm + dst, &tm_w, bar, 0, row);
+      tma_load_2d(sm + dst + 24576, &tm_w, bar, 64, row);
+    };
     if (pt == 0) {
       prefetch_tensormap(&tm_o);
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
       prefetch_tensormap(&tm_t);
+      prefetch_tensormap(&tm_w);
       tma_q(0);
       tma_k(0);
       tma_v(0);
       tma_t(0);
+      tma_w(0);
       if (nch > 1) {
         tma_k(1);
         tma_v(1);
         tma_t(1);
+        tma_w(1);
       }
     }
     // Gates: warp 8 holds g of rows 2 lane and 2 lane + 1 of the next chunk.
@@ -455,50 +454,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) sh.gamC[p % 3] = __expf(GC);
         prefetch_g(p + 1);
       }
-      // 2. Q K^T may start at once: Q and K are in, the chunk's D_X is free
+      // 2. Q K^T may start at once (Q and K are in; it has its own TMEM columns)
       if (!pwait(&sh.bar_q, e)) break;
       if (!pwait(&sh.bar_k[p % 3], (p / 3) & 1)) break;
-      if (p >= 2 && !pwait(&sh.o_read[e], ((p - 2) >> 1) & 1)) break;
       if (pt == 0) {
         mbar_arrive(&sh.mp_ready);
         mbar_arrive(&sh.gates_ready);
       }
-      // 3. T' = T'' diag(gamma)  (the gate tables are visible after the waits above)
-      if (!pwait(&sh.bar_t[e], (p >> 1) & 1)) break;
-      for (int i = pt; i < 512; i += kPrepThreads) {
-        const int c = (i & 7) ^ ((i >> 3) & 7);  // logical 16-byte chunk of this slot
-        float f[8];
-        unpack8h(*reinterpret_cast<const uint4*>(sm + tslot(p) + i * 16), f);
-        const float4 g0 = *reinterpret_cast<const float4*>(&gs.gam[e][8 * c]);
-        const float4 g1 = *reinterpret_cast<const float4*>(&gs.gam[e][8 * c + 4]);
-        f[0] *= g0.x;
-        f[1] *= g0.y;
-        f[2] *= g0.z;
-        f[3] *= g0.w;
-        f[4] *= g1.x;
-        f[5] *= g1.y;
-        f[6] *= g1.z;
-        f[7] *= g1.w;
-        *reinterpret_cast<uint4*>(sm + OFF_TP + i * 16) = pack8h(f);
-      }
-      // 4. V -> fp16 in place
+      // 3. V -> fp16 in place; U~ = T'' V may start once the chunk's D_X is free
       if (!pwait(&sh.bar_v[e], (p >> 1) & 1)) break;
       for (int i = pt; i < 1024; i += kPrepThreads) {
         const int row = (i & 511) >> 3;
         uint8_t* ptr = sm + vslot(p) + (i >> 9) * kTile + (i & 511) * 16;
         cvt8(ptr, ptr, 1.f, row >= lo && row < hi);
       }
-      // 5. once Q K^T is done: K -> fp16 in place (all warps), then P (TMEM lanes 0-63)
+      fence_proxy_async();
+      if (!pwait(&sh.bar_t[e], (p >> 1) & 1)) break;
+      if (p >= 2 && !pwait(&sh.o_read[e], ((p - 2) >> 1) & 1)) break;
+      if (pt == 0) mbar_arrive(&sh.m2_ready);
+      // 4. P = decayed, masked Q K^T (TMEM lanes 0-63) once P U of chunk p-1 has read the
+      //    P tile; Q~ and K~ are done by the chain warps
       if (!pwait(&sh.bar_p, e)) break;
-      for (int i = pt; i < 1024; i += kPrepThreads) {
-        const int row = (i & 511) >> 3;
-        uint8_t* ptr = sm + kslot(p) + (i >> 9) * kTile + (i & 511) * 16;
-        cvt8(ptr, ptr, 1.f, row >= lo && row < hi);
-      }
+      if (p >= 1 && !pwait(&sh.bar_o[(p - 1) & 1], ((p - 1) >> 1) & 1)) break;
       if (tm_reader) {
         const int t = 32 * wq + lane;
         float x[32];
-        tmem_ld32(lane_addr + COL_DX + 128 * e + 32 * ph, x);
+        tmem_ld32(lane_addr + COL_DP + 32 * ph, x);
         float out[32];
         const int j0 = 32 * ph;
         const int jmax = min(j0 + 31, t);
@@ -514,36 +495,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) out[jj] = 0.f;
         }
-        uint8_t* pb = sm + OFF_P + e * kTile;
+        uint8_t* pb = sm + OFF_P;
 #pragma unroll
         for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(pb + swz(t, 4 * ph + c)) = pack8h(&out[8 * c]);
       }
       fence_proxy_async();
       tc_fence_before();
-      psync();
-      if (pt == 0) mbar_arrive(&sh.m2_ready);
-      // 6. -W (TMEM lanes 0-63) into the W rows of XA (free once X of chunk p-1 is done).
-      //    Q~ and K~ of this chunk are converted by the chain warps (see there).
+      // 5. -W of chunk p+1 into the buffer X of chunk p-1 has finished with
       if (p >= 1 && !pwait(&sh.bar_x, (p - 1) & 1)) break;
-      if (!pwait(&sh.bar_m2, e)) break;
-      if (tm_reader) {
-        const int t = 32 * wq + lane;
-        const uint32_t wrow = t + 64 * (1 - e);
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float w[32];
-          tmem_ld32(lane_addr + COL_DW + 64 * ph + 32 * hh, w);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) w[i] = -w[i];
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(sm + OFF_XA + ph * 16384 + swz(wrow, 4 * hh + c)) = pack8h(&w[8 * c]);
-        }
-      }
-      fence_proxy_async();
-      tc_fence_before();
-      psync();
       if (pt == 0) {
+        if (p >= 1 && p + 1 < nch) tma_w(p + 1);
+        // 6. the chunk is ready once U~ and -W are in
+        if (!mbar_wait_or_abort(&sh.bar_m2, e, abort_flag) ||
+            !mbar_wait_or_abort(&sh.bar_w[e], (p >> 1) & 1, abort_flag))
+          *abort_flag = 1;
         if (p + 2 < nch) {
           tma_v(p + 2);
           tma_t(p + 2);
@@ -553,6 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive(&sh.xa_full);
       }
+      psync();
     }
   } else {
     // ================================================================= chain
@@ -592,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The chain warps' share of chunk q's preparation, done while they would
     // otherwise wait for it: Q~ = diag(gamma) Q into the Q~ rows of XA (free:
     // X of chunk q-1 has finished), the next Q load, and K~ = diag(exp(G_C - G)) K
-    // in place once W = T' K has read the fp16 K.
+    // (bf16 -> fp16 in place) once Q K^T has read K.
     const int ci = tid;  // 0..255
     auto help_prep = [&](int q) -> bool {
       const uint32_t eq = q & 1;
@@ -603,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < 4; ++k) {
         const int i = ci + 256 * k;
         const int kb = i >> 9, rc = i & 511, row = rc >> 3;
-        cvt8(sm + OFF_XA + kb * 16384 + eq * kTile + rc * 16, sm + OFF_Q + kb * kTile + rc * 16, gam[row],
+        cvt8(sm + OFF_XA + kb * 24576 + kTile + rc * 16, sm + OFF_Q + kb * kTile + rc * 16, gam[row],
              row >= lo && row < hi);
       }
       fence_proxy_async();
@@ -616,20 +582,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_q(q + 1);
         }
       }
-      if (!cwait(&sh.bar_m2, eq)) return false;  // W has read the fp16 K
+      if (!cwait(&sh.bar_p, eq)) return false;  // Q K^T has read the bf16 K
       const float* ksc = sh.gates.ksc[eq];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int i = ci + 256 * k;
         const int row = (i & 511) >> 3;
-        uint4* ptr = reinterpret_cast<uint4*>(sm + kslot(q) + (i >> 9) * kTile + (i & 511) * 16);
-        const float sc = ksc[row];
-        uint4 u = *ptr;
-        u.x = scale_half2(u.x, sc);
-        u.y = scale_half2(u.y, sc);
-        u.z = scale_half2(u.z, sc);
-        u.w = scale_half2(u.w, sc);
-        *ptr = u;
+        uint8_t* ptr = sm + kslot(q) + (i >> 9) * kTile + (i & 511) * 16;
+        cvt8(ptr, ptr, ksc[row], row >= lo && row < hi);
       }
       fence_proxy_async();
       mbar_arrive(&sh.xa_full);
@@ -643,8 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!help_prep(0)) ok = false;
     for (int c = 0; c < nch && ok; ++c) {
       const uint32_t e = c & 1;
-      // U rows of D_X: 64-127 for even chunks, 0-63 for odd ones; the O rows are the others.
-      const bool isU = (wq >> 1) != static_cast<int>(e);
+      // U rows of D_X: 0-63 for even chunks, 64-127 for odd ones; the O rows are the others.
+      const bool isU = (wq >> 1) == static_cast<int>(e);
       const int t = v & 63;
       const uint32_t dx = lane_addr + COL_DX + 128 * e + 64 * hc;
       if (isU) {  // U -> U16[t][v] (fp16): A of U^T K~ and B of P U
@@ -763,14 +723,16 @@ int launch(PrefillArgs& a, const void* q, const void* k, const void* v, void* wo
   a.num_slots = static_cast<int32_t>(ns);
   a.slot_seq = static_cast<int32_t*>(workspace);
   a.tinv = reinterpret_cast<__half*>(static_cast<uint8_t*>(workspace) + workspace_map_bytes(ns));
+  a.wneg = a.tinv + ns * a.H * (kTinvBytes / 2);
   rc = host::launch_chunk_inverse(a, k, stream);
   if (rc != GDN_OK) return rc;
-  CUtensorMap mq, mk, mv, mt, mo;
+  CUtensorMap mq, mk, mv, mt, mo, mw;
   if (gdn_host::encode_tokens_map(&mq, q, a.T, a.H, kDimK) != GDN_OK ||
       gdn_host::encode_tokens_map(&mk, k, a.T, a.H, kDimK) != GDN_OK ||
       gdn_host::encode_tokens_map(&mv, v, a.T, a.H, kDimV) != GDN_OK ||
       gdn_host::encode_tokens_map(&mo, a.o, a.T, a.H, kDimV) != GDN_OK ||
-      gdn_host::encode_tiles_map_f16(&mt, a.tinv, ns * a.H * 64) != GDN_OK)
+      gdn_host::encode_tiles_map_f16(&mt, a.tinv, ns * a.H * 64, 64) != GDN_OK ||
+      gdn_host::encode_tiles_map_f16(&mw, a.wneg, ns * a.H * 64, 128) != GDN_OK)
     return GDN_ERR_CUDA;
   if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
       cudaSuccess) {
@@ -778,7 +740,7 @@ int launch(PrefillArgs& a, const void* q, const void* k, const void* v, void* wo
     return GDN_ERR_CUDA;
   }
   const long long grid = static_cast<long long>(a.num_seqs) * a.H;
-  prefill_kernel<<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, stream>>>(mq, mk, mv, mt, mo, a);
+  prefill_kernel<<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, stream>>>(mq, mk, mv, mt, mo, mw, a);
   return gdn_host::launch_status();
 }
 

@@ -1,5 +1,6 @@
 // ut.cu -- the chunk-local part of chunked GDN prefill: for every 64-token chunk
-// and head, T'' = (I + A)^-1 diag(beta), written to the workspace.
+// and head, T'' = (I + A)^-1 diag(beta) and -W = -T'' diag(gamma) K, written to
+// the workspace.
 //
 // "flashinfer.gdn_paged", chunk_gated_delta_rule: the gated delta rule in
 // chunked (WY / UT) form.  With rows t = 0..63 of a chunk (rows outside the
@@ -20,6 +21,8 @@
 //   T_d  = inverse of A's 16 x 16 diagonal blocks, forward substitution (fp32)
 //   N    = -T_d A_o           (A_o: A without its diagonal blocks; N^4 = 0)
 //   T    = (I + N)(I + N^2) T_d = Z + N^2 Z,  Z = T_d + N T_d
+//   W    = [T'_a; 0] K_a + [0; T'_b] K_b,  T' = T diag(beta gamma), K reloaded
+//          and converted to fp16 once the inverse no longer needs the space
 // The per-chunk B operands sit side by side ([X_a | X_b], N = 128) so one MMA
 // serves both chunks (the off-diagonal 64 x 64 result blocks are unused); for
 // N [N | T_d] the A operand is padded with a zero tile per chunk instead.
@@ -35,9 +38,10 @@ constexpr int kUtThreads = 128;
 constexpr uint32_t kTile = 8192;  // 64 rows x 128 B
 
 // Shared memory (offsets from the 1024-aligned base).
-//   R2 (24 KB): A_o [a | b]  ->  N_a | 0 | N_b  ->  N^2 stack (16 KB)
-//   R0 (32 KB): K stack  ->  fp32 diagonal blocks (first 8 KB) + T_d stack
-//               (last 16 KB)  ->  Z [a | b] (first 16 KB)
+//   R2 (24 KB): A_o [a | b] -> N_a | 0 | N_b -> N^2 stack (16 KB) -> T'' staging
+//               -> T'_a | 0 | T'_b
+//   R0 (32 KB): K stack -> fp32 diagonal blocks (first 8 KB) + T_d stack (last
+//               16 KB) -> Z [a | b] (first 16 KB) -> K stack again (fp16) -> -W staging
 constexpr uint32_t UT_R2 = 0;
 constexpr uint32_t UT_R0 = 24576;
 constexpr uint32_t UT_TD = UT_R0 + 16384;
@@ -47,6 +51,7 @@ struct UtSmall {
   float G[128];    // cumulative gate per stacked row
   float e[128];    // exp(g)
   float bet[128];  // beta
+  float gam[128];  // exp(G)
   float wsum[4];   // per-warp gate totals for the scan
   uint64_t bar_tma, bar_mma;
   uint32_t tmem_base;
@@ -99,7 +104,8 @@ __global__ void slot_map_kernel(const PrefillArgs a) {
 }
 
 __global__ void __launch_bounds__(kUtThreads, 3)
-    ut_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_t, const PrefillArgs a) {
+    ut_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_t,
+              const __grid_constant__ CUtensorMap tm_w, const PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
@@ -178,6 +184,7 @@ __global__ void __launch_bounds__(kUtThreads, 3)
   sh.G[tid] = s;
   sh.e[tid] = expf(gv);
   sh.bet[tid] = bv;
+  sh.gam[tid] = expf(s);
 
   auto dK = [&](uint32_t off) { return sdesc(sbase + off, 16, 1024); };
   auto dMN = [&](uint32_t off, uint32_t lbo) { return sdesc(sbase + off, lbo, 1024); };
@@ -351,16 +358,25 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     tc_commit(&sh.bar_mma);
   }
   ok = ok && wait_all(&sh.bar_mma, 1);
-  if (ok) {  // T'' rows into a staging tile per chunk (R2 is free again), then TMA stores
+  // K again (the inverse has released R0), for W.
+  if (ok && tid == 0) {
+    mbar_arrive_expect_tx(&sh.bar_tma, 16384u * ((va ? 1u : 0u) + (vb ? 1u : 0u)));
+    for (int hh = 0; hh < 2; ++hh) {
+      if (sh.hi[hh] <= sh.lo[hh]) continue;
+      tma_load_3d(sm + UT_R0 + hh * kTile, &tm_k, &sh.bar_tma, 0, h, sh.tf[hh]);
+      tma_load_3d(sm + UT_R0 + 16384 + hh * kTile, &tm_k, &sh.bar_tma, 64, h, sh.tf[hh]);
+    }
+  }
+  float tr[64];  // row t of T'' = T diag(beta)
+  if (ok) {      // T'' rows into a staging tile per chunk (R2 is free again), then TMA stores
     float d[64];
     tmem_ld64(lane_addr + r0, d);
     uint8_t* stg = sm + UT_R2 + half * kTile;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      float o[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = (z[8 * c + i] + d[8 * c + i]) * sh.bet[r0 + 8 * c + i];
-      *reinterpret_cast<uint4*>(stg + swz(t, c)) = pack8h(o);
+      for (int i = 0; i < 8; ++i) tr[8 * c + i] = (z[8 * c + i] + d[8 * c + i]) * sh.bet[r0 + 8 * c + i];
+      *reinterpret_cast<uint4*>(stg + swz(t, c)) = pack8h(&tr[8 * c]);
     }
   }
   fence_proxy_async();
@@ -368,6 +384,82 @@ __global__ void __launch_bounds__(kUtThreads, 3)
   if (ok && tid == 0) {
     for (int hh = 0; hh < 2; ++hh)
       if (sh.hi[hh] > sh.lo[hh]) tma_store_2d(&tm_t, sm + UT_R2 + hh * kTile, 0, (sh.slot[hh] * H + h) * 64);
+    bulk_commit();
+    bulk_wait_read();
+  }
+  __syncthreads();
+  // T' = T'' diag(gamma) as the A operand of W: [T'_a; 0] and [0; T'_b] from T'_a | 0 | T'_b.
+  if (ok) {
+    uint8_t* tp = sm + UT_R2 + half * 16384;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      float w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = tr[8 * c + i] * sh.gam[r0 + 8 * c + i];
+      *reinterpret_cast<uint4*>(tp + swz(t, c)) = pack8h(w);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      reinterpret_cast<uint4*>(sm + UT_R2 + kTile)[tid + 128 * k] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  // K (bf16) -> fp16 in place, rows outside each chunk zero.
+  if (ok) {
+    if (!mbar_wait(&sh.bar_tma, 1)) sh.flag = 1;
+    for (int i = tid; i < 2048; i += kUtThreads) {
+      const int box = i >> 9;  // K_a kb0 | K_b kb0 | K_a kb1 | K_b kb1
+      const int hh = box & 1, row = (i & 511) >> 3;
+      uint8_t* ptr = sm + UT_R0 + box * kTile + (i & 511) * 16;
+      uint4 out = make_uint4(0u, 0u, 0u, 0u);
+      if (row >= sh.lo[hh] && row < sh.hi[hh]) {
+        const uint4 in = *reinterpret_cast<const uint4*>(ptr);
+        const float2 f0 = unpack_bf162(in.x), f1 = unpack_bf162(in.y), f2 = unpack_bf162(in.z),
+                     f3 = unpack_bf162(in.w);
+        out.x = pack_half2(f0.x, f0.y);
+        out.y = pack_half2(f1.x, f1.y);
+        out.z = pack_half2(f2.x, f2.y);
+        out.w = pack_half2(f3.x, f3.y);
+      }
+      *reinterpret_cast<uint4*>(ptr) = out;
+    }
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  ok = ok && sh.flag == 0;
+
+  // ---- W = [T'_a; 0] K_a + [0; T'_b] K_b ----
+  if (ok && tid == 0) {
+    tc_fence_after();
+    tc_mma4(tmem, dK(UT_R2), 2, dMN(UT_R0, 16384), 128, id_mnB, 0);
+    tc_mma4(tmem, dK(UT_R2 + kTile), 2, dMN(UT_R0 + kTile, 16384), 128, id_mnB, 1);
+    tc_commit(&sh.bar_mma);
+  }
+  ok = ok && wait_all(&sh.bar_mma, 0);
+  // -W rows into staging boxes in R0 (K is no longer needed), then TMA stores.
+  if (ok) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float w[64];
+      tmem_ld64(lane_addr + 64 * hh, w);
+      uint8_t* box = sm + UT_R0 + half * 16384 + hh * kTile;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        float nw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) nw[i] = -w[8 * c + i];
+        *reinterpret_cast<uint4*>(box + swz(t, c)) = pack8h(nw);
+      }
+    }
+  }
+  fence_proxy_async();
+  __syncthreads();
+  if (ok && tid == 0) {
+    for (int hh = 0; hh < 2; ++hh)
+      if (sh.hi[hh] > sh.lo[hh]) {
+        const int row = (sh.slot[hh] * H + h) * 64;
+        tma_store_2d(&tm_w, sm + UT_R0 + hh * 16384, 0, row);
+        tma_store_2d(&tm_w, sm + UT_R0 + hh * 16384 + kTile, 64, row);
+      }
     bulk_commit();
     bulk_wait_all();
   }
@@ -388,16 +480,18 @@ namespace host {
 int launch_chunk_inverse(const PrefillArgs& a, const void* k, cudaStream_t stream) {
   if (a.num_seqs == 0 || a.num_slots == 0) return GDN_OK;
   slot_map_kernel<<<(a.num_slots + 255) / 256, 256, 0, stream>>>(a);
-  CUtensorMap mk, mt;
+  CUtensorMap mk, mt, mw;
+  const int64_t rows = static_cast<int64_t>(a.num_slots) * a.H * 64;
   if (gdn_host::encode_tokens_map(&mk, k, a.T, a.H, kDimK) != GDN_OK ||
-      gdn_host::encode_tiles_map_f16(&mt, a.tinv, static_cast<int64_t>(a.num_slots) * a.H * 64) != GDN_OK)
+      gdn_host::encode_tiles_map_f16(&mt, a.tinv, rows, 64) != GDN_OK ||
+      gdn_host::encode_tiles_map_f16(&mw, a.wneg, rows, 128) != GDN_OK)
     return GDN_ERR_CUDA;
   if (cudaFuncSetAttribute(ut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, UT_SMEM) != cudaSuccess) {
     cudaGetLastError();
     return GDN_ERR_CUDA;
   }
   const dim3 grid(static_cast<unsigned>((a.num_slots + 1) / 2), static_cast<unsigned>(a.H));
-  ut_kernel<<<grid, kUtThreads, UT_SMEM, stream>>>(mk, mt, a);
+  ut_kernel<<<grid, kUtThreads, UT_SMEM, stream>>>(mk, mt, mw, a);
   return gdn_host::launch_status();
 }
 

@@ -180,7 +180,7 @@ int gdn_chunk_gated_delta_rule_paged(const gdn_bf16 *q, const gdn_bf16 *k, const
  * GPU that loads the library holds until the process exits.  The call
  * allocates nothing; it returns GDN_ERR_UNSUPPORTED when
  * gdn_prefill_workspace_bytes(num_seqs, total_tokens, H) exceeds 64 MiB
- * (roughly total_tokens * H <= 500,000).  The first call on a device looks
+ * (roughly total_tokens * H <= 170,000).  The first call on a device looks
  * up the array's device address (cudaGetSymbolAddress) with that device
  * current; make that first call outside any stream capture.  All calls share
  * the one array: nothing in it needs to start at zero (each call writes what
@@ -214,10 +214,11 @@ int gdn_gated_delta_rule_decode_paged(const gdn_bf16 *q, const gdn_bf16 *k, cons
  * total_tokens new tokens and H heads needs (0 for invalid arguments).  The
  * prefill runs in two phases: a chunk-local phase computes, for every 64-token
  * chunk and head in parallel, T'' = (I + A)^-1 diag(beta) of the chunked delta
- * rule (A[t][j] = beta_t exp(G_t - G_j) k_t . k_j, j < t) and stores it as a
- * 64 x 64 fp16 tile; the sequential state chain then reads it back.  The
- * workspace holds one int32 per chunk slot and one 8 KB tile per (chunk slot,
- * head), with total_tokens / 64 + 2 num_seqs + 2 chunk slots. */
+ * rule (A[t][j] = beta_t exp(G_t - G_j) k_t . k_j, j < t) and
+ * -W = -T'' diag(exp(G)) K, and stores them as 64 x 64 and 64 x 128 fp16
+ * tiles; the sequential state chain then reads them back.  The workspace holds
+ * one int32 per chunk slot and 24 KB per (chunk slot, head), with
+ * total_tokens / 64 + 2 num_seqs + 2 chunk slots. */
 size_t gdn_prefill_workspace_bytes(int32_t num_seqs, int32_t total_tokens, int32_t H);
 
 /* Static text for a status code. */
