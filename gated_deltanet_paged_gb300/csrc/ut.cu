@@ -12,20 +12,23 @@
 // every sequence is computed here at once; the sequential state chain (the
 // prefill kernel) then only multiplies.
 //
-// Mapping: one CTA of 128 threads per (pair of chunk slots, head); thread r is
-// row r of the two chunks stacked (rows 0-63 chunk a, 64-127 chunk b), which
-// is also its TMEM lane.  All products are M = 128 tcgen05 MMAs on both chunks
-// at once:
-//   [K_a; K_b] [K_a; K_b]^T   (bf16 straight from TMA; the diagonal 64 x 64
-//                              blocks are K_a K_a^T and K_b K_b^T)
-//   T_d  = inverse of A's 16 x 16 diagonal blocks, forward substitution (fp32)
-//   N    = -T_d A_o           (A_o: A without its diagonal blocks; N^4 = 0)
-//   T    = (I + N)(I + N^2) T_d = Z + N^2 Z,  Z = T_d + N T_d
-//   W    = [T'_a; 0] K_a + [0; T'_b] K_b,  T' = T diag(beta gamma), K reloaded
-//          and converted to fp16 once the inverse no longer needs the space
+// Mapping: one CTA of 128 threads per (pair of chunk slots, head).
+//   [K_a; K_b] [K_a; K_b]^T   one M = 128 tcgen05 MMA, bf16 straight from TMA;
+//                             thread r (TMEM lane r) reads row r of the stacked
+//                             chunks and writes row r of A
+//   T_d = diag(T11, T22)      inverses of (I + A)'s two 32 x 32 diagonal blocks
+//                             by forward substitution on the CUDA cores in fp32,
+//                             one column per thread (2 chunks x 2 blocks x 32
+//                             columns = 128 threads, all with equal work):
+//                             x_t = [t = c] - sum_{j<t} A[t][j] x_j
+//   T21 = -T22 A21 T11        the remaining block of T = (I + A)^-1, by two MMAs:
+//                             N21 = -T22 A21, then T21 = N21 T11
+//   T'' = T diag(beta)        written (fp16) into SW128 tiles that are both the
+//                             staging of the T'' stores and the A operand of W
+//   W = [T''_a; 0] K^_a + [0; T''_b] K^_b,  K^ = diag(gamma) K converted to fp16
+//                             in place once the first MMA has read K
 // The per-chunk B operands sit side by side ([X_a | X_b], N = 128) so one MMA
-// serves both chunks (the off-diagonal 64 x 64 result blocks are unused); for
-// N [N | T_d] the A operand is padded with a zero tile per chunk instead.
+// serves both chunks (the off-diagonal result blocks are unused).
 #include <math.h>
 
 #include "prefill_common.cuh"
@@ -38,14 +41,20 @@ constexpr int kUtThreads = 128;
 constexpr uint32_t kTile = 8192;  // 64 rows x 128 B
 
 // Shared memory (offsets from the 1024-aligned base).
-//   R2 (24 KB): A_o [a | b] -> N_a | 0 | N_b -> N^2 stack (16 KB) -> T'' staging
-//               -> T'_a | 0 | T'_b
-//   R0 (32 KB): K stack -> fp32 diagonal blocks (first 8 KB) + T_d stack (last
-//               16 KB) -> Z [a | b] (first 16 KB) -> K stack again (fp16) -> -W staging
-constexpr uint32_t UT_R2 = 0;
-constexpr uint32_t UT_R0 = 24576;
-constexpr uint32_t UT_TD = UT_R0 + 16384;
-constexpr uint32_t UT_SMALL = UT_R0 + 32768;
+//   UT_X (16 KB): fp32 diagonal blocks of A (8 KB per chunk: rows 0-31 hold
+//                 A11, rows 32-63 hold A22, 128 B per row) -> T_d stack (fp16,
+//                 T_d,a | T_d,b, 64 x 64 SW128 each)
+//   UT_Y (16 KB): A21 of both chunks (fp16, MN-major B: 32 rows x 64 columns,
+//                 4 KB each, columns 32-63 zero) | N21 of both chunks (fp16,
+//                 K-major A rows 0-63, only K 0-31 used)
+//   After the second product UT_X..UT_X+24 KB hold T''_a | zero tile | T''_b.
+//   UT_K (32 KB): K stack (bf16 boxes K_a kb0 | K_b kb0 | K_a kb1 | K_b kb1)
+//                 -> K^ = diag(gamma) K (fp16, in place) -> -W staging
+constexpr uint32_t UT_X = 0;
+constexpr uint32_t UT_Y = 16384;
+constexpr uint32_t UT_N = UT_Y + 8192;
+constexpr uint32_t UT_K = 32768;
+constexpr uint32_t UT_SMALL = UT_K + 32768;
 
 struct UtSmall {
   float G[128];    // cumulative gate per stacked row
@@ -69,18 +78,39 @@ __device__ __forceinline__ uint4 pack8h(const float* x) {
   return u;
 }
 
-__device__ __forceinline__ void unpack8h(uint4 u, float* x) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+// Byte offset of floats 4q..4q+3 (q < 8) of row r of a chunk's fp32 diagonal
+// blocks (rows of 128 B; float4 q of row r sits at q ^ (r % 8), so a warp
+// writing 32 rows at one q meets no bank conflict).
+__device__ __forceinline__ uint32_t af(int r, int q) { return r * 128 + ((q ^ (r & 7)) << 4); }
+
+// Column c (0..31) of (I + B)^-1 for a 32 x 32 diagonal block B of A whose row 0
+// starts at blk (rows 128 B apart, the swizzle of af):
+//   x_t = [t = c] - sum_{j<t} B[t][j] x_j.
+// Every thread reads the same row at the same time (broadcast); four partial
+// sums keep the FMA chains short.
+__device__ __forceinline__ void solve32(const uint8_t* blk, int c, float (&x)[32]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-    x[2 * i] = f.x;
-    x[2 * i + 1] = f.y;
+  for (int t = 0; t < 32; ++t) {
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      if (4 * m < t) {
+        const float4 a4 = *reinterpret_cast<const float4*>(blk + af(t, m));
+        s0 = fmaf(a4.x, x[4 * m], s0);
+        if (4 * m + 1 < t) s1 = fmaf(a4.y, x[4 * m + 1], s1);
+        if (4 * m + 2 < t) s2 = fmaf(a4.z, x[4 * m + 2], s2);
+        if (4 * m + 3 < t) s3 = fmaf(a4.w, x[4 * m + 3], s3);
+      }
+    }
+    const float s = (s0 + s1) + (s2 + s3);
+    x[t] = t > c ? -s : (t == c ? 1.f : 0.f);
   }
 }
 
-// fp32 16-column rows of the diagonal blocks: float4 q of row r at q ^ (r % 4).
-__device__ __forceinline__ float* am_q(float* AM, int r, int q) { return AM + r * 16 + ((q ^ (r & 3)) << 2); }
+// One fp16 element at (row, col) of a 64 x 64 SW128 tile.
+__device__ __forceinline__ void st_h(uint8_t* tile, int row, int col, float v) {
+  *reinterpret_cast<__half*>(tile + row * 128 + (((col >> 3) ^ (row & 7)) << 4) + (col & 7) * 2) = __float2half_rn(v);
+}
 
 // Chunk slot -> sequence (or -1 when the slot holds no chunk).
 __global__ void slot_map_kernel(const PrefillArgs a) {
@@ -110,7 +140,6 @@ __global__ void __launch_bounds__(kUtThreads, 3)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
   UtSmall& sh = *reinterpret_cast<UtSmall*>(sm + UT_SMALL);
-  float* AM = reinterpret_cast<float*>(sm + UT_R0);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int half = tid >> 6, t = tid & 63, r0 = half * 64;
@@ -151,8 +180,8 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     mbar_arrive_expect_tx(&sh.bar_tma, 16384u * ((va ? 1u : 0u) + (vb ? 1u : 0u)));
     for (int hh = 0; hh < 2; ++hh) {
       if (sh.hi[hh] <= sh.lo[hh]) continue;
-      tma_load_3d(sm + UT_R0 + hh * kTile, &tm_k, &sh.bar_tma, 0, h, sh.tf[hh]);
-      tma_load_3d(sm + UT_R0 + 16384 + hh * kTile, &tm_k, &sh.bar_tma, 64, h, sh.tf[hh]);
+      tma_load_3d(sm + UT_K + hh * kTile, &tm_k, &sh.bar_tma, 0, h, sh.tf[hh]);
+      tma_load_3d(sm + UT_K + 16384 + hh * kTile, &tm_k, &sh.bar_tma, 64, h, sh.tf[hh]);
     }
   }
   if (warp == 0) {
@@ -203,8 +232,8 @@ __global__ void __launch_bounds__(kUtThreads, 3)
   if (tid == 0) {
     if (mbar_wait(&sh.bar_tma, 0)) {
       tc_fence_after();
-      tc_mma4(tmem, dK(UT_R0), 2, dK(UT_R0), 2, id_bf16, 0);
-      tc_mma4(tmem, dK(UT_R0 + 16384), 2, dK(UT_R0 + 16384), 2, id_bf16, 1);
+      tc_mma4(tmem, dK(UT_K), 2, dK(UT_K), 2, id_bf16, 0);
+      tc_mma4(tmem, dK(UT_K + 16384), 2, dK(UT_K + 16384), 2, id_bf16, 1);
       tc_commit(&sh.bar_mma);
     } else {
       sh.flag = 1;
@@ -213,15 +242,18 @@ __global__ void __launch_bounds__(kUtThreads, 3)
   __syncthreads();
   bool ok = sh.flag == 0 && wait_all(&sh.bar_mma, 0);
 
-  // ---- A: fp32 diagonal blocks, fp16 A_o (MN-major B of round 1) ----
-  const int dblk = t >> 4;
+  // ---- row t of A: the diagonal block part in fp32, A21 in fp16;
+  //      K -> K^ = diag(gamma) K in fp16 (the MMA has read K) ----
   if (ok) {
-    float x[64];
-    tmem_ld64(lane_addr + r0, x);
+    float kk[64];
+    tmem_ld64(lane_addr + r0, kk);
     const float Gt = sh.G[tid];
-    uint8_t* ao = sm + UT_R2 + half * kTile;
+    uint8_t* arow = sm + UT_X + half * 8192;
+    uint8_t* a21 = sm + UT_Y + half * 4096;
+    const bool lower = t >= 32;  // warp-uniform
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
+      if (q >= 2 && !lower) break;
       float out[16];
       const int jstart = min(16 * q + 15, t - 1);  // last column of the strict lower part
       if (vme && jstart >= 16 * q) {
@@ -230,194 +262,43 @@ __global__ void __launch_bounds__(kUtThreads, 3)
         for (int jj = 15; jj >= 0; --jj) {
           const int j = 16 * q + jj;
           const bool in = (j <= jstart) && (j >= lo);
-          out[jj] = in ? cur * x[j] : 0.f;
+          out[jj] = in ? cur * kk[j] : 0.f;
           if (j <= jstart) cur *= sh.e[r0 + j];
         }
       } else {
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) out[jj] = 0.f;
       }
-      if (q == dblk) {
+      if (lower && q < 2) {
+        *reinterpret_cast<uint4*>(a21 + swz(t - 32, 2 * q)) = pack8h(&out[0]);
+        *reinterpret_cast<uint4*>(a21 + swz(t - 32, 2 * q + 1)) = pack8h(&out[8]);
+      } else {
+        const int qb = 4 * (q & 1);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          *reinterpret_cast<float4*>(am_q(AM, tid, k)) =
+          *reinterpret_cast<float4*>(arow + af(t, qb + k)) =
               make_float4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
-        *reinterpret_cast<uint4*>(ao + swz(t, 2 * q)) = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(ao + swz(t, 2 * q + 1)) = make_uint4(0u, 0u, 0u, 0u);
-      } else {
-        *reinterpret_cast<uint4*>(ao + swz(t, 2 * q)) = pack8h(&out[0]);
-        *reinterpret_cast<uint4*>(ao + swz(t, 2 * q + 1)) = pack8h(&out[8]);
       }
     }
-  }
-  fence_proxy_async();
-  __syncthreads();
-
-  // ---- T_d: thread (chunk, block bb, column jj) solves one column ----
-  if (ok) {
-    const int bb = (tid >> 4) & 3, jj = tid & 15;
-    const int rb = r0 + 16 * bb;
-    float xs[16];
+    if (lower) {
 #pragma unroll
-    for (int tt = 0; tt < 16; ++tt) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int m4 = 0; m4 < 4; ++m4) {
-        if (4 * m4 < tt) {
-          const float4 a4 = *reinterpret_cast<const float4*>(am_q(AM, rb + tt, m4));
-          if (4 * m4 + 0 < tt) acc[0] = fmaf(a4.x, xs[4 * m4 + 0], acc[0]);
-          if (4 * m4 + 1 < tt) acc[1] = fmaf(a4.y, xs[4 * m4 + 1], acc[1]);
-          if (4 * m4 + 2 < tt) acc[2] = fmaf(a4.z, xs[4 * m4 + 2], acc[2]);
-          if (4 * m4 + 3 < tt) acc[3] = fmaf(a4.w, xs[4 * m4 + 3], acc[3]);
-        }
-      }
-      xs[tt] = (tt == jj) ? 1.f : (tt > jj ? -((acc[0] + acc[1]) + (acc[2] + acc[3])) : 0.f);
+      for (int cc = 4; cc < 8; ++cc) *reinterpret_cast<uint4*>(a21 + swz(t - 32, cc)) = make_uint4(0u, 0u, 0u, 0u);
     }
-    __syncthreads();  // every read of A's diagonal blocks is done
-#pragma unroll
-    for (int tt = 0; tt < 16; ++tt) am_q(AM, rb + tt, jj >> 2)[jj & 3] = xs[tt];
-    __syncthreads();
-    float f[16];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float4 v4 = *reinterpret_cast<const float4*>(am_q(AM, tid, k));
-      f[4 * k] = v4.x;
-      f[4 * k + 1] = v4.y;
-      f[4 * k + 2] = v4.z;
-      f[4 * k + 3] = v4.w;
-    }
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      uint4 u = make_uint4(0u, 0u, 0u, 0u);
-      if ((c >> 1) == dblk) u = pack8h(&f[8 * (c & 1)]);
-      *reinterpret_cast<uint4*>(sm + UT_TD + swz(tid, c)) = u;
-    }
-  }
-  fence_proxy_async();
-  tc_fence_before();
-  __syncthreads();
-
-  // ---- round 1: N = -T_d A_o ----
-  if (ok && tid == 0) {
-    tc_fence_after();
-    tc_mma4(tmem, dK(UT_TD), 2, dMN(UT_R2, kTile), 128, id_mnB, 0);
-    tc_commit(&sh.bar_mma);
-  }
-  ok = ok && wait_all(&sh.bar_mma, 1);
-  if (ok) {
-    float d[64];
-    tmem_ld64(lane_addr + r0, d);
-#pragma unroll
-    for (int i = 0; i < 64; ++i) d[i] = -d[i];
-    uint8_t* nt = sm + UT_R2 + half * 16384;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(nt + swz(t, c)) = pack8h(&d[8 * c]);
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      reinterpret_cast<uint4*>(sm + UT_R2 + kTile)[tid + 128 * k] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  fence_proxy_async();
-  tc_fence_before();
-  __syncthreads();
-
-  // ---- round 2: [N^2 | N T_d] = [N_a; 0][N_a | T_d,a] + [0; N_b][N_b | T_d,b] ----
-  if (ok && tid == 0) {
-    tc_fence_after();
-    tc_mma4(tmem, dK(UT_R2), 2, dMN(UT_R2, UT_TD - UT_R2), 128, id_mnB, 0);
-    tc_mma4(tmem, dK(UT_R2 + kTile), 2, dMN(UT_R2 + 16384, UT_TD + kTile - UT_R2 - 16384), 128, id_mnB, 1);
-    tc_commit(&sh.bar_mma);
-  }
-  ok = ok && wait_all(&sh.bar_mma, 0);
-  float z[64];
-  if (ok) {
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      float n2[32], nt[32];
-      tmem_ld32(lane_addr + 32 * hh, n2);
-      tmem_ld32(lane_addr + 64 + 32 * hh, nt);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int cc = 4 * hh + c;
-        float td[8];
-        unpack8h(*reinterpret_cast<const uint4*>(sm + UT_TD + swz(tid, cc)), td);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) z[8 * cc + i] = td[i] + nt[8 * c + i];
-        *reinterpret_cast<uint4*>(sm + UT_R2 + swz(tid, cc)) = pack8h(&n2[8 * c]);
-        *reinterpret_cast<uint4*>(sm + UT_R0 + half * kTile + swz(t, cc)) = pack8h(&z[8 * cc]);
-      }
-    }
-  }
-  fence_proxy_async();
-  tc_fence_before();
-  __syncthreads();
-
-  // ---- round 3: T = Z + N^2 Z;  T'' = T diag(beta) -> workspace ----
-  if (ok && tid == 0) {
-    tc_fence_after();
-    tc_mma4(tmem, dK(UT_R2), 2, dMN(UT_R0, kTile), 128, id_mnB, 0);
-    tc_commit(&sh.bar_mma);
-  }
-  ok = ok && wait_all(&sh.bar_mma, 1);
-  // K again (the inverse has released R0), for W.
-  if (ok && tid == 0) {
-    mbar_arrive_expect_tx(&sh.bar_tma, 16384u * ((va ? 1u : 0u) + (vb ? 1u : 0u)));
-    for (int hh = 0; hh < 2; ++hh) {
-      if (sh.hi[hh] <= sh.lo[hh]) continue;
-      tma_load_3d(sm + UT_R0 + hh * kTile, &tm_k, &sh.bar_tma, 0, h, sh.tf[hh]);
-      tma_load_3d(sm + UT_R0 + 16384 + hh * kTile, &tm_k, &sh.bar_tma, 64, h, sh.tf[hh]);
-    }
-  }
-  float tr[64];  // row t of T'' = T diag(beta)
-  if (ok) {      // T'' rows into a staging tile per chunk (R2 is free again), then TMA stores
-    float d[64];
-    tmem_ld64(lane_addr + r0, d);
-    uint8_t* stg = sm + UT_R2 + half * kTile;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) tr[8 * c + i] = (z[8 * c + i] + d[8 * c + i]) * sh.bet[r0 + 8 * c + i];
-      *reinterpret_cast<uint4*>(stg + swz(t, c)) = pack8h(&tr[8 * c]);
-    }
-  }
-  fence_proxy_async();
-  __syncthreads();
-  if (ok && tid == 0) {
-    for (int hh = 0; hh < 2; ++hh)
-      if (sh.hi[hh] > sh.lo[hh]) tma_store_2d(&tm_t, sm + UT_R2 + hh * kTile, 0, (sh.slot[hh] * H + h) * 64);
-    bulk_commit();
-    bulk_wait_read();
-  }
-  __syncthreads();
-  // T' = T'' diag(gamma) as the A operand of W: [T'_a; 0] and [0; T'_b] from T'_a | 0 | T'_b.
-  if (ok) {
-    uint8_t* tp = sm + UT_R2 + half * 16384;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      float w[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) w[i] = tr[8 * c + i] * sh.gam[r0 + 8 * c + i];
-      *reinterpret_cast<uint4*>(tp + swz(t, c)) = pack8h(w);
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      reinterpret_cast<uint4*>(sm + UT_R2 + kTile)[tid + 128 * k] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  // K (bf16) -> fp16 in place, rows outside each chunk zero.
-  if (ok) {
-    if (!mbar_wait(&sh.bar_tma, 1)) sh.flag = 1;
+#pragma unroll 4
     for (int i = tid; i < 2048; i += kUtThreads) {
       const int box = i >> 9;  // K_a kb0 | K_b kb0 | K_a kb1 | K_b kb1
       const int hh = box & 1, row = (i & 511) >> 3;
-      uint8_t* ptr = sm + UT_R0 + box * kTile + (i & 511) * 16;
+      uint8_t* ptr = sm + UT_K + box * kTile + (i & 511) * 16;
       uint4 out = make_uint4(0u, 0u, 0u, 0u);
       if (row >= sh.lo[hh] && row < sh.hi[hh]) {
+        const float gr = sh.gam[hh * 64 + row];
         const uint4 in = *reinterpret_cast<const uint4*>(ptr);
         const float2 f0 = unpack_bf162(in.x), f1 = unpack_bf162(in.y), f2 = unpack_bf162(in.z),
                      f3 = unpack_bf162(in.w);
-        out.x = pack_half2(f0.x, f0.y);
-        out.y = pack_half2(f1.x, f1.y);
-        out.z = pack_half2(f2.x, f2.y);
-        out.w = pack_half2(f3.x, f3.y);
+        out.x = pack_half2(f0.x * gr, f0.y * gr);
+        out.y = pack_half2(f1.x * gr, f1.y * gr);
+        out.z = pack_half2(f2.x * gr, f2.y * gr);
+        out.w = pack_half2(f3.x * gr, f3.y * gr);
       }
       *reinterpret_cast<uint4*>(ptr) = out;
     }
@@ -425,23 +306,106 @@ __global__ void __launch_bounds__(kUtThreads, 3)
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
-  ok = ok && sh.flag == 0;
 
-  // ---- W = [T'_a; 0] K_a + [0; T'_b] K_b ----
+  // ---- T_d: thread (chunk, block bk, column c) solves column c of block bk ----
+  const int bk = warp & 1;
+  float x[32];
+  if (ok) solve32(sm + UT_X + half * 8192 + bk * 32 * 128, lane, x);
+  __syncthreads();  // every read of the fp32 blocks is done: the space becomes T_d
+  if (ok) {
+    uint8_t* td = sm + UT_X + half * 8192;
+    const int col = 32 * bk + lane;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      st_h(td, 32 * bk + i, col, x[i]);
+      st_h(td, 32 * (1 - bk) + i, col, 0.f);
+    }
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+
+  // ---- N21 = -T22 A21: [T_d,a; T_d,b] (K = 32..63) x [A21_a | A21_b] ----
   if (ok && tid == 0) {
     tc_fence_after();
-    tc_mma4(tmem, dK(UT_R2), 2, dMN(UT_R0, 16384), 128, id_mnB, 0);
-    tc_mma4(tmem, dK(UT_R2 + kTile), 2, dMN(UT_R0 + kTile, 16384), 128, id_mnB, 1);
+    tc_mma2(tmem, dK(UT_X + 64), 2, dMN(UT_Y, 4096), 128, id_mnB, 0);
+    tc_commit(&sh.bar_mma);
+  }
+  ok = ok && wait_all(&sh.bar_mma, 1);
+  if (ok && bk == 1) {  // rows 32-63 of each chunk -> rows 32 h + i of the N21 stack
+    float d[32];
+    tmem_ld32(lane_addr + r0, d);
+    uint8_t* nt = sm + UT_N;
+    const int nr = 32 * half + lane;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      float nv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) nv[i] = -d[8 * cc + i];
+      *reinterpret_cast<uint4*>(nt + swz(nr, cc)) = pack8h(nv);
+    }
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+
+  // ---- T21 = N21 T11: [N21_a; N21_b] (K = 0..31) x [T_d,a | T_d,b] ----
+  if (ok && tid == 0) {
+    tc_fence_after();
+    tc_mma2(tmem, dK(UT_N), 2, dMN(UT_X, 8192), 128, id_mnB, 0);
     tc_commit(&sh.bar_mma);
   }
   ok = ok && wait_all(&sh.bar_mma, 0);
-  // -W rows into staging boxes in R0 (K is no longer needed), then TMA stores.
+
+  // ---- T'' = T diag(beta) into T''_a | 0 | T''_b (T_d, A21 and N21 are dead) ----
+  if (ok) {
+    uint8_t* tile = sm + UT_X + half * 16384;
+    const float bc = sh.bet[tid];
+    const int col = 32 * bk + lane;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) st_h(tile, 32 * bk + i, col, x[i] * bc);
+    if (bk == 1) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) st_h(tile, i, col, 0.f);
+    }
+    if (warp < 2) {  // warp w: T21 of chunk w (TMEM lanes 32 w + i, columns 64 w + j)
+      float d[32];
+      tmem_ld32(lane_addr + 64 * warp, d);
+      uint8_t* tw = sm + UT_X + warp * 16384;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = d[8 * cc + i] * sh.bet[64 * warp + 8 * cc + i];
+        *reinterpret_cast<uint4*>(tw + swz(32 + lane, cc)) = pack8h(v);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      reinterpret_cast<uint4*>(sm + UT_X + kTile)[tid + 128 * k] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+
+  // ---- W = [T''_a; 0] K^_a + [0; T''_b] K^_b;  T'' tiles -> workspace ----
+  if (ok && tid == 0) {
+    tc_fence_after();
+    tc_mma4(tmem, dK(UT_X), 2, dMN(UT_K, 16384), 128, id_mnB, 0);
+    tc_mma4(tmem, dK(UT_X + kTile), 2, dMN(UT_K + kTile, 16384), 128, id_mnB, 1);
+    tc_commit(&sh.bar_mma);
+    for (int hh = 0; hh < 2; ++hh)
+      if (sh.hi[hh] > sh.lo[hh]) tma_store_2d(&tm_t, sm + UT_X + hh * 16384, 0, (sh.slot[hh] * H + h) * 64);
+    bulk_commit();
+  }
+  ok = ok && wait_all(&sh.bar_mma, 1);
+  // -W rows into staging boxes over K^ (the MMA has read it), then TMA stores.
   if (ok) {
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       float w[64];
       tmem_ld64(lane_addr + 64 * hh, w);
-      uint8_t* box = sm + UT_R0 + half * 16384 + hh * kTile;
+      uint8_t* box = sm + UT_K + half * 16384 + hh * kTile;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         float nw[8];
@@ -453,15 +417,16 @@ __global__ void __launch_bounds__(kUtThreads, 3)
   }
   fence_proxy_async();
   __syncthreads();
-  if (ok && tid == 0) {
-    for (int hh = 0; hh < 2; ++hh)
-      if (sh.hi[hh] > sh.lo[hh]) {
-        const int row = (sh.slot[hh] * H + h) * 64;
-        tma_store_2d(&tm_w, sm + UT_R0 + hh * 16384, 0, row);
-        tma_store_2d(&tm_w, sm + UT_R0 + hh * 16384 + kTile, 64, row);
-      }
+  if (tid == 0) {
+    if (ok)
+      for (int hh = 0; hh < 2; ++hh)
+        if (sh.hi[hh] > sh.lo[hh]) {
+          const int row = (sh.slot[hh] * H + h) * 64;
+          tma_store_2d(&tm_w, sm + UT_K + hh * 16384, 0, row);
+          tma_store_2d(&tm_w, sm + UT_K + hh * 16384 + kTile, 64, row);
+        }
     bulk_commit();
-    bulk_wait_all();
+    bulk_wait_read();
   }
   if (!ok && tid == 0) record_error(a.err_word, GDN_DEVERR_TIMEOUT, 0);
   tc_fence_before();
