@@ -38,10 +38,12 @@ struct PrefillArgs {
   int32_t page_size;
   int32_t num_pages;
   int32_t* err_word;
-  // Workspace: chunk slot -> sequence map, then per (chunk slot, head) a
-  // 64 x 64 fp16 tile T'' = (I + A)^-1 diag(beta) and a 64 x 128 fp16 tile
+  // Workspace: per chunk slot its geometry {first token, lo, hi, sequence}
+  // (rows lo..hi-1 of the 64 hold tokens first + lo .. first + hi - 1; hi <= lo
+  // for a slot without a chunk), then per (chunk slot, head) a 64 x 64 fp16
+  // tile T'' = (I + A)^-1 diag(beta) and a 64 x 128 fp16 tile
   // -W = -T'' diag(gamma) K.
-  int32_t* slot_seq;
+  int4* slot_geo;
   __half* tinv;
   __half* wneg;
   int32_t num_slots;
@@ -59,7 +61,7 @@ constexpr uint32_t kTinvBytes = 64 * 64 * 2;  // one T'' tile
 constexpr uint32_t kWBytes = 64 * 128 * 2;    // one -W tile
 
 __host__ __device__ inline size_t workspace_map_bytes(int64_t num_slots) {
-  return static_cast<size_t>((num_slots * 4 + 1023) / 1024 * 1024);
+  return static_cast<size_t>((num_slots * 16 + 1023) / 1024 * 1024);
 }
 __host__ __device__ inline size_t workspace_bytes(int64_t T, int64_t num_seqs, int64_t H) {
   const int64_t ns = num_chunk_slots(T, num_seqs);

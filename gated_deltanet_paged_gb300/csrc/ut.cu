@@ -112,7 +112,8 @@ __device__ __forceinline__ void st_h(uint8_t* tile, int row, int col, float v) {
   *reinterpret_cast<__half*>(tile + row * 128 + (((col >> 3) ^ (row & 7)) << 4) + (col & 7) * 2) = __float2half_rn(v);
 }
 
-// Chunk slot -> sequence (or -1 when the slot holds no chunk).
+// Chunk slot -> {first token of its 64 rows, lo, hi, sequence}; hi <= lo (and
+// sequence -1) when the slot holds no chunk.
 __global__ void slot_map_kernel(const PrefillArgs a) {
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= a.num_slots) return;
@@ -125,12 +126,16 @@ __global__ void slot_map_kernel(const PrefillArgs a) {
     else
       hi = mid - 1;
   }
-  int out = -1, cu_b, L, P;
+  int4 out = make_int4(0, 0, 0, -1);
+  int cu_b, L, P;
   if (seq_extent(a, lo, cu_b, L, P)) {
     const int c = s - slot_base(cu_b, lo);
-    if (c >= 0 && c < chunk_count(P, L)) out = lo;
+    if (c >= 0 && c < chunk_count(P, L)) {
+      const int a0 = (P / 64) * 64 + 64 * c;
+      out = make_int4(cu_b + a0 - P, max(P - a0, 0), min(P + L - a0, 64), lo);
+    }
   }
-  a.slot_seq[s] = out;
+  a.slot_geo[s] = out;
 }
 
 __global__ void __launch_bounds__(kUtThreads, 3)
@@ -147,23 +152,10 @@ __global__ void __launch_bounds__(kUtThreads, 3)
 
   if (t == 0) {
     const int s = 2 * blockIdx.x + half;
-    int tf = 0, lo = 0, hi = 0;
-    if (s < a.num_slots) {
-      const int b = a.slot_seq[s];
-      int cu_b, L, P;
-      if (b >= 0 && seq_extent(a, b, cu_b, L, P)) {
-        const int c = s - slot_base(cu_b, b);
-        if (c >= 0 && c < chunk_count(P, L)) {
-          const int a0 = (P / 64) * 64 + 64 * c;
-          lo = max(P - a0, 0);
-          hi = min(P + L - a0, 64);
-          tf = cu_b + a0 - P;
-        }
-      }
-    }
-    sh.tf[half] = tf;
-    sh.lo[half] = lo;
-    sh.hi[half] = hi;
+    const int4 geo = s < a.num_slots ? a.slot_geo[s] : make_int4(0, 0, 0, -1);
+    sh.tf[half] = geo.x;
+    sh.lo[half] = geo.y;
+    sh.hi[half] = geo.z;
     sh.slot[half] = s;
   }
   __syncthreads();

@@ -217,7 +217,8 @@ int gdn_gated_delta_rule_decode_paged(const gdn_bf16 *q, const gdn_bf16 *k, cons
  * rule (A[t][j] = beta_t exp(G_t - G_j) k_t . k_j, j < t) and
  * -W = -T'' diag(exp(G)) K, and stores them as 64 x 64 and 64 x 128 fp16
  * tiles; the sequential state chain then reads them back.  The workspace holds
- * one int32 per chunk slot and 24 KB per (chunk slot, head), with
+ * 16 bytes per chunk slot (rounded up to 1 KB) and 24 KB per (chunk slot,
+ * head), with
  * total_tokens / 64 + 2 num_seqs + 2 chunk slots. */
 size_t gdn_prefill_workspace_bytes(int32_t num_seqs, int32_t total_tokens, int32_t H);
 
