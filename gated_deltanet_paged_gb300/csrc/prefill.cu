@@ -86,9 +86,9 @@ struct Small {
   // TMA completion
   uint64_t bar_q, bar_v[2], bar_t[2], bar_k[3], bar_w[2];
   // MMA completion (tcgen05.commit)
-  uint64_t bar_p, bar_m2, bar_x, bar_su, bar_o[2];
+  uint64_t bar_p[2], bar_m2, bar_x[2], bar_su[2], bar_o[2];
   // hand-offs between warp groups
-  uint64_t xa_full, mp_ready, m2_ready, u_ready, s16_ready, gates_ready, qt_done, o_read[2];
+  uint64_t xa_full, mp_ready, m2_ready, u_ready, s16_ready, gates_ready[2], qt_done, kt_ready[2], o_read[2];
   uint64_t o_staged, stg_free;  // output staging in the U16 tile
   uint32_t tmem_base;
   int seq;
@@ -233,15 +233,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.bar_t[i], 1);
       mbar_init(&sh.bar_o[i], 1);
       mbar_init(&sh.o_read[i], 128);
+      mbar_init(&sh.bar_p[i], 1);
+      mbar_init(&sh.bar_x[i], 1);
+      mbar_init(&sh.bar_su[i], 1);
+      mbar_init(&sh.gates_ready[i], 1);
+      mbar_init(&sh.kt_ready[i], 128);
     }
     for (int i = 0; i < 3; ++i) mbar_init(&sh.bar_k[i], 1);
-    mbar_init(&sh.bar_p, 1);
     mbar_init(&sh.bar_m2, 1);
-    mbar_init(&sh.bar_x, 1);
-    mbar_init(&sh.bar_su, 1);
-    mbar_init(&sh.xa_full, 1 + 256);  // the prep's leader and every chain thread
-    mbar_init(&sh.gates_ready, 1);
-    mbar_init(&sh.qt_done, 256);
+    mbar_init(&sh.xa_full, 128);  // the chain threads that write Q~
+    mbar_init(&sh.qt_done, 128);
     mbar_init(&sh.mp_ready, 1);
     mbar_init(&sh.m2_ready, 1);
     mbar_init(&sh.u_ready, 128);
@@ -291,14 +292,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t id_kmn = idesc_f16(128, 128, false, false, false, true);
     const uint32_t id_qk = idesc_f16(128, 64, true, true, false, false);
     int cx = 0, px = 0;  // next op of each stream, two per chunk
+    int qx = 1;          // next Q load
     uint64_t t_last = globaltimer_ns();
     while (cx < 2 * nch || px < 2 * nch) {
       bool did = false;
+      if (qx < nch) {  // Q of chunk qx once Q~ and Q K^T of chunk qx-1 have read the buffer
+        const int q = qx - 1;
+        bool ready = mbar_test(&sh.qt_done, q & 1) && mbar_test(&sh.bar_p[q & 1], (q >> 1) & 1);
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        if (ready) {
+          if (lane == 0) tma_q(qx);
+          __syncwarp();
+          ++qx;
+          did = true;
+        }
+      }
       if (cx < 2 * nch) {
         const int c = cx >> 1;
         const uint32_t e = c & 1;
-        bool ready = ((cx & 1) == 0) ? (mbar_test(&sh.xa_full, e) && mbar_test(&sh.s16_ready, e))
-                                     : mbar_test(&sh.u_ready, e);
+        // X(c) also needs U~(c) issued before it (same accumulator) and -W(c) in.
+        bool ready = ((cx & 1) == 0) ? (mbar_test(&sh.xa_full, e) && mbar_test(&sh.s16_ready, e) &&
+                                        px >= 2 * c + 2 && mbar_test(&sh.bar_w[e], (c >> 1) & 1))
+                                     : (mbar_test(&sh.u_ready, e) && mbar_test(&sh.kt_ready[e], (c >> 1) & 1));
         ready = __shfl_sync(0xffffffffu, ready, 0);
         if (ready) {
           tc_fence_after();
@@ -307,10 +322,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if ((cx & 1) == 0) {  // D_X += XA S0^T
               tc_mma4(d, dK(OFF_XA + kTile * e), 2, dK(OFF_S16), 2, id_kk, 1);
               tc_mma4(d, dK(OFF_XA + 24576 + kTile * e), 2, dK(OFF_S16 + 16384), 2, id_kk, 1);
-              tc_commit(&sh.bar_x);
+              tc_commit(&sh.bar_x[e]);
             } else {  // D_SU = U^T K~;  O rows += P U
               tc_mma4(tmem + COL_DSU, dMN(OFF_U16, kTile), 128, dMN(kslot(c), kTile), 128, id_mnmn, 0);
-              tc_commit(&sh.bar_su);
+              tc_commit(&sh.bar_su[e]);
               tc_mma4(d, dK(OFF_P - kTile * (1 - e)), 2, dMN(OFF_U16, kTile), 128, id_kmn, 1);
               tc_commit(&sh.bar_o[e]);
             }
@@ -332,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if ((px & 1) == 0) {  // Q K^T (bf16)
               tc_mma4(tmem + COL_DP, dK(OFF_Q), 2, dK(kslot(p)), 2, id_qk, 0);
               tc_mma4(tmem + COL_DP, dK(OFF_Q + kTile), 2, dK(kslot(p) + kTile), 2, id_qk, 1);
-              tc_commit(&sh.bar_p);
+              tc_commit(&sh.bar_p[e]);
             } else {  // U~ into the U rows of D_X (zeros in the O rows)
               const uint32_t at = OFF_TZT + kTile * e;
               tc_mma4(d, dK(at), 2, dMN(vslot(p), kTile), 128, id_kmn, 0);
@@ -433,7 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t e = p & 1;
       const int lo = chunk_lo(p), hi = chunk_hi(p);
       Gates& gs = sh.gates;
-      // 1. cumulative gate of chunk p and its tables
+      // 1. cumulative gate of chunk p and its tables (slot e: K~ of chunk p-2 has
+      //    finished with its exp(G_C - G))
+      if (p >= 2 && !pwait(&sh.kt_ready[e], ((p - 2) >> 1) & 1)) break;
       if (pw == 0) {
         float s = pg0 + pg1;
 #pragma unroll
@@ -459,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!pwait(&sh.bar_k[p % 3], (p / 3) & 1)) break;
       if (pt == 0) {
         mbar_arrive(&sh.mp_ready);
-        mbar_arrive(&sh.gates_ready);
+        mbar_arrive(&sh.gates_ready[e]);
       }
       // 3. V -> fp16 in place; U~ = T'' V may start once the chunk's D_X is free
       if (!pwait(&sh.bar_v[e], (p >> 1) & 1)) break;
@@ -474,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pt == 0) mbar_arrive(&sh.m2_ready);
       // 4. P = decayed, masked Q K^T (TMEM lanes 0-63) once P U of chunk p-1 has read the
       //    P tile; Q~ and K~ are done by the chain warps
-      if (!pwait(&sh.bar_p, e)) break;
+      if (!pwait(&sh.bar_p[e], (p >> 1) & 1)) break;
       if (p >= 1 && !pwait(&sh.bar_o[(p - 1) & 1], ((p - 1) >> 1) & 1)) break;
       if (tm_reader) {
         const int t = 32 * wq + lane;
@@ -502,21 +519,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async();
       tc_fence_before();
       // 5. -W of chunk p+1 into the buffer X of chunk p-1 has finished with
-      if (p >= 1 && !pwait(&sh.bar_x, (p - 1) & 1)) break;
+      if (p >= 1 && !pwait(&sh.bar_x[(p - 1) & 1], ((p - 1) >> 1) & 1)) break;
       if (pt == 0) {
         if (p >= 1 && p + 1 < nch) tma_w(p + 1);
-        // 6. the chunk is ready once U~ and -W are in
-        if (!mbar_wait_or_abort(&sh.bar_m2, e, abort_flag) ||
-            !mbar_wait_or_abort(&sh.bar_w[e], (p >> 1) & 1, abort_flag))
-          *abort_flag = 1;
+        // 6. V and T'' of chunk p+2 once U~ of chunk p has read their slots
+        if (!mbar_wait_or_abort(&sh.bar_m2, e, abort_flag)) *abort_flag = 1;
         if (p + 2 < nch) {
           tma_v(p + 2);
           tma_t(p + 2);
           // The K slot of chunk p+2 held K~ of chunk p-1 until its U^T K~ finished.
-          if (p >= 1 && !mbar_wait_or_abort(&sh.bar_su, (p - 1) & 1, abort_flag)) *abort_flag = 1;
+          if (p >= 1 && !mbar_wait_or_abort(&sh.bar_su[(p - 1) & 1], ((p - 1) >> 1) & 1, abort_flag))
+            *abort_flag = 1;
           tma_k(p + 2);
         }
-        mbar_arrive(&sh.xa_full);
       }
       psync();
     }
@@ -555,44 +570,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(s16 + swz(v, c)) = pack8h(&S[8 * c]);
     fence_proxy_async();
     mbar_arrive(&sh.s16_ready);
-    // The chain warps' share of chunk q's preparation, done while they would
-    // otherwise wait for it: Q~ = diag(gamma) Q into the Q~ rows of XA (free:
-    // X of chunk q-1 has finished), the next Q load, and K~ = diag(exp(G_C - G)) K
-    // (bf16 -> fp16 in place) once Q K^T has read K.
-    const int ci = tid;  // 0..255
-    auto help_prep = [&](int q) -> bool {
+    // The chain warps' share of chunk q's preparation, in two halves of 128
+    // threads that would otherwise wait: the threads with (wq >> 1) == q % 2
+    // write Q~ = diag(gamma) Q into the Q~ rows of XA (free once X of chunk q-1
+    // has finished) and so release X of chunk q; the others convert K in place
+    // to K~ = diag(exp(G_C - G)) K (fp16) once Q K^T has read it, which U^T K~
+    // of chunk q waits for.
+    const int ci = 32 * (wq & 1) + lane + 64 * hc;  // 0..127 within a half
+    auto qt_part = [&](int q) -> bool {
       const uint32_t eq = q & 1;
       const int lo = chunk_lo(q), hi = chunk_hi(q);
-      if (!cwait(&sh.bar_q, eq) || !cwait(&sh.gates_ready, eq)) return false;
+      if (!cwait(&sh.bar_q, eq) || !cwait(&sh.gates_ready[eq], (q >> 1) & 1)) return false;
       const float* gam = sh.gates.gam[eq];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int i = ci + 256 * k;
+      for (int k = 0; k < 8; ++k) {
+        const int i = ci + 128 * k;
         const int kb = i >> 9, rc = i & 511, row = rc >> 3;
         cvt8(sm + OFF_XA + kb * 24576 + kTile + rc * 16, sm + OFF_Q + kb * kTile + rc * 16, gam[row],
              row >= lo && row < hi);
       }
       fence_proxy_async();
       mbar_arrive(&sh.qt_done);
-      if (ci == 0 && q + 1 < nch) {  // the Q buffer is free once Q~ and Q K^T have read it
-        if (!mbar_wait_or_abort(&sh.qt_done, eq, abort_flag) || !mbar_wait_or_abort(&sh.bar_p, eq, abort_flag)) {
-          *abort_flag = 1;
-          ok = false;
-        } else {
-          tma_q(q + 1);
-        }
-      }
-      if (!cwait(&sh.bar_p, eq)) return false;  // Q K^T has read the bf16 K
+      mbar_arrive(&sh.xa_full);
+      return true;
+    };
+    auto kt_part = [&](int q) -> bool {
+      const uint32_t eq = q & 1;
+      const int lo = chunk_lo(q), hi = chunk_hi(q);
+      if (!cwait(&sh.bar_p[eq], (q >> 1) & 1) || !cwait(&sh.gates_ready[eq], (q >> 1) & 1)) return false;
       const float* ksc = sh.gates.ksc[eq];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int i = ci + 256 * k;
+      for (int k = 0; k < 8; ++k) {
+        const int i = ci + 128 * k;
         const int row = (i & 511) >> 3;
         uint8_t* ptr = sm + kslot(q) + (i >> 9) * kTile + (i & 511) * 16;
         cvt8(ptr, ptr, ksc[row], row >= lo && row < hi);
       }
       fence_proxy_async();
-      mbar_arrive(&sh.xa_full);
+      mbar_arrive(&sh.kt_ready[eq]);
       return true;
     };
     auto store_state = [&](float* pool, int row) {
@@ -600,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i) dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
     };
-    if (!help_prep(0)) ok = false;
+    if (!((wq >> 1) == 0 ? qt_part(0) : kt_part(0))) ok = false;
     for (int c = 0; c < nch && ok; ++c) {
       const uint32_t e = c & 1;
       // U rows of D_X: 0-63 for even chunks, 64-127 for odd ones; the O rows are the others.
@@ -608,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = v & 63;
       const uint32_t dx = lane_addr + COL_DX + 128 * e + 64 * hc;
       if (isU) {  // U -> U16[t][v] (fp16): A of U^T K~ and B of P U
-        if (!cwait(&sh.bar_x, e)) break;
+        if (!cwait(&sh.bar_x[e], (c >> 1) & 1)) break;
         // the previous chunk's outputs were staged in this tile
         if (c >= 1 && !cwait(&sh.stg_free, (c - 1) & 1)) break;
 #pragma unroll
@@ -622,9 +637,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async();
         tc_fence_before();
         mbar_arrive(&sh.u_ready);
+      } else if (c + 1 < nch) {  // Q~ of the next chunk once X of this one has read Q~
+        if (!cwait(&sh.bar_x[e], (c >> 1) & 1) || !qt_part(c + 1)) break;
       }
       // S1 = gamma_C S0 + U^T K~, and its fp16 copy for the next chunk
-      if (!cwait(&sh.bar_su, e)) break;
+      if (!cwait(&sh.bar_su[e], (c >> 1) & 1)) break;
       const float gamC = sh.gamC[c % 3];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -698,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      if (c + 1 < nch && !help_prep(c + 1)) break;
+      if (isU && c + 1 < nch && !kt_part(c + 1)) break;
     }
     bulk_wait_all();
     if (ok && out_row >= 0) store_state(out_pool, out_row);
