@@ -52,7 +52,8 @@ namespace {
 using namespace gdn;
 
 constexpr int kThreads = 512;
-constexpr int kPrepThreads = 224;  // warps 8-14
+constexpr int kPrepThreads = 192;  // warps 8-13
+constexpr int kPrepIssuerWarp = 14;
 constexpr int kIssuerWarp = 15;
 constexpr uint32_t kTile = 8192;  // 64 rows x 128 B
 
@@ -86,7 +87,7 @@ struct Small {
   // TMA completion
   uint64_t bar_q, bar_v[2], bar_t[2], bar_k[3], bar_w[2];
   // MMA completion (tcgen05.commit)
-  uint64_t bar_p[2], bar_m2, bar_x[2], bar_su[2], bar_o[2];
+  uint64_t bar_p[2], bar_m2[2], bar_x[2], bar_su[2], bar_o[2];
   // hand-offs between warp groups
   uint64_t xa_full, mp_ready, m2_ready, u_ready, s16_ready, gates_ready[2], qt_done, kt_ready[2], o_read[2];
   uint64_t o_staged, stg_free;  // output staging in the U16 tile
@@ -238,9 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.bar_su[i], 1);
       mbar_init(&sh.gates_ready[i], 1);
       mbar_init(&sh.kt_ready[i], 128);
+      mbar_init(&sh.bar_m2[i], 1);
     }
     for (int i = 0; i < 3; ++i) mbar_init(&sh.bar_k[i], 1);
-    mbar_init(&sh.bar_m2, 1);
     mbar_init(&sh.xa_full, 128);  // the chain threads that write Q~
     mbar_init(&sh.qt_done, 128);
     mbar_init(&sh.mp_ready, 1);
@@ -285,89 +286,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_rows(&tm_q, OFF_Q, &sh.bar_q, ch);
   };
 
+  // Two issuing warps, so that an MMA of the preparation never holds up one of
+  // the chain (a thread's issue runs almost in step with the tensor core).  Each
+  // stream's operations come in a fixed order, so its issuing thread sleeps in
+  // the wait for the next one's inputs.
   if (warp == kIssuerWarp) {
-    // ================================================================ issuer
+    // ========================================================== chain issuer
     const uint32_t id_kk = idesc_f16(128, 128, false, false, false, false);
     const uint32_t id_mnmn = idesc_f16(128, 128, false, false, true, true);
     const uint32_t id_kmn = idesc_f16(128, 128, false, false, false, true);
-    const uint32_t id_qk = idesc_f16(128, 64, true, true, false, false);
-    int cx = 0, px = 0;  // next op of each stream, two per chunk
-    int qx = 1;          // next Q load
-    uint64_t t_last = globaltimer_ns();
-    while (cx < 2 * nch || px < 2 * nch) {
-      bool did = false;
-      if (qx < nch) {  // Q of chunk qx once Q~ and Q K^T of chunk qx-1 have read the buffer
-        const int q = qx - 1;
-        bool ready = mbar_test(&sh.qt_done, q & 1) && mbar_test(&sh.bar_p[q & 1], (q >> 1) & 1);
-        ready = __shfl_sync(0xffffffffu, ready, 0);
-        if (ready) {
-          if (lane == 0) tma_q(qx);
-          __syncwarp();
-          ++qx;
-          did = true;
+    if (lane == 0) {
+      auto w = [&](uint64_t* bar, uint32_t parity) { return mbar_wait_or_abort(bar, parity, abort_flag); };
+      for (int c = 0; c < nch; ++c) {
+        const uint32_t e = c & 1, ph = (c >> 1) & 1;
+        const uint32_t d = tmem + COL_DX + 128 * e;
+        // D_X += XA S0^T once Q~, S0, -W and U~ (same accumulator) are in
+        if (!w(&sh.xa_full, e) || !w(&sh.s16_ready, e) || !w(&sh.bar_w[e], ph) || !w(&sh.bar_m2[e], ph)) {
+          *abort_flag = 1;
+          break;
         }
-      }
-      if (cx < 2 * nch) {
-        const int c = cx >> 1;
-        const uint32_t e = c & 1;
-        // X(c) also needs U~(c) issued before it (same accumulator) and -W(c) in.
-        bool ready = ((cx & 1) == 0) ? (mbar_test(&sh.xa_full, e) && mbar_test(&sh.s16_ready, e) &&
-                                        px >= 2 * c + 2 && mbar_test(&sh.bar_w[e], (c >> 1) & 1))
-                                     : (mbar_test(&sh.u_ready, e) && mbar_test(&sh.kt_ready[e], (c >> 1) & 1));
-        ready = __shfl_sync(0xffffffffu, ready, 0);
-        if (ready) {
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t d = tmem + COL_DX + 128 * e;
-            if ((cx & 1) == 0) {  // D_X += XA S0^T
-              tc_mma4(d, dK(OFF_XA + kTile * e), 2, dK(OFF_S16), 2, id_kk, 1);
-              tc_mma4(d, dK(OFF_XA + 24576 + kTile * e), 2, dK(OFF_S16 + 16384), 2, id_kk, 1);
-              tc_commit(&sh.bar_x[e]);
-            } else {  // D_SU = U^T K~;  O rows += P U
-              tc_mma4(tmem + COL_DSU, dMN(OFF_U16, kTile), 128, dMN(kslot(c), kTile), 128, id_mnmn, 0);
-              tc_commit(&sh.bar_su[e]);
-              tc_mma4(d, dK(OFF_P - kTile * (1 - e)), 2, dMN(OFF_U16, kTile), 128, id_kmn, 1);
-              tc_commit(&sh.bar_o[e]);
-            }
-          }
-          __syncwarp();
-          ++cx;
-          did = true;
+        tc_fence_after();
+        tc_mma4(d, dK(OFF_XA + kTile * e), 2, dK(OFF_S16), 2, id_kk, 1);
+        tc_mma4(d, dK(OFF_XA + 24576 + kTile * e), 2, dK(OFF_S16 + 16384), 2, id_kk, 1);
+        tc_commit(&sh.bar_x[e]);
+        // D_SU = U^T K~;  O rows += P U
+        if (!w(&sh.u_ready, e) || !w(&sh.kt_ready[e], ph)) {
+          *abort_flag = 1;
+          break;
         }
-      }
-      if (!did && px < 2 * nch) {
-        const int p = px >> 1;
-        const uint32_t e = p & 1;
-        bool ready = ((px & 1) == 0) ? mbar_test(&sh.mp_ready, e) : mbar_test(&sh.m2_ready, e);
-        ready = __shfl_sync(0xffffffffu, ready, 0);
-        if (ready) {
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t d = tmem + COL_DX + 128 * e;
-            if ((px & 1) == 0) {  // Q K^T (bf16)
-              tc_mma4(tmem + COL_DP, dK(OFF_Q), 2, dK(kslot(p)), 2, id_qk, 0);
-              tc_mma4(tmem + COL_DP, dK(OFF_Q + kTile), 2, dK(kslot(p) + kTile), 2, id_qk, 1);
-              tc_commit(&sh.bar_p[e]);
-            } else {  // U~ into the U rows of D_X (zeros in the O rows)
-              const uint32_t at = OFF_TZT + kTile * e;
-              tc_mma4(d, dK(at), 2, dMN(vslot(p), kTile), 128, id_kmn, 0);
-              tc_commit(&sh.bar_m2);
-            }
-          }
-          __syncwarp();
-          ++px;
-          did = true;
-        }
-      }
-      if (did) {
-        t_last = globaltimer_ns();
-      } else if (*abort_flag || globaltimer_ns() - t_last > 2000000000ull) {
-        *abort_flag = 1;
-        break;
-      } else {
-        __nanosleep(32);  // give the issue slots to the working warps
+        tc_fence_after();
+        tc_mma4(tmem + COL_DSU, dMN(OFF_U16, kTile), 128, dMN(kslot(c), kTile), 128, id_mnmn, 0);
+        tc_commit(&sh.bar_su[e]);
+        tc_mma4(d, dK(OFF_P - kTile * (1 - e)), 2, dMN(OFF_U16, kTile), 128, id_kmn, 1);
+        tc_commit(&sh.bar_o[e]);
       }
     }
+    __syncwarp();
+  } else if (warp == kPrepIssuerWarp) {
+    // =========================================================== prep issuer
+    const uint32_t id_kmn = idesc_f16(128, 128, false, false, false, true);
+    const uint32_t id_qk = idesc_f16(128, 64, true, true, false, false);
+    if (lane == 0) {
+      for (int p = 0; p < nch; ++p) {
+        const uint32_t e = p & 1;
+        if (!mbar_wait_or_abort(&sh.mp_ready, e, abort_flag)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();  // Q K^T (bf16)
+        tc_mma4(tmem + COL_DP, dK(OFF_Q), 2, dK(kslot(p)), 2, id_qk, 0);
+        tc_mma4(tmem + COL_DP, dK(OFF_Q + kTile), 2, dK(kslot(p) + kTile), 2, id_qk, 1);
+        tc_commit(&sh.bar_p[e]);
+        if (!mbar_wait_or_abort(&sh.m2_ready, e, abort_flag)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();  // U~ into the U rows of D_X (zeros in the O rows)
+        tc_mma4(tmem + COL_DX + 128 * e, dK(OFF_TZT + kTile * e), 2, dMN(vslot(p), kTile), 128, id_kmn, 0);
+        tc_commit(&sh.bar_m2[e]);
+      }
+    }
+    __syncwarp();
   } else if (warp >= 8) {
     // ================================================================== prep
     const int pt = tid - 256, pw = warp - 8;
@@ -523,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pt == 0) {
         if (p >= 1 && p + 1 < nch) tma_w(p + 1);
         // 6. V and T'' of chunk p+2 once U~ of chunk p has read their slots
-        if (!mbar_wait_or_abort(&sh.bar_m2, e, abort_flag)) *abort_flag = 1;
+        if (!mbar_wait_or_abort(&sh.bar_m2[e], (p >> 1) & 1, abort_flag)) *abort_flag = 1;
         if (p + 2 < nch) {
           tma_v(p + 2);
           tma_t(p + 2);
@@ -598,6 +577,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t eq = q & 1;
       const int lo = chunk_lo(q), hi = chunk_hi(q);
       if (!cwait(&sh.bar_p[eq], (q >> 1) & 1) || !cwait(&sh.gates_ready[eq], (q >> 1) & 1)) return false;
+      // Q of chunk q+1 once Q~ and Q K^T of chunk q have read the buffer
+      if (ci == 0 && q + 1 < nch) {
+        if (!mbar_wait_or_abort(&sh.qt_done, eq, abort_flag)) {
+          *abort_flag = 1;
+          ok = false;
+          return false;
+        }
+        tma_q(q + 1);
+      }
       const float* ksc = sh.gates.ksc[eq];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
