@@ -276,23 +276,27 @@ __global__ void __launch_bounds__(kUtThreads, 3)
 #pragma unroll
       for (int cc = 4; cc < 8; ++cc) *reinterpret_cast<uint4*>(a21 + swz(t - 32, cc)) = make_uint4(0u, 0u, 0u, 0u);
     }
-#pragma unroll 4
-    for (int i = tid; i < 2048; i += kUtThreads) {
-      const int box = i >> 9;  // K_a kb0 | K_b kb0 | K_a kb1 | K_b kb1
-      const int hh = box & 1, row = (i & 511) >> 3;
-      uint8_t* ptr = sm + UT_K + box * kTile + (i & 511) * 16;
-      uint4 out = make_uint4(0u, 0u, 0u, 0u);
-      if (row >= sh.lo[hh] && row < sh.hi[hh]) {
-        const float gr = sh.gam[hh * 64 + row];
-        const uint4 in = *reinterpret_cast<const uint4*>(ptr);
-        const float2 f0 = unpack_bf162(in.x), f1 = unpack_bf162(in.y), f2 = unpack_bf162(in.z),
-                     f3 = unpack_bf162(in.w);
-        out.x = pack_half2(f0.x * gr, f0.y * gr);
-        out.y = pack_half2(f1.x * gr, f1.y * gr);
-        out.z = pack_half2(f2.x * gr, f2.y * gr);
-        out.w = pack_half2(f3.x * gr, f3.y * gr);
+    // In place, four 16-byte pieces per thread in flight at a time.
+    for (int i0 = tid; i0 < 2048; i0 += 4 * kUtThreads) {
+      uint4 in[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) in[k] = *reinterpret_cast<const uint4*>(sm + UT_K + (i0 + k * kUtThreads) * 16);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = i0 + k * kUtThreads;
+        const int hh = (i >> 9) & 1, row = (i & 511) >> 3;  // boxes K_a kb0 | K_b kb0 | K_a kb1 | K_b kb1
+        uint4 out = make_uint4(0u, 0u, 0u, 0u);
+        if (row >= sh.lo[hh] && row < sh.hi[hh]) {
+          const float gr = sh.gam[hh * 64 + row];
+          const float2 f0 = unpack_bf162(in[k].x), f1 = unpack_bf162(in[k].y), f2 = unpack_bf162(in[k].z),
+                       f3 = unpack_bf162(in[k].w);
+          out.x = pack_half2(f0.x * gr, f0.y * gr);
+          out.y = pack_half2(f1.x * gr, f1.y * gr);
+          out.z = pack_half2(f2.x * gr, f2.y * gr);
+          out.w = pack_half2(f3.x * gr, f3.y * gr);
+        }
+        *reinterpret_cast<uint4*>(sm + UT_K + i * 16) = out;
       }
-      *reinterpret_cast<uint4*>(ptr) = out;
     }
   }
   fence_proxy_async();
