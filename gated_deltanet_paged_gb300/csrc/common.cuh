@@ -261,6 +261,17 @@ __device__ __forceinline__ void tc_mma4_ts(uint32_t d, uint32_t a_tmem, uint32_t
       "r"(a_tmem), "r"(astep), "l"(b), "l"(static_cast<uint64_t>(bstep)), "r"(idesc), "r"(acc0)
       : "memory");
 }
+__device__ __forceinline__ void tc_mma2_ts(uint32_t d, uint32_t a_tmem, uint32_t astep, uint64_t b, uint32_t bstep,
+                                           uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b32 a1;\n\t.reg .b64 b1;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 q, %6, %6;\n\t"
+      "add.u32 a1, %1, %2;\n\tadd.s64 b1, %3, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %3, %5, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %5, q;\n\t}\n" ::"r"(d),
+      "r"(a_tmem), "r"(astep), "l"(b), "l"(static_cast<uint64_t>(bstep)), "r"(idesc), "r"(acc0)
+      : "memory");
+}
 
 // Store 16 (8) consecutive 32-bit columns of this thread's TMEM lane and wait.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {

@@ -58,20 +58,20 @@ constexpr int kIssuerWarp = 15;
 constexpr uint32_t kTile = 8192;  // 64 rows x 128 B
 
 // Shared memory (byte offsets from the 1024-aligned base).
-constexpr uint32_t OFF_Q = 0;         // Q bf16 [kb0 | kb1] (one chunk)
-constexpr uint32_t OFF_K = 16384;     // 3 x K [kb0 | kb1]: bf16 -> fp16 -> K~, in place
+constexpr uint32_t OFF_Q = 0;         // 2 x Q bf16 [kb0 | kb1], by chunk parity
+constexpr uint32_t OFF_K = 32768;     // 2 x K [kb0 | kb1]: bf16 -> K~ (fp16), in place; by chunk parity
 constexpr uint32_t OFF_V = 65536;     // 2 x V [kb0 | kb1]: bf16 -> fp16, in place
 constexpr uint32_t OFF_TZT = 98304;   // T''(even chunk) | zero tile | T''(odd chunk)
-constexpr uint32_t OFF_P = 122880;    // P, rows t, K-major
-constexpr uint32_t OFF_XA = 131072;   // per K block (24 KB apart): -W (even) | Q~ | -W (odd)
-constexpr uint32_t OFF_S16 = 180224;  // S0 fp16, K-major B (rows v), [kb0 | kb1]
-constexpr uint32_t OFF_U16 = 212992;  // U fp16 [t][v], MN-major, [v 0-63 | v 64-127]
-constexpr uint32_t OFF_SMALL = 229376;
+constexpr uint32_t OFF_P = 122880;    // 2 x P (rows t, K-major), by chunk parity
+constexpr uint32_t OFF_XA = 139264;   // per K block (32 KB apart): -W (even) | Q~ (even) | Q~ (odd) | -W (odd)
+constexpr uint32_t OFF_OST = 204800;  // outputs of a full chunk, bf16 [v 0-63 | v 64-127], staged for TMA stores
+constexpr uint32_t OFF_SMALL = 221184;
 
-// TMEM columns.
-constexpr uint32_t COL_DX = 0;     // two 128-column accumulators, by chunk parity
-constexpr uint32_t COL_DP = 256;   // Q K^T of the chunk being prepared (rows 0-63, 64 columns)
-constexpr uint32_t COL_DSU = 384;  // U^T K~
+// TMEM columns (lane = state row v).
+constexpr uint32_t COL_DX = 0;     // two 128-column accumulators S0 [XA rows]^T, by chunk parity
+constexpr uint32_t COL_DSU = 256;  // U^T K~
+constexpr uint32_t COL_DP = 384;   // Q K^T of the chunk being prepared (lanes t 0-63, 64 columns)
+constexpr uint32_t COL_SA = 448;   // S0 in fp16 pairs: the A operand of S0 [XA rows]^T
 constexpr uint32_t TMEM_COLS = 512;
 
 struct Gates {       // of the chunk being prepared
@@ -85,12 +85,13 @@ struct Small {
   Gates gates;
   float gamC[4];  // exp(G_C) by chunk, ring of 3 (read by the chain)
   // TMA completion
-  uint64_t bar_q, bar_v[2], bar_t[2], bar_k[3], bar_w[2];
+  uint64_t bar_q[2], bar_v[2], bar_t[2], bar_k[2], bar_w[2];
   // MMA completion (tcgen05.commit)
   uint64_t bar_p[2], bar_m2[2], bar_x[2], bar_su[2], bar_o[2];
   // hand-offs between warp groups
-  uint64_t xa_full, mp_ready, m2_ready, u_ready, s16_ready, gates_ready[2], qt_done, kt_ready[2], o_read[2];
-  uint64_t o_staged, stg_free;  // output staging in the U16 tile
+  uint64_t xa_full, mp_ready, m2_ready, u_ready, s16_ready, gates_ready[2], kt_ready[2], o_read[2];
+  uint64_t o_staged, stg_free;  // output staging tile
+  uint64_t p_ready[2];          // P of a chunk written (the prep's TMEM readers), by parity
   uint32_t tmem_base;
   int seq;
   int flag;
@@ -226,29 +227,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- set-up: barriers, TMEM, the zero tile ----
   if (tid == 0) {
-    mbar_init(&sh.bar_q, 1);
-    mbar_init(&sh.bar_w[0], 1);
-    mbar_init(&sh.bar_w[1], 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.bar_q[i], 1);
+      mbar_init(&sh.bar_w[i], 1);
       mbar_init(&sh.bar_v[i], 1);
       mbar_init(&sh.bar_t[i], 1);
       mbar_init(&sh.bar_o[i], 1);
-      mbar_init(&sh.o_read[i], 128);
+      mbar_init(&sh.o_read[i], 256);
       mbar_init(&sh.bar_p[i], 1);
       mbar_init(&sh.bar_x[i], 1);
       mbar_init(&sh.bar_su[i], 1);
       mbar_init(&sh.gates_ready[i], 1);
-      mbar_init(&sh.kt_ready[i], 128);
+      mbar_init(&sh.kt_ready[i], 256);
       mbar_init(&sh.bar_m2[i], 1);
     }
-    for (int i = 0; i < 3; ++i) mbar_init(&sh.bar_k[i], 1);
-    mbar_init(&sh.xa_full, 128);  // the chain threads that write Q~
-    mbar_init(&sh.qt_done, 128);
+    for (int i = 0; i < 2; ++i) mbar_init(&sh.bar_k[i], 1);
+    mbar_init(&sh.xa_full, 256);  // every chain thread writes a share of Q~
     mbar_init(&sh.mp_ready, 1);
     mbar_init(&sh.m2_ready, 1);
-    mbar_init(&sh.u_ready, 128);
+    mbar_init(&sh.u_ready, 256);
     mbar_init(&sh.s16_ready, 256);
-    mbar_init(&sh.o_staged, 128);
+    mbar_init(&sh.o_staged, 256);
+    mbar_init(&sh.p_ready[0], 128);
+    mbar_init(&sh.p_ready[1], 128);
     mbar_init(&sh.stg_free, 1);
     sh.abort = 0;
     fence_mbar_init();
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto chunk_lo = [&](int ch) { return max(P - chunk_a0(ch), 0); };
   auto chunk_hi = [&](int ch) { return min(end_pos - chunk_a0(ch), kChunk); };
   auto chunk_tf = [&](int ch) { return cu_b + (chunk_a0(ch) - P); };
-  auto kslot = [&](int ch) { return OFF_K + static_cast<uint32_t>(ch % 3) * 16384u; };
+  auto kslot = [&](int ch) { return OFF_K + static_cast<uint32_t>(ch & 1) * 16384u; };
   auto vslot = [&](int ch) { return OFF_V + static_cast<uint32_t>(ch & 1) * 16384u; };
   auto tslot = [&](int ch) { return OFF_TZT + static_cast<uint32_t>(ch & 1) * 16384u; };
   auto dK = [&](uint32_t off) { return sdesc(sbase + off, 16, 1024); };
@@ -281,9 +282,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_load_3d(sm + dst, map, bar, 0, h, chunk_tf(ch));
     tma_load_3d(sm + dst + kTile, map, bar, 64, h, chunk_tf(ch));
   };
+  auto qslot = [&](int ch) { return OFF_Q + static_cast<uint32_t>(ch & 1) * 16384u; };
   auto tma_q = [&](int ch) {
-    mbar_arrive_expect_tx(&sh.bar_q, 16384);
-    tma_rows(&tm_q, OFF_Q, &sh.bar_q, ch);
+    mbar_arrive_expect_tx(&sh.bar_q[ch & 1], 16384);
+    tma_rows(&tm_q, qslot(ch), &sh.bar_q[ch & 1], ch);
+  };
+  // Slot refills, each issued by the thread that learns first that the slot is
+  // free: -W after X, K after U^T K~, V and T'' after U~, Q after Q~ and Q K^T.
+  auto tma_k = [&](int ch) {
+    mbar_arrive_expect_tx(&sh.bar_k[ch & 1], 16384);
+    tma_rows(&tm_k, kslot(ch), &sh.bar_k[ch & 1], ch);
+  };
+  auto tma_v = [&](int ch) {
+    mbar_arrive_expect_tx(&sh.bar_v[ch & 1], 16384);
+    tma_rows(&tm_v, vslot(ch), &sh.bar_v[ch & 1], ch);
+  };
+  auto tma_t = [&](int ch) {
+    mbar_arrive_expect_tx(&sh.bar_t[ch & 1], kTinvBytes);
+    tma_load_2d(sm + tslot(ch), &tm_t, &sh.bar_t[ch & 1], 0, ((slot0 + ch) * H + h) * 64);
+  };
+  // -W of chunk ch straight into its -W buffer of the X operand (by chunk parity).
+  auto tma_w = [&](int ch) {
+    const uint32_t dst = OFF_XA + static_cast<uint32_t>(ch & 1) * 24576u;
+    const int row = ((slot0 + ch) * H + h) * 64;
+    uint64_t* bar = &sh.bar_w[ch & 1];
+    mbar_arrive_expect_tx(bar, kWBytes);
+    tma_load_2d(sm + dst, &tm_w, bar, 0, row);
+    tma_load_2d(sm + dst + 32768, &tm_w, bar, 64, row);
   };
 
   // Two issuing warps, so that an MMA of the preparation never holds up one of
@@ -292,39 +317,61 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the wait for the next one's inputs.
   if (warp == kIssuerWarp) {
     // ========================================================== chain issuer
-    const uint32_t id_kk = idesc_f16(128, 128, false, false, false, false);
-    const uint32_t id_mnmn = idesc_f16(128, 128, false, false, true, true);
-    const uint32_t id_kmn = idesc_f16(128, 128, false, false, false, true);
+    // Per chunk (M = 128 = state rows v, fp32 in TMEM; e = chunk parity; the U
+    // half of D_X is columns 0-63 for even chunks, 64-127 for odd ones):
+    //   D_X  += S0 [XA rows]^T      A: S0 fp16 (TMEM), B: [-W; Q~] or [Q~; -W]
+    //   D_SU  = U^T K~              A: U^T fp16 (TMEM, over the U half), B: K~
+    //   D_X(O half) += U^T P^T      A: U^T, B: P (rows t)
+    // U^T sits in columns [0, 16) and [32, 48) of the U half (each chain thread
+    // packs its 32 values in place), so its K = 64 runs as two pairs of steps.
+    const uint32_t id_x = idesc_f16(128, 128, false, false, false, false);
+    const uint32_t id_su = idesc_f16(128, 128, false, false, false, true);
+    const uint32_t id_o = idesc_f16(128, 64, false, false, false, false);
     if (lane == 0) {
       auto w = [&](uint64_t* bar, uint32_t parity) { return mbar_wait_or_abort(bar, parity, abort_flag); };
       for (int c = 0; c < nch; ++c) {
         const uint32_t e = c & 1, ph = (c >> 1) & 1;
         const uint32_t d = tmem + COL_DX + 128 * e;
-        // D_X += XA S0^T once Q~, S0, -W and U~ (same accumulator) are in
+        const uint32_t ua = d + 64 * e;         // U half
+        const uint32_t od = d + 64 * (1 - e);  // O half
         if (!w(&sh.xa_full, e) || !w(&sh.s16_ready, e) || !w(&sh.bar_w[e], ph) || !w(&sh.bar_m2[e], ph)) {
           *abort_flag = 1;
           break;
         }
+        if (c + 2 < nch) {  // U~ of chunk c has read its V and T'' slots
+          tma_v(c + 2);
+          tma_t(c + 2);
+        }
         tc_fence_after();
-        tc_mma4(d, dK(OFF_XA + kTile * e), 2, dK(OFF_S16), 2, id_kk, 1);
-        tc_mma4(d, dK(OFF_XA + 24576 + kTile * e), 2, dK(OFF_S16 + 16384), 2, id_kk, 1);
+        tc_mma4_ts(d, tmem + COL_SA, 8, dK(OFF_XA + 16384 * e), 2, id_x, 1);
+        tc_mma4_ts(d, tmem + COL_SA + 32, 8, dK(OFF_XA + 32768 + 16384 * e), 2, id_x, 1);
         tc_commit(&sh.bar_x[e]);
-        // D_SU = U^T K~;  O rows += P U
         if (!w(&sh.u_ready, e) || !w(&sh.kt_ready[e], ph)) {
           *abort_flag = 1;
           break;
         }
         tc_fence_after();
-        tc_mma4(tmem + COL_DSU, dMN(OFF_U16, kTile), 128, dMN(kslot(c), kTile), 128, id_mnmn, 0);
+        const uint64_t bk = dMN(kslot(c), kTile), bp = dK(OFF_P + 8192 * e);
+        tc_mma2_ts(tmem + COL_DSU, ua, 8, bk, 128, id_su, 0);
+        tc_mma2_ts(tmem + COL_DSU, ua + 32, 8, bk + 256, 128, id_su, 1);
         tc_commit(&sh.bar_su[e]);
-        tc_mma4(d, dK(OFF_P - kTile * (1 - e)), 2, dMN(OFF_U16, kTile), 128, id_kmn, 1);
+        if (!w(&sh.p_ready[e], ph)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        tc_mma2_ts(od, ua, 8, bp, 2, id_o, 1);
+        tc_mma2_ts(od, ua + 32, 8, bp + 4, 2, id_o, 1);
         tc_commit(&sh.bar_o[e]);
       }
     }
     __syncwarp();
   } else if (warp == kPrepIssuerWarp) {
     // =========================================================== prep issuer
-    const uint32_t id_kmn = idesc_f16(128, 128, false, false, false, true);
+    //   D_P  = [Q; .] K^T                      (bf16 from TMA; rows 0-63)
+    //   D_X  = V^T [T''; 0]^T or V^T [0; T'']^T  (U~^T into the U half, zeros
+    //                                            into the O half)
+    const uint32_t id_m2 = idesc_f16(128, 128, false, false, true, false);
     const uint32_t id_qk = idesc_f16(128, 64, true, true, false, false);
     if (lane == 0) {
       for (int p = 0; p < nch; ++p) {
@@ -333,16 +380,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           *abort_flag = 1;
           break;
         }
-        tc_fence_after();  // Q K^T (bf16)
-        tc_mma4(tmem + COL_DP, dK(OFF_Q), 2, dK(kslot(p)), 2, id_qk, 0);
-        tc_mma4(tmem + COL_DP, dK(OFF_Q + kTile), 2, dK(kslot(p) + kTile), 2, id_qk, 1);
+        tc_fence_after();
+        tc_mma4(tmem + COL_DP, dK(qslot(p)), 2, dK(kslot(p)), 2, id_qk, 0);
+        tc_mma4(tmem + COL_DP, dK(qslot(p) + kTile), 2, dK(kslot(p) + kTile), 2, id_qk, 1);
         tc_commit(&sh.bar_p[e]);
         if (!mbar_wait_or_abort(&sh.m2_ready, e, abort_flag)) {
           *abort_flag = 1;
           break;
         }
-        tc_fence_after();  // U~ into the U rows of D_X (zeros in the O rows)
-        tc_mma4(tmem + COL_DX + 128 * e, dK(OFF_TZT + kTile * e), 2, dMN(vslot(p), kTile), 128, id_kmn, 0);
+        tc_fence_after();
+        tc_mma4(tmem + COL_DX + 128 * e, dMN(vslot(p), kTile), 128, dK(OFF_TZT + kTile * e), 2, id_m2, 0);
         tc_commit(&sh.bar_m2[e]);
       }
     }
@@ -371,27 +418,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       return any == 0;
     };
-    auto tma_k = [&](int ch) {
-      mbar_arrive_expect_tx(&sh.bar_k[ch % 3], 16384);
-      tma_rows(&tm_k, kslot(ch), &sh.bar_k[ch % 3], ch);
-    };
-    auto tma_v = [&](int ch) {
-      mbar_arrive_expect_tx(&sh.bar_v[ch & 1], 16384);
-      tma_rows(&tm_v, vslot(ch), &sh.bar_v[ch & 1], ch);
-    };
-    auto tma_t = [&](int ch) {
-      mbar_arrive_expect_tx(&sh.bar_t[ch & 1], kTinvBytes);
-      tma_load_2d(sm + tslot(ch), &tm_t, &sh.bar_t[ch & 1], 0, ((slot0 + ch) * H + h) * 64);
-    };
-    // -W of chunk ch straight into its -W buffer of the X operand (by chunk parity).
-    auto tma_w = [&](int ch) {
-      const uint32_t dst = OFF_XA + static_cast<uint32_t>(ch & 1) * 16384u;
-      const int row = ((slot0 + ch) * H + h) * 64;
-      uint64_t* bar = &sh.bar_w[ch & 1];
-      mbar_arrive_expect_tx(bar, kWBytes);
-      tma_load_2d(sm + dst, &tm_w, bar, 0, row);
-      tma_load_2d(sm + dst + 24576, &tm_w, bar, 64, row);
-    };
     if (pt == 0) {
       prefetch_tensormap(&tm_o);
       prefetch_tensormap(&tm_q);
@@ -405,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_t(0);
       tma_w(0);
       if (nch > 1) {
+        tma_q(1);
         tma_k(1);
         tma_v(1);
         tma_t(1);
@@ -451,8 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_g(p + 1);
       }
       // 2. Q K^T may start at once (Q and K are in; it has its own TMEM columns)
-      if (!pwait(&sh.bar_q, e)) break;
-      if (!pwait(&sh.bar_k[p % 3], (p / 3) & 1)) break;
+      if (!pwait(&sh.bar_q[e], (p >> 1) & 1)) break;
+      if (!pwait(&sh.bar_k[e], (p >> 1) & 1)) break;
       if (pt == 0) {
         mbar_arrive(&sh.mp_ready);
         mbar_arrive(&sh.gates_ready[e]);
@@ -471,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 4. P = decayed, masked Q K^T (TMEM lanes 0-63) once P U of chunk p-1 has read the
       //    P tile; Q~ and K~ are done by the chain warps
       if (!pwait(&sh.bar_p[e], (p >> 1) & 1)) break;
-      if (p >= 1 && !pwait(&sh.bar_o[(p - 1) & 1], ((p - 1) >> 1) & 1)) break;
+      if (p >= 2 && !pwait(&sh.bar_o[e], ((p - 2) >> 1) & 1)) break;  // U^T P^T of chunk p-2 read this P tile
       if (tm_reader) {
         const int t = 32 * wq + lane;
         float x[32];
@@ -491,31 +518,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) out[jj] = 0.f;
         }
-        uint8_t* pb = sm + OFF_P;
+        uint8_t* pb = sm + OFF_P + 8192 * e;
 #pragma unroll
         for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(pb + swz(t, 4 * ph + c)) = pack8h(&out[8 * c]);
+        fence_proxy_async();
+        mbar_arrive(&sh.p_ready[e]);  // U^T P^T of chunk p may read it
       }
       fence_proxy_async();
       tc_fence_before();
-      // 5. -W of chunk p+1 into the buffer X of chunk p-1 has finished with
-      if (p >= 1 && !pwait(&sh.bar_x[(p - 1) & 1], ((p - 1) >> 1) & 1)) break;
-      if (pt == 0) {
-        if (p >= 1 && p + 1 < nch) tma_w(p + 1);
-        // 6. V and T'' of chunk p+2 once U~ of chunk p has read their slots
-        if (!mbar_wait_or_abort(&sh.bar_m2[e], (p >> 1) & 1, abort_flag)) *abort_flag = 1;
-        if (p + 2 < nch) {
-          tma_v(p + 2);
-          tma_t(p + 2);
-          // The K slot of chunk p+2 held K~ of chunk p-1 until its U^T K~ finished.
-          if (p >= 1 && !mbar_wait_or_abort(&sh.bar_su[(p - 1) & 1], ((p - 1) >> 1) & 1, abort_flag))
-            *abort_flag = 1;
-          tma_k(p + 2);
-        }
-      }
       psync();
     }
   } else {
     // ================================================================= chain
+    // Thread (v, hc): state row v (TMEM lane v) and state columns 64 hc .. 64 hc
+    // + 63 in registers; of each 64-column half of D_X it reads columns 32 hc ..
+    // 32 hc + 31 (tokens t of this chunk).
     const int wq = warp & 3, hc = warp >> 2;
     const int v = 32 * wq + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * wq) << 16);
@@ -544,32 +561,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 64; ++i) S[i] = 0.f;
     }
-    uint8_t* s16 = sm + OFF_S16 + hc * 16384;
+    // S0 in fp16 pairs: the TMEM A operand of the next S0 [XA rows]^T.
+    auto stage_state = [&]() {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(s16 + swz(v, c)) = pack8h(&S[8 * c]);
-    fence_proxy_async();
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = pack_half2(S[32 * hh + 2 * i], S[32 * hh + 2 * i + 1]);
+        tmem_st16(lane_addr + COL_SA + 32 * hc + 16 * hh, w);
+      }
+      tc_fence_before();
+    };
+    stage_state();
     mbar_arrive(&sh.s16_ready);
-    // The chain warps' share of chunk q's preparation, in two halves of 128
-    // threads that would otherwise wait: the threads with (wq >> 1) == q % 2
-    // write Q~ = diag(gamma) Q into the Q~ rows of XA (free once X of chunk q-1
-    // has finished) and so release X of chunk q; the others convert K in place
-    // to K~ = diag(exp(G_C - G)) K (fp16) once Q K^T has read it, which U^T K~
-    // of chunk q waits for.
-    const int ci = 32 * (wq & 1) + lane + 64 * hc;  // 0..127 within a half
+    // The chain warps' share of the preparation, done while they would otherwise
+    // wait.  Q~ of chunk q = diag(gamma) Q goes into its own Q~ tile of XA (by
+    // chunk parity; X of chunk q-2 has read it) and releases X of chunk q.  K~
+    // of chunk q = diag(exp(G_C - G)) K is converted in place (fp16) once Q K^T
+    // has read K, and U^T K~ of chunk q waits for it.  Each thread converts four
+    // of the 1024 16-byte pieces of a tile.
+    const int ci = tid;  // 0..255
     auto qt_part = [&](int q) -> bool {
       const uint32_t eq = q & 1;
       const int lo = chunk_lo(q), hi = chunk_hi(q);
-      if (!cwait(&sh.bar_q, eq) || !cwait(&sh.gates_ready[eq], (q >> 1) & 1)) return false;
+      if (!cwait(&sh.bar_q[eq], (q >> 1) & 1) || !cwait(&sh.gates_ready[eq], (q >> 1) & 1)) return false;
       const float* gam = sh.gates.gam[eq];
+      const uint8_t* src = sm + qslot(q);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int i = ci + 128 * k;
+      for (int k = 0; k < 4; ++k) {
+        const int i = ci + 256 * k;
         const int kb = i >> 9, rc = i & 511, row = rc >> 3;
-        cvt8(sm + OFF_XA + kb * 24576 + kTile + rc * 16, sm + OFF_Q + kb * kTile + rc * 16, gam[row],
-             row >= lo && row < hi);
+        cvt8(sm + OFF_XA + kb * 32768 + 8192 + 8192 * eq + rc * 16, src + i * 16, gam[row], row >= lo && row < hi);
       }
       fence_proxy_async();
-      mbar_arrive(&sh.qt_done);
       mbar_arrive(&sh.xa_full);
       return true;
     };
@@ -577,22 +601,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t eq = q & 1;
       const int lo = chunk_lo(q), hi = chunk_hi(q);
       if (!cwait(&sh.bar_p[eq], (q >> 1) & 1) || !cwait(&sh.gates_ready[eq], (q >> 1) & 1)) return false;
-      // Q of chunk q+1 once Q~ and Q K^T of chunk q have read the buffer
-      if (ci == 0 && q + 1 < nch) {
-        if (!mbar_wait_or_abort(&sh.qt_done, eq, abort_flag)) {
+      // Q of chunk q+2 into the slot of chunk q once its Q~ and Q K^T are done
+      if (ci == 0 && q + 2 < nch) {
+        if (!mbar_wait_or_abort(&sh.xa_full, eq, abort_flag)) {
           *abort_flag = 1;
           ok = false;
           return false;
         }
-        tma_q(q + 1);
+        tma_q(q + 2);
       }
       const float* ksc = sh.gates.ksc[eq];
+      uint8_t* kt = sm + kslot(q);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int i = ci + 128 * k;
+      for (int k = 0; k < 4; ++k) {
+        const int i = ci + 256 * k;
         const int row = (i & 511) >> 3;
-        uint8_t* ptr = sm + kslot(q) + (i >> 9) * kTile + (i & 511) * 16;
-        cvt8(ptr, ptr, ksc[row], row >= lo && row < hi);
+        cvt8(kt + i * 16, kt + i * 16, ksc[row], row >= lo && row < hi);
       }
       fence_proxy_async();
       mbar_arrive(&sh.kt_ready[eq]);
@@ -603,33 +627,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i) dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
     };
-    if (!((wq >> 1) == 0 ? qt_part(0) : kt_part(0))) ok = false;
+    if (!qt_part(0) || !kt_part(0)) ok = false;
     for (int c = 0; c < nch && ok; ++c) {
-      const uint32_t e = c & 1;
-      // U rows of D_X: 0-63 for even chunks, 64-127 for odd ones; the O rows are the others.
-      const bool isU = (wq >> 1) == static_cast<int>(e);
-      const int t = v & 63;
-      const uint32_t dx = lane_addr + COL_DX + 128 * e + 64 * hc;
-      if (isU) {  // U -> U16[t][v] (fp16): A of U^T K~ and B of P U
-        if (!cwait(&sh.bar_x[e], (c >> 1) & 1)) break;
-        // the previous chunk's outputs were staged in this tile
-        if (c >= 1 && !cwait(&sh.stg_free, (c - 1) & 1)) break;
+      const uint32_t e = c & 1, ph = (c >> 1) & 1;
+      const uint32_t dx = lane_addr + COL_DX + 128 * e;
+      const uint32_t uh = dx + 64 * e, oh = dx + 64 * (1 - e);  // U and O halves of D_X
+      // U^T, row v: 32 fp32 values packed in place into 16 fp16 pairs (the A
+      // operand of U^T K~ and U^T P^T)
+      if (!cwait(&sh.bar_x[e], ph)) break;
+      if (tid == 0 && c + 2 < nch) tma_w(c + 2);  // X of chunk c has read its -W buffer
+      {
+        float u[32];
+        tmem_ld32(uh + 32 * hc, u);
+        uint32_t w[16];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float u[32];
-          tmem_ld32(dx + 32 * hh, u);
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-            *reinterpret_cast<uint4*>(sm + OFF_U16 + hc * kTile + swz(t, 4 * hh + cc)) = pack8h(&u[8 * cc]);
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        mbar_arrive(&sh.u_ready);
-      } else if (c + 1 < nch) {  // Q~ of the next chunk once X of this one has read Q~
-        if (!cwait(&sh.bar_x[e], (c >> 1) & 1) || !qt_part(c + 1)) break;
+        for (int i = 0; i < 16; ++i) w[i] = pack_half2(u[2 * i], u[2 * i + 1]);
+        tmem_st16(uh + 32 * hc, w);
       }
+      tc_fence_before();
+      mbar_arrive(&sh.u_ready);
+      // Q~ of the next chunk while U^T K~ runs
+      if (c + 1 < nch && !qt_part(c + 1)) break;
       // S1 = gamma_C S0 + U^T K~, and its fp16 copy for the next chunk
-      if (!cwait(&sh.bar_su[e], (c >> 1) & 1)) break;
+      if (!cwait(&sh.bar_su[e], ph)) break;
+      if (tid == 0 && c + 2 < nch) tma_k(c + 2);  // U^T K~ of chunk c has read its K slot
       const float gamC = sh.gamC[c % 3];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -637,75 +658,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(lane_addr + COL_DSU + 64 * hc + 32 * hh, su);
 #pragma unroll
         for (int i = 0; i < 32; ++i) S[32 * hh + i] = fmaf(gamC, S[32 * hh + i], su[i]);
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-          *reinterpret_cast<uint4*>(s16 + swz(v, 4 * hh + cc)) = pack8h(&S[32 * hh + 8 * cc]);
       }
-      fence_proxy_async();
-      tc_fence_before();
+      stage_state();
       mbar_arrive(&sh.s16_ready);
       const int a_end = chunk_a0(c) + kChunk;
       if (ck_rows && ck_pool && a_end % N == 0 && a_end <= end_pos) {
         const int row = ck_rows[a_end / N - 1 - first_ck];
         if (row >= 0) store_state(ck_pool, row);
       }
-      if (!isU) {
-        // Outputs of chunk c from the O rows.  A full chunk goes through a bf16
-        // staging copy in the U16 tile (free once P U is done) and two TMA
-        // stores; a partial one (first / last of a sequence) row by row, so
-        // that no row of another sequence is touched.
-        if (!cwait(&sh.bar_o[e], (c >> 1) & 1)) break;
-        const int lo = chunk_lo(c), hi = chunk_hi(c);
-        const bool full = lo == 0 && hi == kChunk;
-        uint8_t* stg = sm + OFF_U16 + hc * kTile;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float o[32];
-          tmem_ld32(dx + 32 * hh, o);
-          uint4 w[4];
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            w[cc].x = pack_bf162(a.scale * o[8 * cc], a.scale * o[8 * cc + 1]);
-            w[cc].y = pack_bf162(a.scale * o[8 * cc + 2], a.scale * o[8 * cc + 3]);
-            w[cc].z = pack_bf162(a.scale * o[8 * cc + 4], a.scale * o[8 * cc + 5]);
-            w[cc].w = pack_bf162(a.scale * o[8 * cc + 6], a.scale * o[8 * cc + 7]);
-          }
-          if (full) {
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint4*>(stg + swz(t, 4 * hh + cc)) = w[cc];
-          } else if (t >= lo && t < hi) {
-            uint4* dst = reinterpret_cast<uint4*>(a.o + (static_cast<int64_t>(chunk_tf(c) + t) * H + h) * kDimV +
-                                                  64 * hc + 32 * hh);
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) dst[cc] = w[cc];
-          }
-        }
+      // Outputs of chunk c: column v of O^T for this thread's 32 tokens.  A full
+      // chunk goes through the bf16 staging tile and two TMA stores (thread 0
+      // issues them, and lets the tile go one chunk later, when the stores have
+      // long read it); a partial one (first / last of a sequence) is stored
+      // element by element, so that no row of another sequence is touched.
+      if (!cwait(&sh.bar_o[e], ph)) break;
+      {
+        float o[32];
+        tmem_ld32(oh + 32 * hc, o);
         tc_fence_before();
         mbar_arrive(&sh.o_read[e]);
-        fence_proxy_async();
-        mbar_arrive(&sh.o_staged);
-        bool bad = false;
-        if (lane == 0 && (wq & 1) == 0 && hc == 0) {  // one thread of the group (warp 0 or 2)
-          bad = !mbar_wait_or_abort(&sh.o_staged, c & 1, abort_flag);
-          if (!bad) {
-            if (full) {
-              tma_store_3d(&tm_o, sm + OFF_U16, 0, h, chunk_tf(c));
-              tma_store_3d(&tm_o, sm + OFF_U16 + kTile, 64, h, chunk_tf(c));
-              bulk_commit();
-              bulk_wait_read();
-            }
-            mbar_arrive(&sh.stg_free);
+        const int lo = chunk_lo(c), hi = chunk_hi(c), tf = chunk_tf(c);
+        const bool full = lo == 0 && hi == kChunk;
+        if (tid == 0 && c >= 1) {
+          bulk_wait_read();
+          mbar_arrive(&sh.stg_free);
+        }
+        if (c >= 1 && !cwait(&sh.stg_free, (c - 1) & 1)) break;
+        if (full) {
+          uint8_t* stg = sm + OFF_OST + (v >> 6) * kTile + (v & 7) * 2;
+          const int vc = (v & 63) >> 3;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int t = 32 * hc + i;
+            *reinterpret_cast<__nv_bfloat16*>(stg + t * 128 + ((vc ^ (t & 7)) << 4)) =
+                __float2bfloat16_rn(a.scale * o[i]);
+          }
+          fence_proxy_async();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int t = 32 * hc + i;
+            if (t >= lo && t < hi)
+              a.o[(static_cast<int64_t>(tf + t) * H + h) * kDimV + v] = __float2bfloat16_rn(a.scale * o[i]);
           }
         }
-        if (__shfl_sync(0xffffffffu, bad, 0)) {
-          ok = false;
-          *abort_flag = 1;
-          break;
+        mbar_arrive(&sh.o_staged);
+        if (tid == 0) {
+          if (!cwait(&sh.o_staged, c & 1)) break;
+          if (full) {
+            tma_store_3d(&tm_o, sm + OFF_OST, 0, h, tf);
+            tma_store_3d(&tm_o, sm + OFF_OST + kTile, 64, h, tf);
+          }
+          bulk_commit();
         }
       }
-      if (isU && c + 1 < nch && !kt_part(c + 1)) break;
+      if (c + 1 < nch && !kt_part(c + 1)) break;
     }
-    bulk_wait_all();
+    if (tid == 0) bulk_wait_all();
     if (ok && out_row >= 0) store_state(out_pool, out_row);
   }
 
