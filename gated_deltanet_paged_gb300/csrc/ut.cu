@@ -249,13 +249,18 @@ __global__ void __launch_bounds__(kUtThreads, 3)
       float out[16];
       const int jstart = min(16 * q + 15, t - 1);  // last column of the strict lower part
       if (vme && jstart >= 16 * q) {
-        float cur = bv * expf(Gt - sh.G[r0 + jstart]);
+        // The block's gate values come into registers together (shared-memory
+        // loads would otherwise wait behind the previous block's stores).
+        float eb[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) eb[jj] = sh.e[r0 + 16 * q + jj];
+        float cur = bv * __expf(Gt - sh.G[r0 + jstart]);
 #pragma unroll
         for (int jj = 15; jj >= 0; --jj) {
           const int j = 16 * q + jj;
           const bool in = (j <= jstart) && (j >= lo);
           out[jj] = in ? cur * kk[j] : 0.f;
-          if (j <= jstart) cur *= sh.e[r0 + j];
+          if (j <= jstart) cur *= eb[jj];
         }
       } else {
 #pragma unroll
@@ -276,24 +281,33 @@ __global__ void __launch_bounds__(kUtThreads, 3)
 #pragma unroll
       for (int cc = 4; cc < 8; ++cc) *reinterpret_cast<uint4*>(a21 + swz(t - 32, cc)) = make_uint4(0u, 0u, 0u, 0u);
     }
-    // In place, four 16-byte pieces per thread in flight at a time.
+    // In place; each batch loads its four 16-byte pieces and their gamma values
+    // before any store (a store could alias a later load, so the compiler would
+    // otherwise wait for every load in turn).
+    const int lo0 = sh.lo[0], hi0 = sh.hi[0], lo1 = sh.lo[1], hi1 = sh.hi[1];
     for (int i0 = tid; i0 < 2048; i0 += 4 * kUtThreads) {
       uint4 in[4];
+      float gr[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) in[k] = *reinterpret_cast<const uint4*>(sm + UT_K + (i0 + k * kUtThreads) * 16);
+      for (int k = 0; k < 4; ++k) {
+        const int i = i0 + k * kUtThreads;
+        in[k] = *reinterpret_cast<const uint4*>(sm + UT_K + i * 16);
+        gr[k] = sh.gam[((i >> 9) & 1) * 64 + ((i & 511) >> 3)];
+      }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int i = i0 + k * kUtThreads;
         const int hh = (i >> 9) & 1, row = (i & 511) >> 3;  // boxes K_a kb0 | K_b kb0 | K_a kb1 | K_b kb1
+        const bool keep = hh ? (row >= lo1 && row < hi1) : (row >= lo0 && row < hi0);
         uint4 out = make_uint4(0u, 0u, 0u, 0u);
-        if (row >= sh.lo[hh] && row < sh.hi[hh]) {
-          const float gr = sh.gam[hh * 64 + row];
+        if (keep) {
+          const float g = gr[k];
           const float2 f0 = unpack_bf162(in[k].x), f1 = unpack_bf162(in[k].y), f2 = unpack_bf162(in[k].z),
                        f3 = unpack_bf162(in[k].w);
-          out.x = pack_half2(f0.x * gr, f0.y * gr);
-          out.y = pack_half2(f1.x * gr, f1.y * gr);
-          out.z = pack_half2(f2.x * gr, f2.y * gr);
-          out.w = pack_half2(f3.x * gr, f3.y * gr);
+          out.x = pack_half2(f0.x * g, f0.y * g);
+          out.y = pack_half2(f1.x * g, f1.y * g);
+          out.z = pack_half2(f2.x * g, f2.y * g);
+          out.w = pack_half2(f3.x * g, f3.y * g);
         }
         *reinterpret_cast<uint4*>(sm + UT_K + i * 16) = out;
       }
