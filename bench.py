@@ -40,6 +40,11 @@ BYTES_PER_TOKEN_HEAD = 2 * (2 * K + 2 * V) + 8           # q, k, v, o bf16 + g, 
 STATE_BYTES = V * K * 4                                   # one (row, head) state, fp32
 DECODE_BYTES_PER_SEQ_HEAD = 2 * STATE_BYTES + 2 * (2 * K + 2 * V) + 8   # 132,104
 
+# DRAM bytes (read + write) of one paged prefill call per new token, over all heads:
+# ncu capture of the 4 x 8192-token case (ut_kernel 0.643 GB + prefill_kernel 1.515 GB
+# for 32,768 tokens); the traffic grows in proportion to the tokens.
+PREFILL_TRAFFIC_PER_TOKEN = 2.158e9 / 32768
+TRAFFIC_SOURCE = "ncu dram__bytes_read+write of 4x8192-token call, scaled by tokens"
 PREFILL = dict(S=4, L=65536, H=32, page_size=1152, num_pages=256)
 DECODE = dict(B=256, H=32, page_size=1024, num_pages=10000)
 
@@ -253,7 +258,8 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
                    "tokens_per_step": T, "l2": "inputs larger than L2 (streamed q/k/v/o per step), no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": None, "kernel": "paged prefill call (slot map + chunk-local inverse + state chain)",
+                     "traffic": PREFILL_TRAFFIC_PER_TOKEN * T, "traffic_source": TRAFFIC_SOURCE,
+                     "kernel": "paged prefill call (slot map + chunk-local kernel + state chain)",
                      "kernel_ms": kernel_ms,
                      "algorithmic_bytes": prefill_bytes, "peak_kind": peak_kind},
         "tensor": {"achieved_tflops": prefill_flops / (kernel_ms * 1e-3) / 1e12, "peak_tflops": bf16,

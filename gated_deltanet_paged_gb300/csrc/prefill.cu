@@ -18,29 +18,29 @@
 // which equals the token-by-token recurrence up to rounding.
 //
 // Mapping.  One CTA (16 warps) per chain, chains ordered by decreasing length;
-// the warps are specialised and hand work to each other through mbarriers:
+// the warps are specialised and hand work to each other through mbarriers.
+// The chain runs transposed: TMEM lane = state row v, so the state and U^T
+// are fp16 A operands in TMEM and never pass through shared memory.
 //   - warps 0-7, "chain": the fp32 state in registers (thread = state row v,
-//     64 columns), U read back from TMEM, the state update, the outputs and
-//     the page-boundary / final state stores;
-//   - warps 8-14, "prep": everything of chunk c+1 that does not depend on the
-//     state, while the chain works on chunk c: TMA of Q, K, V, T'' and -W,
-//     gates, V -> fp16, P (decayed, masked Q K^T); the chain warps convert
-//     Q~ = diag(gamma) Q and K~ = diag(exp(G_C - G)) K in their idle time;
-//   - warp 15, "issuer": every tcgen05.mma, in whatever order the two streams
-//     become ready (chain first).  A thread's MMA issue runs almost in step with
-//     the tensor core, so no warp that has other work issues.
-// Per chunk the MMAs are (M = 128, fp32 accumulators in TMEM):
+//     64 columns), U^T packed in place in TMEM, the state update and its fp16
+//     copy, the outputs and the page-boundary / final state stores; Q~ and K~
+//     of the next chunk, and the slot refills they are first to learn about;
+//   - warps 8-13, "prep": gates, V -> fp16 and P (decayed, masked Q K^T) of the
+//     next chunk while the chain works on the current one;
+//   - warp 14 issues the preparation's MMAs, warp 15 the chain's.  A thread's
+//     MMA issue runs almost in step with the tensor core, so one issuer would
+//     let a preparation MMA hold up a chain MMA for its whole duration.
+// Per chunk (M = 128 = state rows v, fp32 accumulators in TMEM; the U half of
+// D_X is its columns 0-63 for even chunks, 64-127 for odd ones):
 //   prep : D_P  = [Q; .] K^T                  (bf16 from TMA; P from rows 0-63)
-//          D_X  = [0; T''] V  or [T''; 0] V   (U~ into the chunk's U rows)
-//   chain: D_X += [Q~; -W] S0^T or [-W; Q~] S0^T   (U rows: U~ - W S0^T = U;
-//                                                   O rows: Q~ S0^T)
-//          D_SU = U^T K~;  D_X += [P_even; P_odd] U (O rows += P U)
-// D_X alternates between two TMEM buffers and its U / O row halves swap with
-// the chunk parity (U rows 0-63 for even chunks), so one zero tile serves both
-// [T''; 0] and [0; T''], one Q~ tile sits between the two -W buffers of the
-// X operand, and one P tile serves both [P; .] and [.; P].  Operands
-// are fp16 (an 11-bit significand keeps written states within 1e-3 relative
-// error; bf16 would not) except Q K^T, which uses the bf16 tiles as loaded.
+//          D_X  = V^T [T''; 0]^T or V^T [0; T'']^T   (U~^T into the U half,
+//                                                      zeros into the O half)
+//   chain: D_X += S0 [-W; Q~]^T or S0 [Q~; -W]^T      (U half: U^T; O half:
+//                                                      (Q~ S0^T)^T)
+//          D_SU = U^T K~;  D_X(O half) += U^T P^T
+// One zero tile serves both [T''; 0] and [0; T''].  Operands are fp16 (an
+// 11-bit significand keeps written states within 1e-3 relative error; bf16
+// would not) except Q K^T, which uses the bf16 tiles as loaded.
 #include <math.h>
 
 #include <mutex>
