@@ -40,21 +40,25 @@ using namespace gdn;
 constexpr int kUtThreads = 128;
 constexpr uint32_t kTile = 8192;  // 64 rows x 128 B
 
-// Shared memory (offsets from the 1024-aligned base).
-//   UT_X (16 KB): fp32 diagonal blocks of A (8 KB per chunk: rows 0-31 hold
-//                 A11, rows 32-63 hold A22, 128 B per row) -> T_d stack (fp16,
-//                 T_d,a | T_d,b, 64 x 64 SW128 each)
-//   UT_Y (16 KB): A21 of both chunks (fp16, MN-major B: 32 rows x 64 columns,
-//                 4 KB each, columns 32-63 zero) | N21 of both chunks (fp16,
-//                 K-major A rows 0-63, only K 0-31 used)
-//   After the second product UT_X..UT_X+24 KB hold T''_a | zero tile | T''_b.
-//   UT_K (32 KB): K stack (bf16 boxes K_a kb0 | K_b kb0 | K_a kb1 | K_b kb1)
-//                 -> K^ = diag(gamma) K (fp16, in place) -> -W staging
-constexpr uint32_t UT_X = 0;
-constexpr uint32_t UT_Y = 16384;
-constexpr uint32_t UT_N = UT_Y + 8192;
-constexpr uint32_t UT_K = 32768;
-constexpr uint32_t UT_SMALL = UT_K + 32768;
+// Shared memory (offsets from the 1024-aligned base): two 32 KB regions that
+// swap roles from one work item to the next.
+//   K region:      K stack (bf16 boxes K_a kb0 | K_b kb0 | K_a kb1 | K_b kb1)
+//                  -> K^ = diag(gamma) K (fp16, in place) -> -W staging
+//   A-tile region: fp32 diagonal blocks of A (8 KB per chunk: rows 0-31 hold A11,
+//                  rows 32-63 hold A22, 128 B per row) -> T_d stack (fp16,
+//                  T_d,a | T_d,b, 64 x 64 SW128 each) in the first 16 KB;
+//                  A21 of both chunks (fp16, MN-major B: 32 rows x 64 columns,
+//                  4 KB each, columns 32-63 zero) -> N21 of both chunks (fp16,
+//                  K-major A rows 0-63, only K 0-31 used) in the second 16 KB;
+//                  as a 128-row A operand N21 reads rows 64-127 from the rest
+//                  of that 16 KB, which stays inside the region whichever
+//                  half of shared memory the region is;
+//                  after the second product T''_a | zero tile | T''_b (24 KB)
+// The next item's K lands in this item's A-tile region once its T'' stores
+// have read it; this item's -W staging becomes the next item's A-tile region
+// once the -W stores have read it.
+constexpr uint32_t UT_REGION = 32768;
+constexpr uint32_t UT_SMALL = 2 * UT_REGION;
 
 struct UtSmall {
   float G[128];    // cumulative gate per stacked row
@@ -64,7 +68,7 @@ struct UtSmall {
   float wsum[4];   // per-warp gate totals for the scan
   uint64_t bar_tma, bar_mma;
   uint32_t tmem_base;
-  int tf[2], lo[2], hi[2], slot[2];
+  int4 geo[2][2];  // [item parity][chunk]: first token, lo, hi, sequence of the chunk slot
   int flag;
 };
 constexpr uint32_t UT_SMEM = UT_SMALL + ((sizeof(UtSmall) + 127) / 128) * 128 + 1024;
@@ -148,64 +152,66 @@ __global__ void __launch_bounds__(kUtThreads, 3)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int half = tid >> 6, t = tid & 63, r0 = half * 64;
-  const int h = blockIdx.y, H = a.H;
+  const int H = a.H;
+  // Work items (pair of chunk slots, head), item = pair * H + head, taken in
+  // strides of the grid by persistent CTAs.  The two 32 KB regions swap roles
+  // from one item to the next (K of item i -> the A tiles of item i+1), so the
+  // next item's K is loaded while this one finishes.
+  const int nitems = ((a.num_slots + 1) / 2) * H;
 
-  if (t == 0) {
-    const int s = 2 * blockIdx.x + half;
-    const int4 geo = s < a.num_slots ? a.slot_geo[s] : make_int4(0, 0, 0, -1);
-    sh.tf[half] = geo.x;
-    sh.lo[half] = geo.y;
-    sh.hi[half] = geo.z;
-    sh.slot[half] = s;
-  }
-  __syncthreads();
-  const bool va = sh.hi[0] > sh.lo[0], vb = sh.hi[1] > sh.lo[1];
-  if (!va && !vb) return;
-  const int lo = sh.lo[half], hi = sh.hi[half], tf = sh.tf[half];
+  // Geometry of item it's two chunk slots into geo[b] (threads t == 0).
+  auto load_geo = [&](int it, int b) {
+    const int s = 2 * (it / H) + half;
+    sh.geo[b][half] = (it < nitems && s < a.num_slots) ? a.slot_geo[s] : make_int4(0, 0, 0, -1);
+  };
+  // K of item it (geometry in geo[b]) into the region at kbase (thread 0).
+  auto issue_k = [&](int it, int b, uint32_t kbase) {
+    const int hd = it % H;
+    uint32_t bytes = 0;
+    for (int hh = 0; hh < 2; ++hh) bytes += sh.geo[b][hh].z > sh.geo[b][hh].y ? 16384u : 0u;
+    mbar_arrive_expect_tx(&sh.bar_tma, bytes);
+    for (int hh = 0; hh < 2; ++hh) {
+      const int4 g = sh.geo[b][hh];
+      if (g.z <= g.y) continue;
+      tma_load_3d(sm + kbase + hh * kTile, &tm_k, &sh.bar_tma, 0, hd, g.x);
+      tma_load_3d(sm + kbase + 16384 + hh * kTile, &tm_k, &sh.bar_tma, 64, hd, g.x);
+    }
+  };
+  // g and beta of row t of this thread's chunk of item it (geometry in geo[b]).
+  float gv_n = 0.f, bv_n = 0.f;
+  auto load_gb = [&](int it, int b) {
+    const int4 g = sh.geo[b][half];
+    gv_n = 0.f;
+    bv_n = 0.f;
+    if (it < nitems && t >= g.y && t < g.z) {
+      const int64_t idx = static_cast<int64_t>(g.x + t) * H + it % H;
+      gv_n = a.g[idx];
+      bv_n = a.beta[idx];
+    }
+  };
 
+  int it = blockIdx.x;
   if (tid == 0) {
     mbar_init(&sh.bar_tma, 1);
     mbar_init(&sh.bar_mma, 1);
     sh.flag = 0;
     fence_mbar_init();
     prefetch_tensormap(&tm_k);
-    mbar_arrive_expect_tx(&sh.bar_tma, 16384u * ((va ? 1u : 0u) + (vb ? 1u : 0u)));
-    for (int hh = 0; hh < 2; ++hh) {
-      if (sh.hi[hh] <= sh.lo[hh]) continue;
-      tma_load_3d(sm + UT_K + hh * kTile, &tm_k, &sh.bar_tma, 0, h, sh.tf[hh]);
-      tma_load_3d(sm + UT_K + 16384 + hh * kTile, &tm_k, &sh.bar_tma, 64, h, sh.tf[hh]);
-    }
+    prefetch_tensormap(&tm_t);
+    prefetch_tensormap(&tm_w);
   }
+  if (t == 0) load_geo(it, 0);
   if (warp == 0) {
     tmem_alloc(&sh.tmem_base, 128);
     tmem_relinquish();
   }
-
-  // Gates of this row; inclusive scan over the chunk's 64 rows.
-  const bool vme = t >= lo && t < hi;
-  float gv = 0.f, bv = 0.f;
-  if (vme) {
-    const int64_t idx = static_cast<int64_t>(tf + t) * H + h;
-    gv = a.g[idx];
-    bv = a.beta[idx];
-  }
-  float s = gv;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, s, off);
-    if (lane >= off) s += y;
-  }
-  if (lane == 31) sh.wsum[warp] = s;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
   const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
-  if (warp & 1) s += sh.wsum[warp - 1];
-  sh.G[tid] = s;
-  sh.e[tid] = expf(gv);
-  sh.bet[tid] = bv;
-  sh.gam[tid] = expf(s);
+  if (tid == 0) issue_k(it, 0, UT_REGION);
+  load_gb(it, 0);
 
   auto dK = [&](uint32_t off) { return sdesc(sbase + off, 16, 1024); };
   auto dMN = [&](uint32_t off, uint32_t lbo) { return sdesc(sbase + off, lbo, 1024); };
@@ -220,224 +226,276 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     return sh.flag == 0;
   };
 
-  // ---- [K_a; K_b] [K_a; K_b]^T ----
-  if (tid == 0) {
-    if (mbar_wait(&sh.bar_tma, 0)) {
+  uint32_t mph = 0;  // parity of the next bar_mma phase
+  auto wait_mma = [&]() -> bool {
+    const bool r = wait_all(&sh.bar_mma, mph);
+    mph ^= 1;
+    return r;
+  };
+
+  bool ok = true;
+  for (int i = 0; it < nitems && ok; ++i, it += gridDim.x) {
+    const int b = i & 1;
+    const uint32_t KB = (i & 1) ? 0u : UT_REGION;  // K, then K^, then the -W staging
+    const uint32_t XB = UT_REGION - KB;            // A blocks, T_d, A21 -> N21, then the T'' tiles
+    const int pair = it / H, h = it % H, nit = it + gridDim.x;
+    const int4 ga = sh.geo[b][0], gb = sh.geo[b][1];
+    const bool va = ga.z > ga.y, vb = gb.z > gb.y;
+    const int lo = half ? gb.y : ga.y, hi = half ? gb.z : ga.z;
+    if (t == 0) load_geo(nit, b ^ 1);
+
+    // Gates of this row; inclusive scan over the chunk's 64 rows.
+    const bool vme = t >= lo && t < hi;
+    const float gv = gv_n, bv = bv_n;
+    float s = gv;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, s, off);
+      if (lane >= off) s += y;
+    }
+    if (lane == 31) sh.wsum[warp] = s;
+    tc_fence_before();  // the previous item's TMEM reads come before this item's first MMA
+    __syncthreads();
+    tc_fence_after();
+    if (warp & 1) s += sh.wsum[warp - 1];
+    sh.G[tid] = s;
+    sh.e[tid] = __expf(gv);
+    sh.bet[tid] = bv;
+    sh.gam[tid] = __expf(s);
+    load_gb(nit, b ^ 1);  // in flight during this item
+
+    // ---- [K_a; K_b] [K_a; K_b]^T ----
+    if (tid == 0) {
+      bulk_wait_read();  // the previous item's -W stores have read this item's A-tile region
+      if (mbar_wait(&sh.bar_tma, i & 1)) {
+        tc_fence_after();
+        if (va || vb) {
+          tc_mma4(tmem, dK(KB), 2, dK(KB), 2, id_bf16, 0);
+          tc_mma4(tmem, dK(KB + 16384), 2, dK(KB + 16384), 2, id_bf16, 1);
+          tc_commit(&sh.bar_mma);
+        }
+      } else {
+        sh.flag = 1;
+      }
+    }
+    __syncthreads();
+    ok = sh.flag == 0;
+    if (!(va || vb)) {  // no chunk in either slot: nothing to compute or store
+      if (ok && tid == 0 && nit < nitems) issue_k(nit, b ^ 1, XB);
+      continue;
+    }
+    ok = ok && wait_mma();
+
+    // ---- row t of A: the diagonal block part in fp32, A21 in fp16;
+    //      K -> K^ = diag(gamma) K in fp16 (the MMA has read K) ----
+    if (ok) {
+      float kk[64];
+      tmem_ld64(lane_addr + r0, kk);
+      const float Gt = sh.G[tid];
+      uint8_t* arow = sm + XB + half * 8192;
+      uint8_t* a21 = sm + XB + 16384 + half * 4096;
+      const bool lower = t >= 32;  // warp-uniform
+  #pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (q >= 2 && !lower) break;
+        float out[16];
+        const int jstart = min(16 * q + 15, t - 1);  // last column of the strict lower part
+        if (vme && jstart >= 16 * q) {
+          // The block's gate values come into registers together (shared-memory
+          // loads would otherwise wait behind the previous block's stores).
+          float eb[16];
+  #pragma unroll
+          for (int jj = 0; jj < 16; ++jj) eb[jj] = sh.e[r0 + 16 * q + jj];
+          float cur = bv * __expf(Gt - sh.G[r0 + jstart]);
+  #pragma unroll
+          for (int jj = 15; jj >= 0; --jj) {
+            const int j = 16 * q + jj;
+            const bool in = (j <= jstart) && (j >= lo);
+            out[jj] = in ? cur * kk[j] : 0.f;
+            if (j <= jstart) cur *= eb[jj];
+          }
+        } else {
+  #pragma unroll
+          for (int jj = 0; jj < 16; ++jj) out[jj] = 0.f;
+        }
+        if (lower && q < 2) {
+          *reinterpret_cast<uint4*>(a21 + swz(t - 32, 2 * q)) = pack8h(&out[0]);
+          *reinterpret_cast<uint4*>(a21 + swz(t - 32, 2 * q + 1)) = pack8h(&out[8]);
+        } else {
+          const int qb = 4 * (q & 1);
+  #pragma unroll
+          for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<float4*>(arow + af(t, qb + k)) =
+                make_float4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
+        }
+      }
+      if (lower) {
+  #pragma unroll
+        for (int cc = 4; cc < 8; ++cc) *reinterpret_cast<uint4*>(a21 + swz(t - 32, cc)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      // In place; each batch loads its four 16-byte pieces and their gamma values
+      // before any store (a store could alias a later load, so the compiler would
+      // otherwise wait for every load in turn).
+      const int lo0 = ga.y, hi0 = ga.z, lo1 = gb.y, hi1 = gb.z;
+      for (int i0 = tid; i0 < 2048; i0 += 4 * kUtThreads) {
+        uint4 in[4];
+        float gr[4];
+  #pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = i0 + k * kUtThreads;
+          in[k] = *reinterpret_cast<const uint4*>(sm + KB + i * 16);
+          gr[k] = sh.gam[((i >> 9) & 1) * 64 + ((i & 511) >> 3)];
+        }
+  #pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = i0 + k * kUtThreads;
+          const int hh = (i >> 9) & 1, row = (i & 511) >> 3;  // boxes K_a kb0 | K_b kb0 | K_a kb1 | K_b kb1
+          const bool keep = hh ? (row >= lo1 && row < hi1) : (row >= lo0 && row < hi0);
+          uint4 out = make_uint4(0u, 0u, 0u, 0u);
+          if (keep) {
+            const float g = gr[k];
+            const float2 f0 = unpack_bf162(in[k].x), f1 = unpack_bf162(in[k].y), f2 = unpack_bf162(in[k].z),
+                         f3 = unpack_bf162(in[k].w);
+            out.x = pack_half2(f0.x * g, f0.y * g);
+            out.y = pack_half2(f1.x * g, f1.y * g);
+            out.z = pack_half2(f2.x * g, f2.y * g);
+            out.w = pack_half2(f3.x * g, f3.y * g);
+          }
+          *reinterpret_cast<uint4*>(sm + KB + i * 16) = out;
+        }
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- T_d: thread (chunk, block bk, column c) solves column c of block bk ----
+    const int bk = warp & 1;
+    float x[32];
+    if (ok) solve32(sm + XB + half * 8192 + bk * 32 * 128, lane, x);
+    __syncthreads();  // every read of the fp32 blocks is done: the space becomes T_d
+    if (ok) {
+      uint8_t* td = sm + XB + half * 8192;
+      const int col = 32 * bk + lane;
+  #pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        st_h(td, 32 * bk + i, col, x[i]);
+        st_h(td, 32 * (1 - bk) + i, col, 0.f);
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- N21 = -T22 A21: [T_d,a; T_d,b] (K = 32..63) x [A21_a | A21_b] ----
+    if (ok && tid == 0) {
       tc_fence_after();
-      tc_mma4(tmem, dK(UT_K), 2, dK(UT_K), 2, id_bf16, 0);
-      tc_mma4(tmem, dK(UT_K + 16384), 2, dK(UT_K + 16384), 2, id_bf16, 1);
+      tc_mma2(tmem, dK(XB + 64), 2, dMN(XB + 16384, 4096), 128, id_mnB, 0);
       tc_commit(&sh.bar_mma);
-    } else {
-      sh.flag = 1;
     }
-  }
-  __syncthreads();
-  bool ok = sh.flag == 0 && wait_all(&sh.bar_mma, 0);
-
-  // ---- row t of A: the diagonal block part in fp32, A21 in fp16;
-  //      K -> K^ = diag(gamma) K in fp16 (the MMA has read K) ----
-  if (ok) {
-    float kk[64];
-    tmem_ld64(lane_addr + r0, kk);
-    const float Gt = sh.G[tid];
-    uint8_t* arow = sm + UT_X + half * 8192;
-    uint8_t* a21 = sm + UT_Y + half * 4096;
-    const bool lower = t >= 32;  // warp-uniform
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (q >= 2 && !lower) break;
-      float out[16];
-      const int jstart = min(16 * q + 15, t - 1);  // last column of the strict lower part
-      if (vme && jstart >= 16 * q) {
-        // The block's gate values come into registers together (shared-memory
-        // loads would otherwise wait behind the previous block's stores).
-        float eb[16];
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) eb[jj] = sh.e[r0 + 16 * q + jj];
-        float cur = bv * __expf(Gt - sh.G[r0 + jstart]);
-#pragma unroll
-        for (int jj = 15; jj >= 0; --jj) {
-          const int j = 16 * q + jj;
-          const bool in = (j <= jstart) && (j >= lo);
-          out[jj] = in ? cur * kk[j] : 0.f;
-          if (j <= jstart) cur *= eb[jj];
-        }
-      } else {
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) out[jj] = 0.f;
-      }
-      if (lower && q < 2) {
-        *reinterpret_cast<uint4*>(a21 + swz(t - 32, 2 * q)) = pack8h(&out[0]);
-        *reinterpret_cast<uint4*>(a21 + swz(t - 32, 2 * q + 1)) = pack8h(&out[8]);
-      } else {
-        const int qb = 4 * (q & 1);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          *reinterpret_cast<float4*>(arow + af(t, qb + k)) =
-              make_float4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
-      }
-    }
-    if (lower) {
-#pragma unroll
-      for (int cc = 4; cc < 8; ++cc) *reinterpret_cast<uint4*>(a21 + swz(t - 32, cc)) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    // In place; each batch loads its four 16-byte pieces and their gamma values
-    // before any store (a store could alias a later load, so the compiler would
-    // otherwise wait for every load in turn).
-    const int lo0 = sh.lo[0], hi0 = sh.hi[0], lo1 = sh.lo[1], hi1 = sh.hi[1];
-    for (int i0 = tid; i0 < 2048; i0 += 4 * kUtThreads) {
-      uint4 in[4];
-      float gr[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int i = i0 + k * kUtThreads;
-        in[k] = *reinterpret_cast<const uint4*>(sm + UT_K + i * 16);
-        gr[k] = sh.gam[((i >> 9) & 1) * 64 + ((i & 511) >> 3)];
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int i = i0 + k * kUtThreads;
-        const int hh = (i >> 9) & 1, row = (i & 511) >> 3;  // boxes K_a kb0 | K_b kb0 | K_a kb1 | K_b kb1
-        const bool keep = hh ? (row >= lo1 && row < hi1) : (row >= lo0 && row < hi0);
-        uint4 out = make_uint4(0u, 0u, 0u, 0u);
-        if (keep) {
-          const float g = gr[k];
-          const float2 f0 = unpack_bf162(in[k].x), f1 = unpack_bf162(in[k].y), f2 = unpack_bf162(in[k].z),
-                       f3 = unpack_bf162(in[k].w);
-          out.x = pack_half2(f0.x * g, f0.y * g);
-          out.y = pack_half2(f1.x * g, f1.y * g);
-          out.z = pack_half2(f2.x * g, f2.y * g);
-          out.w = pack_half2(f3.x * g, f3.y * g);
-        }
-        *reinterpret_cast<uint4*>(sm + UT_K + i * 16) = out;
-      }
-    }
-  }
-  fence_proxy_async();
-  tc_fence_before();
-  __syncthreads();
-
-  // ---- T_d: thread (chunk, block bk, column c) solves column c of block bk ----
-  const int bk = warp & 1;
-  float x[32];
-  if (ok) solve32(sm + UT_X + half * 8192 + bk * 32 * 128, lane, x);
-  __syncthreads();  // every read of the fp32 blocks is done: the space becomes T_d
-  if (ok) {
-    uint8_t* td = sm + UT_X + half * 8192;
-    const int col = 32 * bk + lane;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      st_h(td, 32 * bk + i, col, x[i]);
-      st_h(td, 32 * (1 - bk) + i, col, 0.f);
-    }
-  }
-  fence_proxy_async();
-  tc_fence_before();
-  __syncthreads();
-
-  // ---- N21 = -T22 A21: [T_d,a; T_d,b] (K = 32..63) x [A21_a | A21_b] ----
-  if (ok && tid == 0) {
-    tc_fence_after();
-    tc_mma2(tmem, dK(UT_X + 64), 2, dMN(UT_Y, 4096), 128, id_mnB, 0);
-    tc_commit(&sh.bar_mma);
-  }
-  ok = ok && wait_all(&sh.bar_mma, 1);
-  if (ok && bk == 1) {  // rows 32-63 of each chunk -> rows 32 h + i of the N21 stack
-    float d[32];
-    tmem_ld32(lane_addr + r0, d);
-    uint8_t* nt = sm + UT_N;
-    const int nr = 32 * half + lane;
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      float nv[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) nv[i] = -d[8 * cc + i];
-      *reinterpret_cast<uint4*>(nt + swz(nr, cc)) = pack8h(nv);
-    }
-  }
-  fence_proxy_async();
-  tc_fence_before();
-  __syncthreads();
-
-  // ---- T21 = N21 T11: [N21_a; N21_b] (K = 0..31) x [T_d,a | T_d,b] ----
-  if (ok && tid == 0) {
-    tc_fence_after();
-    tc_mma2(tmem, dK(UT_N), 2, dMN(UT_X, 8192), 128, id_mnB, 0);
-    tc_commit(&sh.bar_mma);
-  }
-  ok = ok && wait_all(&sh.bar_mma, 0);
-
-  // ---- T'' = T diag(beta) into T''_a | 0 | T''_b (T_d, A21 and N21 are dead) ----
-  if (ok) {
-    uint8_t* tile = sm + UT_X + half * 16384;
-    const float bc = sh.bet[tid];
-    const int col = 32 * bk + lane;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) st_h(tile, 32 * bk + i, col, x[i] * bc);
-    if (bk == 1) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) st_h(tile, i, col, 0.f);
-    }
-    if (warp < 2) {  // warp w: T21 of chunk w (TMEM lanes 32 w + i, columns 64 w + j)
+    ok = ok && wait_mma();
+    if (ok && bk == 1) {  // rows 32-63 of each chunk -> rows 32 h + i of the N21 stack
       float d[32];
-      tmem_ld32(lane_addr + 64 * warp, d);
-      uint8_t* tw = sm + UT_X + warp * 16384;
-#pragma unroll
+      tmem_ld32(lane_addr + r0, d);
+      uint8_t* nt = sm + XB + 16384;  // over A21, which round 1 has read
+      const int nr = 32 * half + lane;
+  #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        float v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = d[8 * cc + i] * sh.bet[64 * warp + 8 * cc + i];
-        *reinterpret_cast<uint4*>(tw + swz(32 + lane, cc)) = pack8h(v);
+        float nv[8];
+  #pragma unroll
+        for (int i = 0; i < 8; ++i) nv[i] = -d[8 * cc + i];
+        *reinterpret_cast<uint4*>(nt + swz(nr, cc)) = pack8h(nv);
       }
     }
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      reinterpret_cast<uint4*>(sm + UT_X + kTile)[tid + 128 * k] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  fence_proxy_async();
-  tc_fence_before();
-  __syncthreads();
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
 
-  // ---- W = [T''_a; 0] K^_a + [0; T''_b] K^_b;  T'' tiles -> workspace ----
-  if (ok && tid == 0) {
-    tc_fence_after();
-    tc_mma4(tmem, dK(UT_X), 2, dMN(UT_K, 16384), 128, id_mnB, 0);
-    tc_mma4(tmem, dK(UT_X + kTile), 2, dMN(UT_K + kTile, 16384), 128, id_mnB, 1);
-    tc_commit(&sh.bar_mma);
-    for (int hh = 0; hh < 2; ++hh)
-      if (sh.hi[hh] > sh.lo[hh]) tma_store_2d(&tm_t, sm + UT_X + hh * 16384, 0, (sh.slot[hh] * H + h) * 64);
-    bulk_commit();
-  }
-  ok = ok && wait_all(&sh.bar_mma, 1);
-  // -W rows into staging boxes over K^ (the MMA has read it), then TMA stores.
-  if (ok) {
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      float w[64];
-      tmem_ld64(lane_addr + 64 * hh, w);
-      uint8_t* box = sm + UT_K + half * 16384 + hh * kTile;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        float nw[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) nw[i] = -w[8 * c + i];
-        *reinterpret_cast<uint4*>(box + swz(t, c)) = pack8h(nw);
+    // ---- T21 = N21 T11: [N21_a; N21_b] (K = 0..31) x [T_d,a | T_d,b] ----
+    if (ok && tid == 0) {
+      tc_fence_after();
+      tc_mma2(tmem, dK(XB + 16384), 2, dMN(XB, 8192), 128, id_mnB, 0);
+      tc_commit(&sh.bar_mma);
+    }
+    ok = ok && wait_mma();
+
+    // ---- T'' = T diag(beta) into T''_a | 0 | T''_b (T_d, A21 and N21 are dead) ----
+    if (ok) {
+      uint8_t* tile = sm + XB + half * 16384;
+      const float bc = sh.bet[tid];
+      const int col = 32 * bk + lane;
+  #pragma unroll
+      for (int i = 0; i < 32; ++i) st_h(tile, 32 * bk + i, col, x[i] * bc);
+      if (bk == 1) {
+  #pragma unroll
+        for (int i = 0; i < 32; ++i) st_h(tile, i, col, 0.f);
+      }
+      if (warp < 2) {  // warp w: T21 of chunk w (TMEM lanes 32 w + i, columns 64 w + j)
+        float d[32];
+        tmem_ld32(lane_addr + 64 * warp, d);
+        uint8_t* tw = sm + XB + warp * 16384;
+  #pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          float v[8];
+  #pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = d[8 * cc + i] * sh.bet[64 * warp + 8 * cc + i];
+          *reinterpret_cast<uint4*>(tw + swz(32 + lane, cc)) = pack8h(v);
+        }
+      }
+  #pragma unroll
+      for (int k = 0; k < 4; ++k)
+        reinterpret_cast<uint4*>(sm + XB + kTile)[tid + 128 * k] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- W = [T''_a; 0] K^_a + [0; T''_b] K^_b;  T'' tiles -> workspace ----
+    if (ok && tid == 0) {
+      tc_fence_after();
+      tc_mma4(tmem, dK(XB), 2, dMN(KB, 16384), 128, id_mnB, 0);
+      tc_mma4(tmem, dK(XB + kTile), 2, dMN(KB + kTile, 16384), 128, id_mnB, 1);
+      tc_commit(&sh.bar_mma);
+      for (int hh = 0; hh < 2; ++hh)
+        if (hh ? vb : va) tma_store_2d(&tm_t, sm + XB + hh * 16384, 0, ((2 * pair + hh) * H + h) * 64);
+      bulk_commit();
+    }
+    ok = ok && wait_mma();
+    // The T'' stores have read the A-tile region: the next item's K may land there.
+    if (ok && tid == 0 && nit < nitems) {
+      bulk_wait_read();
+      issue_k(nit, b ^ 1, XB);
+    }
+    // -W rows into staging boxes over K^ (the MMA has read it), then TMA stores.
+    if (ok) {
+  #pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float w[64];
+        tmem_ld64(lane_addr + 64 * hh, w);
+        uint8_t* box = sm + KB + half * 16384 + hh * kTile;
+  #pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          float nw[8];
+  #pragma unroll
+          for (int i = 0; i < 8; ++i) nw[i] = -w[8 * c + i];
+          *reinterpret_cast<uint4*>(box + swz(t, c)) = pack8h(nw);
+        }
       }
     }
+    fence_proxy_async();
+    __syncthreads();
+    if (tid == 0) {
+      if (ok)
+        for (int hh = 0; hh < 2; ++hh)
+          if (hh ? vb : va) {
+            const int row = ((2 * pair + hh) * H + h) * 64;
+            tma_store_2d(&tm_w, sm + KB + hh * 16384, 0, row);
+            tma_store_2d(&tm_w, sm + KB + hh * 16384 + kTile, 64, row);
+          }
+      bulk_commit();  // read before the next item writes its A tiles here
+    }
   }
-  fence_proxy_async();
-  __syncthreads();
-  if (tid == 0) {
-    if (ok)
-      for (int hh = 0; hh < 2; ++hh)
-        if (sh.hi[hh] > sh.lo[hh]) {
-          const int row = (sh.slot[hh] * H + h) * 64;
-          tma_store_2d(&tm_w, sm + UT_K + hh * 16384, 0, row);
-          tma_store_2d(&tm_w, sm + UT_K + hh * 16384 + kTile, 64, row);
-        }
-    bulk_commit();
-    bulk_wait_read();
-  }
+  if (tid == 0) bulk_wait_read();
   if (!ok && tid == 0) record_error(a.err_word, GDN_DEVERR_TIMEOUT, 0);
   tc_fence_before();
   __syncthreads();
@@ -465,7 +523,17 @@ int launch_chunk_inverse(const PrefillArgs& a, const void* k, cudaStream_t strea
     cudaGetLastError();
     return GDN_ERR_CUDA;
   }
-  const dim3 grid(static_cast<unsigned>((a.num_slots + 1) / 2), static_cast<unsigned>(a.H));
+  // Persistent CTAs: three per SM (the shared-memory and register budget), each
+  // taking work items in strides of the grid.
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return GDN_ERR_CUDA;
+    num_sms = n;
+  }
+  const long long items = static_cast<long long>((a.num_slots + 1) / 2) * a.H;
+  const unsigned grid = static_cast<unsigned>(items < 3LL * num_sms ? items : 3LL * num_sms);
   ut_kernel<<<grid, kUtThreads, UT_SMEM, stream>>>(mk, mt, mw, a);
   return gdn_host::launch_status();
 }
