@@ -390,6 +390,7 @@ int encode_tokens_map(CUtensorMap* map, const void* base, int64_t T, int64_t H, 
 // Encode a 2-D fp16 tensor map over [rows, cols] (cols a multiple of 64) with
 // a box of 64 x 64 and 128-byte swizzle.
 int encode_tiles_map_f16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols);
+int encode_tokens_map_32(CUtensorMap* map, const void* base, int64_t T, int64_t H, int64_t D);
 
 inline int launch_status() { return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
 

@@ -64,7 +64,7 @@ constexpr uint32_t OFF_V = 65536;     // 2 x V [kb0 | kb1]: bf16 -> fp16, in pla
 constexpr uint32_t OFF_TZT = 98304;   // T''(even chunk) | zero tile | T''(odd chunk)
 constexpr uint32_t OFF_P = 122880;    // 2 x P (rows t, K-major), by chunk parity
 constexpr uint32_t OFF_XA = 139264;   // per K block (32 KB apart): -W (even) | Q~ (even) | Q~ (odd) | -W (odd)
-constexpr uint32_t OFF_OST = 204800;  // outputs of a full chunk, bf16 [v 0-63 | v 64-127], staged for TMA stores
+constexpr uint32_t OFF_OST = 204800;  // outputs of a full chunk: 2 KB per chain warp (32 tokens x 32 columns, bf16)
 constexpr uint32_t OFF_SMALL = 221184;
 
 // TMEM columns (lane = state row v).
@@ -90,7 +90,6 @@ struct Small {
   uint64_t bar_p[2], bar_m2[2], bar_x[2], bar_su[2], bar_o[2];
   // hand-offs between warp groups
   uint64_t xa_full, mp_ready, m2_ready, u_ready, s16_ready, gates_ready[2], kt_ready[2], o_read[2];
-  uint64_t o_staged, stg_free;  // output staging tile
   uint64_t p_ready[2];          // P of a chunk written (the prep's TMEM readers), by parity
   uint32_t tmem_base;
   int seq;
@@ -247,10 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.m2_ready, 1);
     mbar_init(&sh.u_ready, 256);
     mbar_init(&sh.s16_ready, 256);
-    mbar_init(&sh.o_staged, 256);
     mbar_init(&sh.p_ready[0], 128);
     mbar_init(&sh.p_ready[1], 128);
-    mbar_init(&sh.stg_free, 1);
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -666,11 +663,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = ck_rows[a_end / N - 1 - first_ck];
         if (row >= 0) store_state(ck_pool, row);
       }
-      // Outputs of chunk c: column v of O^T for this thread's 32 tokens.  A full
-      // chunk goes through the bf16 staging tile and two TMA stores (thread 0
-      // issues them, and lets the tile go one chunk later, when the stores have
-      // long read it); a partial one (first / last of a sequence) is stored
-      // element by element, so that no row of another sequence is touched.
+      // Outputs of chunk c: column v of O^T for this thread's 32 tokens.  In a
+      // full chunk each warp stages its 32 x 32 block (64-byte rows, a warp's
+      // stores fill a row) and stores it with one TMA store of its own, so no
+      // warp waits for another; a partial chunk (first / last of a sequence) is
+      // stored element by element, so that no row of another sequence is touched.
       if (!cwait(&sh.bar_o[e], ph)) break;
       {
         float o[32];
@@ -678,22 +675,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&sh.o_read[e]);
         const int lo = chunk_lo(c), hi = chunk_hi(c), tf = chunk_tf(c);
-        const bool full = lo == 0 && hi == kChunk;
-        if (tid == 0 && c >= 1) {
-          bulk_wait_read();
-          mbar_arrive(&sh.stg_free);
-        }
-        if (c >= 1 && !cwait(&sh.stg_free, (c - 1) & 1)) break;
-        if (full) {
-          uint8_t* stg = sm + OFF_OST + (v >> 6) * kTile + (v & 7) * 2;
-          const int vc = (v & 63) >> 3;
+        if (lo == 0 && hi == kChunk) {
+          uint8_t* stg = sm + OFF_OST + warp * 2048;
+          if (lane == 0) bulk_wait_read();  // this warp's previous store has read the block
+          __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int t = 32 * hc + i;
-            *reinterpret_cast<__nv_bfloat16*>(stg + t * 128 + ((vc ^ (t & 7)) << 4)) =
-                __float2bfloat16_rn(a.scale * o[i]);
-          }
+          for (int i = 0; i < 32; ++i)
+            *reinterpret_cast<__nv_bfloat16*>(stg + i * 64 + lane * 2) = __float2bfloat16_rn(a.scale * o[i]);
           fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tm_o, stg, 32 * wq, h, tf + 32 * hc);
+            bulk_commit();
+          }
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -702,19 +696,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               a.o[(static_cast<int64_t>(tf + t) * H + h) * kDimV + v] = __float2bfloat16_rn(a.scale * o[i]);
           }
         }
-        mbar_arrive(&sh.o_staged);
-        if (tid == 0) {
-          if (!cwait(&sh.o_staged, c & 1)) break;
-          if (full) {
-            tma_store_3d(&tm_o, sm + OFF_OST, 0, h, tf);
-            tma_store_3d(&tm_o, sm + OFF_OST + kTile, 64, h, tf);
-          }
-          bulk_commit();
-        }
       }
       if (c + 1 < nch && !kt_part(c + 1)) break;
     }
-    if (tid == 0) bulk_wait_all();
+    if (lane == 0) bulk_wait_all();
     if (ok && out_row >= 0) store_state(out_pool, out_row);
   }
 
@@ -744,7 +729,7 @@ int launch(PrefillArgs& a, const void* q, const void* k, const void* v, void* wo
   if (gdn_host::encode_tokens_map(&mq, q, a.T, a.H, kDimK) != GDN_OK ||
       gdn_host::encode_tokens_map(&mk, k, a.T, a.H, kDimK) != GDN_OK ||
       gdn_host::encode_tokens_map(&mv, v, a.T, a.H, kDimV) != GDN_OK ||
-      gdn_host::encode_tokens_map(&mo, a.o, a.T, a.H, kDimV) != GDN_OK ||
+      gdn_host::encode_tokens_map_32(&mo, a.o, a.T, a.H, kDimV) != GDN_OK ||
       gdn_host::encode_tiles_map_f16(&mt, a.tinv, ns * a.H * 64, 64) != GDN_OK ||
       gdn_host::encode_tiles_map_f16(&mw, a.wneg, ns * a.H * 64, 128) != GDN_OK)
     return GDN_ERR_CUDA;
