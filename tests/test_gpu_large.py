@@ -168,3 +168,43 @@ def test_long_context_prefill_then_decode():
         errs.state = max(errs.state, float(e.max()))
         assert e.max() <= S_TOL
     print("long context 4 x 65536, H=32, then 128 decode steps: %r" % errs)
+
+
+def test_prefill_and_decode_are_deterministic():
+    """The kernels do no atomic or order-dependent arithmetic, so repeating a
+    call on the same inputs gives the same bits.  Runs the prefill of a
+    multi-chunk, multi-page workload (4 x 16,384 tokens, H = 32: many chunk-local
+    work items per CTA, page-boundary stores, every warp role of the chain busy)
+    and the full decode batch three times each; any race between the kernels'
+    warp roles or CTAs would show as a difference between the repeats."""
+    w = workloads.long_context("cuda", L=16384, decode_steps=0)
+    pre = w.calls[0]
+    outs, pools = [], []
+    for _ in range(3):
+        pool = w.pool.clone()
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        o = gdn.gdn_chunk_gated_delta_rule_paged(pre.q, pre.k, pre.v, pre.g, pre.beta, pre.cu_seqlens, pool,
+                                                 pre.page_indices, pre.page_indptr, pre.page_size,
+                                                 pre.last_page_len, scale=SCALE, err_word=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        outs.append(o)
+        pools.append(pool)
+    for r in (1, 2):
+        assert torch.equal(outs[0].view(torch.int16), outs[r].view(torch.int16)), "prefill outputs differ"
+        assert bits_equal(pools[0], pools[r]), "prefill states differ"
+
+    wd = workloads.decode_batch("cuda")  # 21 GB pool: one extra copy at a time
+    dc = wd.calls[0]
+    first = None
+    for _ in range(3):
+        dpool = wd.pool.clone()
+        od = gdn.gdn_gated_delta_rule_decode_paged(dc.q, dc.k, dc.v, dc.g, dc.beta, dpool, dc.page_indices,
+                                                   dc.page_indptr, dc.last_page_len, scale=SCALE)
+        torch.cuda.synchronize()
+        if first is None:
+            first = (od, dpool)
+        else:
+            assert torch.equal(first[0].view(torch.int16), od.view(torch.int16)), "decode outputs differ"
+            assert bits_equal(first[1], dpool), "decode states differ"
+        del dpool
