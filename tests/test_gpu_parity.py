@@ -76,6 +76,18 @@ def test_ragged_prefixes_and_tails(case, decay):
     print("ragged case %d decay=%g: %r" % (case, decay, errs))
 
 
+@pytest.mark.parametrize("H", [1, 3, 5])
+def test_head_counts_that_are_not_powers_of_two(H):
+    """The chunk-local kernel's work items (chunk pair x head) and the chain's
+    grid (sequence x head) both map through H; odd head counts (and one head)
+    run the ragged prefixes / lengths of the page_size 128 case."""
+    ps, lens, prefixes = RAGGED[2]
+    call, pool = _ragged_case(200 + H, ps, lens, prefixes, H=H)
+    errs = Errors()
+    prefill_paged_both(call, pool.cuda(), pool.numpy().copy(), errs)
+    print("H=%d ragged case 2: %r" % (H, errs))
+
+
 def test_split_prompt_matches_single_call_on_gpu():
     """Chunked prefill can split a prompt at any token: a 173 + 527 split on the
     GPU equals one 700-token GPU call within the state tolerance."""
