@@ -264,6 +264,42 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     sh.gam[tid] = __expf(s);
     load_gb(nit, b ^ 1);  // in flight during this item
 
+    // K -> K^ = diag(gamma) K in fp16, in place (the first MMA has read K), in two
+    // halves done while the two small MMA rounds run.  Each batch loads its four
+    // 16-byte pieces and their gamma values before any store (a store could alias
+    // a later load, so the compiler would otherwise wait for every load in turn).
+    auto khat_half = [&](int part) {
+      const int lo0 = ga.y, hi0 = ga.z, lo1 = gb.y, hi1 = gb.z;
+      for (int i0 = tid + 1024 * part; i0 < 1024 * (part + 1); i0 += 4 * kUtThreads) {
+        uint4 in[4];
+        float gr[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = i0 + k * kUtThreads;
+          in[k] = *reinterpret_cast<const uint4*>(sm + KB + i * 16);
+          gr[k] = sh.gam[((i >> 9) & 1) * 64 + ((i & 511) >> 3)];
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = i0 + k * kUtThreads;
+          const int hh = (i >> 9) & 1, row = (i & 511) >> 3;  // boxes K_a kb0 | K_b kb0 | K_a kb1 | K_b kb1
+          const bool keep = hh ? (row >= lo1 && row < hi1) : (row >= lo0 && row < hi0);
+          uint4 out = make_uint4(0u, 0u, 0u, 0u);
+          if (keep) {
+            const float g = gr[k];
+            const float2 f0 = unpack_bf162(in[k].x), f1 = unpack_bf162(in[k].y), f2 = unpack_bf162(in[k].z),
+                         f3 = unpack_bf162(in[k].w);
+            out.x = pack_half2(f0.x * g, f0.y * g);
+            out.y = pack_half2(f1.x * g, f1.y * g);
+            out.z = pack_half2(f2.x * g, f2.y * g);
+            out.w = pack_half2(f3.x * g, f3.y * g);
+          }
+          *reinterpret_cast<uint4*>(sm + KB + i * 16) = out;
+        }
+      }
+      fence_proxy_async();
+    };
+
     // ---- [K_a; K_b] [K_a; K_b]^T ----
     if (tid == 0) {
       bulk_wait_read();  // the previous item's -W stores have read this item's A-tile region
@@ -286,8 +322,7 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     }
     ok = ok && wait_mma();
 
-    // ---- row t of A: the diagonal block part in fp32, A21 in fp16;
-    //      K -> K^ = diag(gamma) K in fp16 (the MMA has read K) ----
+    // ---- row t of A: the diagonal block part in fp32, A21 in fp16 ----
     if (ok) {
       float kk[64];
       tmem_ld64(lane_addr + r0, kk);
@@ -333,37 +368,6 @@ __global__ void __launch_bounds__(kUtThreads, 3)
   #pragma unroll
         for (int cc = 4; cc < 8; ++cc) *reinterpret_cast<uint4*>(a21 + swz(t - 32, cc)) = make_uint4(0u, 0u, 0u, 0u);
       }
-      // In place; each batch loads its four 16-byte pieces and their gamma values
-      // before any store (a store could alias a later load, so the compiler would
-      // otherwise wait for every load in turn).
-      const int lo0 = ga.y, hi0 = ga.z, lo1 = gb.y, hi1 = gb.z;
-      for (int i0 = tid; i0 < 2048; i0 += 4 * kUtThreads) {
-        uint4 in[4];
-        float gr[4];
-  #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int i = i0 + k * kUtThreads;
-          in[k] = *reinterpret_cast<const uint4*>(sm + KB + i * 16);
-          gr[k] = sh.gam[((i >> 9) & 1) * 64 + ((i & 511) >> 3)];
-        }
-  #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int i = i0 + k * kUtThreads;
-          const int hh = (i >> 9) & 1, row = (i & 511) >> 3;  // boxes K_a kb0 | K_b kb0 | K_a kb1 | K_b kb1
-          const bool keep = hh ? (row >= lo1 && row < hi1) : (row >= lo0 && row < hi0);
-          uint4 out = make_uint4(0u, 0u, 0u, 0u);
-          if (keep) {
-            const float g = gr[k];
-            const float2 f0 = unpack_bf162(in[k].x), f1 = unpack_bf162(in[k].y), f2 = unpack_bf162(in[k].z),
-                         f3 = unpack_bf162(in[k].w);
-            out.x = pack_half2(f0.x * g, f0.y * g);
-            out.y = pack_half2(f1.x * g, f1.y * g);
-            out.z = pack_half2(f2.x * g, f2.y * g);
-            out.w = pack_half2(f3.x * g, f3.y * g);
-          }
-          *reinterpret_cast<uint4*>(sm + KB + i * 16) = out;
-        }
-      }
     }
     fence_proxy_async();
     tc_fence_before();
@@ -387,12 +391,14 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     tc_fence_before();
     __syncthreads();
 
-    // ---- N21 = -T22 A21: [T_d,a; T_d,b] (K = 32..63) x [A21_a | A21_b] ----
+    // ---- N21 = -T22 A21: [T_d,a; T_d,b] (K = 32..63) x [A21_a | A21_b];
+    //      the first half of K^ while it runs ----
     if (ok && tid == 0) {
       tc_fence_after();
       tc_mma2(tmem, dK(XB + 64), 2, dMN(XB + 16384, 4096), 128, id_mnB, 0);
       tc_commit(&sh.bar_mma);
     }
+    if (ok) khat_half(0);
     ok = ok && wait_mma();
     if (ok && bk == 1) {  // rows 32-63 of each chunk -> rows 32 h + i of the N21 stack
       float d[32];
@@ -411,12 +417,14 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     tc_fence_before();
     __syncthreads();
 
-    // ---- T21 = N21 T11: [N21_a; N21_b] (K = 0..31) x [T_d,a | T_d,b] ----
+    // ---- T21 = N21 T11: [N21_a; N21_b] (K = 0..31) x [T_d,a | T_d,b]; the second
+    //      half of K^ while it runs ----
     if (ok && tid == 0) {
       tc_fence_after();
       tc_mma2(tmem, dK(XB + 16384), 2, dMN(XB, 8192), 128, id_mnB, 0);
       tc_commit(&sh.bar_mma);
     }
+    if (ok) khat_half(1);
     ok = ok && wait_mma();
 
     // ---- T'' = T diag(beta) into T''_a | 0 | T''_b (T_d, A21 and N21 are dead) ----
