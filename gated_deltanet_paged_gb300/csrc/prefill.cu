@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) mbar_init(&sh.bar_k[i], 1);
     mbar_init(&sh.xa_full, 256);  // every chain thread writes a share of Q~
     mbar_init(&sh.mp_ready, 1);
-    mbar_init(&sh.m2_ready, 1);
+    mbar_init(&sh.m2_ready, kPrepThreads);  // every preparation thread converts a share of V
     mbar_init(&sh.u_ready, 256);
     mbar_init(&sh.s16_ready, 256);
     mbar_init(&sh.p_ready[0], 128);
@@ -335,14 +335,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           *abort_flag = 1;
           break;
         }
-        if (c + 2 < nch) {  // U~ of chunk c has read its V and T'' slots
-          tma_v(c + 2);
-          tma_t(c + 2);
-        }
         tc_fence_after();
         tc_mma4_ts(d, tmem + COL_SA, 8, dK(OFF_XA + 16384 * e), 2, id_x, 1);
         tc_mma4_ts(d, tmem + COL_SA + 32, 8, dK(OFF_XA + 32768 + 16384 * e), 2, id_x, 1);
         tc_commit(&sh.bar_x[e]);
+        if (c + 2 < nch) {  // U~ of chunk c has read its V and T'' slots
+          tma_v(c + 2);
+          tma_t(c + 2);
+        }
         if (!w(&sh.u_ready, e) || !w(&sh.kt_ready[e], ph)) {
           *abort_flag = 1;
           break;
@@ -370,18 +370,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     //                                            into the O half)
     const uint32_t id_m2 = idesc_f16(128, 128, false, false, true, false);
     const uint32_t id_qk = idesc_f16(128, 64, true, true, false, false);
+    // Q K^T is committed only once the chunk's V conversion is in (m2_ready):
+    // the preparation threads learn of it (bar_p) before they can arrive on
+    // m2_ready or mp_ready for the next chunk, so neither barrier can run a
+    // phase ahead of this thread.
     if (lane == 0) {
+      auto w = [&](uint64_t* bar, uint32_t parity) { return mbar_wait_or_abort(bar, parity, abort_flag); };
       for (int p = 0; p < nch; ++p) {
-        const uint32_t e = p & 1;
-        if (!mbar_wait_or_abort(&sh.mp_ready, e, abort_flag)) {
+        const uint32_t e = p & 1, ph = (p >> 1) & 1;
+        if (!w(&sh.mp_ready, e)) {
           *abort_flag = 1;
           break;
         }
         tc_fence_after();
         tc_mma4(tmem + COL_DP, dK(qslot(p)), 2, dK(kslot(p)), 2, id_qk, 0);
         tc_mma4(tmem + COL_DP, dK(qslot(p) + kTile), 2, dK(kslot(p) + kTile), 2, id_qk, 1);
+        // U~ = T'' V once V is in fp16, T'' has landed and the O readout of chunk
+        // p-2 has emptied this D_X half
+        if (!w(&sh.m2_ready, e)) {
+          *abort_flag = 1;
+          break;
+        }
         tc_commit(&sh.bar_p[e]);
-        if (!mbar_wait_or_abort(&sh.m2_ready, e, abort_flag)) {
+        if (!w(&sh.bar_t[e], ph) || (p >= 2 && !w(&sh.o_read[e], ph ^ 1))) {
           *abort_flag = 1;
           break;
         }
@@ -397,22 +408,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp & 3, ph = pw >> 2;
     const bool tm_reader = wq < 2;                      // warps 8, 9, 12, 13: TMEM lanes 0-63
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * wq) << 16);
-    auto psync = [&]() { asm volatile("bar.sync 2, %0;" ::"r"(kPrepThreads) : "memory"); };
-    // One thread waits; the whole group learns the outcome at once.
+    // Every thread waits for what it needs itself; a thread whose wait fails
+    // skips its work, and the group agrees on stopping once per chunk, at the
+    // barrier that closes it.
+    bool ok = true;
     auto pwait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      uint32_t bad = 0;
-      if (pt == 0 && !mbar_wait_or_abort(bar, parity, abort_flag)) {
-        bad = 1;
+      if (ok && !mbar_wait_or_abort(bar, parity, abort_flag)) {
+        ok = false;
         *abort_flag = 1;
       }
+      tc_fence_after();
+      return ok;
+    };
+    auto pclose = [&]() -> bool {
       uint32_t any;
       asm volatile(
-          "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+          "{\n\t.reg .pred p, q;\n\tsetp.eq.u32 p, %1, 0;\n\t"
           "bar.red.or.pred q, 2, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}\n"
           : "=r"(any)
-          : "r"(bad), "r"(kPrepThreads)
+          : "r"(ok ? 1u : 0u), "r"(kPrepThreads)
           : "memory");
-      tc_fence_after();
       return any == 0;
     };
     if (pt == 0) {
@@ -451,11 +466,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t e = p & 1;
       const int lo = chunk_lo(p), hi = chunk_hi(p);
       Gates& gs = sh.gates;
-      // 1. cumulative gate of chunk p and its tables (slot e: K~ of chunk p-2 has
-      //    finished with its exp(G_C - G))
-      if (p >= 2 && !pwait(&sh.kt_ready[e], ((p - 2) >> 1) & 1)) break;
+      // 1. warp 8: cumulative gate of chunk p and its tables (slot e: K~ of chunk
+      //    p-2 has finished with its exp(G_C - G)); Q K^T may start once Q and K
+      //    are in (it has its own TMEM columns)
       if (pw == 0) {
-        float s = pg0 + pg1;
+        // warp-uniform, so that the shuffles below see every lane
+        const bool go = __all_sync(0xffffffffu, p < 2 || pwait(&sh.kt_ready[e], ((p - 2) >> 1) & 1));
+        float s = go ? pg0 + pg1 : 0.f;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
           const float y = __shfl_up_sync(0xffffffffu, s, off);
@@ -463,40 +480,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float G0 = s - pg1, G1 = s;
         const float GC = __shfl_sync(0xffffffffu, s, 31);
-        gs.G[2 * lane] = G0;
-        gs.G[2 * lane + 1] = G1;
-        gs.e[2 * lane] = __expf(pg0);
-        gs.e[2 * lane + 1] = __expf(pg1);
-        gs.gam[e][2 * lane] = __expf(G0);
-        gs.gam[e][2 * lane + 1] = __expf(G1);
-        gs.ksc[e][2 * lane] = __expf(GC - G0);
-        gs.ksc[e][2 * lane + 1] = __expf(GC - G1);
-        if (lane == 0) sh.gamC[p % 3] = __expf(GC);
-        prefetch_g(p + 1);
+        if (go) {
+          gs.G[2 * lane] = G0;
+          gs.G[2 * lane + 1] = G1;
+          gs.e[2 * lane] = __expf(pg0);
+          gs.e[2 * lane + 1] = __expf(pg1);
+          gs.gam[e][2 * lane] = __expf(G0);
+          gs.gam[e][2 * lane + 1] = __expf(G1);
+          gs.ksc[e][2 * lane] = __expf(GC - G0);
+          gs.ksc[e][2 * lane + 1] = __expf(GC - G1);
+          if (lane == 0) sh.gamC[p % 3] = __expf(GC);
+          prefetch_g(p + 1);
+        }
+        __syncwarp();
+        if (lane == 0 && go && pwait(&sh.bar_q[e], (p >> 1) & 1) && pwait(&sh.bar_k[e], (p >> 1) & 1)) {
+          mbar_arrive(&sh.mp_ready);
+          mbar_arrive(&sh.gates_ready[e]);
+        }
       }
-      // 2. Q K^T may start at once (Q and K are in; it has its own TMEM columns)
-      if (!pwait(&sh.bar_q[e], (p >> 1) & 1)) break;
-      if (!pwait(&sh.bar_k[e], (p >> 1) & 1)) break;
-      if (pt == 0) {
-        mbar_arrive(&sh.mp_ready);
-        mbar_arrive(&sh.gates_ready[e]);
+      // 2. V -> fp16 in place; U~ = T'' V follows (its issuer waits for T'' and
+      //    for the chunk's D_X half)
+      if (pwait(&sh.bar_v[e], (p >> 1) & 1)) {
+        for (int i = pt; i < 1024; i += kPrepThreads) {
+          const int row = (i & 511) >> 3;
+          uint8_t* ptr = sm + vslot(p) + (i >> 9) * kTile + (i & 511) * 16;
+          cvt8(ptr, ptr, 1.f, row >= lo && row < hi);
+        }
+        fence_proxy_async();
+        mbar_arrive(&sh.m2_ready);
       }
-      // 3. V -> fp16 in place; U~ = T'' V may start once the chunk's D_X is free
-      if (!pwait(&sh.bar_v[e], (p >> 1) & 1)) break;
-      for (int i = pt; i < 1024; i += kPrepThreads) {
-        const int row = (i & 511) >> 3;
-        uint8_t* ptr = sm + vslot(p) + (i >> 9) * kTile + (i & 511) * 16;
-        cvt8(ptr, ptr, 1.f, row >= lo && row < hi);
-      }
-      fence_proxy_async();
-      if (!pwait(&sh.bar_t[e], (p >> 1) & 1)) break;
-      if (p >= 2 && !pwait(&sh.o_read[e], ((p - 2) >> 1) & 1)) break;
-      if (pt == 0) mbar_arrive(&sh.m2_ready);
-      // 4. P = decayed, masked Q K^T (TMEM lanes 0-63) once P U of chunk p-1 has read the
-      //    P tile; Q~ and K~ are done by the chain warps
-      if (!pwait(&sh.bar_p[e], (p >> 1) & 1)) break;
-      if (p >= 2 && !pwait(&sh.bar_o[e], ((p - 2) >> 1) & 1)) break;  // U^T P^T of chunk p-2 read this P tile
-      if (tm_reader) {
+      // 3. P = decayed, masked Q K^T (TMEM lanes 0-63) once U^T P^T of chunk p-2
+      //    has read this P tile; warps other than 8 read its gate tables
+      if (tm_reader && pwait(&sh.bar_p[e], (p >> 1) & 1) &&
+          (p < 2 || pwait(&sh.bar_o[e], ((p - 2) >> 1) & 1)) &&
+          (pw == 0 || pwait(&sh.gates_ready[e], (p >> 1) & 1))) {
         const int t = 32 * wq + lane;
         float x[32];
         tmem_ld32(lane_addr + COL_DP + 32 * ph, x);
@@ -521,9 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async();
         mbar_arrive(&sh.p_ready[e]);  // U^T P^T of chunk p may read it
       }
-      fence_proxy_async();
       tc_fence_before();
-      psync();
+      if (!pclose()) break;
     }
   } else {
     // ================================================================= chain
@@ -637,7 +653,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // U^T, row v: 32 fp32 values packed in place into 16 fp16 pairs (the A
       // operand of U^T K~ and U^T P^T)
       if (!cwait(&sh.bar_x[e], ph)) break;
-      if (tid == 0 && c + 2 < nch) tma_w(c + 2);  // X of chunk c has read its -W buffer
       {
         float u[32];
         tmem_ld32(uh + 32 * hc, u);
@@ -648,11 +663,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&sh.u_ready);
+      if (tid == 0 && c + 2 < nch) tma_w(c + 2);  // X of chunk c has read its -W buffer
       // Q~ of the next chunk while U^T K~ runs
       if (c + 1 < nch && !qt_part(c + 1)) break;
       // S1 = gamma_C S0 + U^T K~, and its fp16 copy for the next chunk
       if (!cwait(&sh.bar_su[e], ph)) break;
-      if (tid == 0 && c + 2 < nch) tma_k(c + 2);  // U^T K~ of chunk c has read its K slot
       const float gamC = sh.gamC[c % 3];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -663,6 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       stage_state();
       mbar_arrive(&sh.s16_ready);
+      if (tid == 0 && c + 2 < nch) tma_k(c + 2);  // U^T K~ of chunk c has read its K slot
       const int a_end = chunk_a0(c) + kChunk;
       if (ck_rows && ck_pool && a_end % N == 0 && a_end <= end_pos) {
         const int row = ck_rows[a_end / N - 1 - first_ck];
