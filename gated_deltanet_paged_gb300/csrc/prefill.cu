@@ -625,16 +625,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float* ksc = sh.gates.ksc[eq];
       uint8_t* kt = sm + kslot(q);
-      // Half of the chain threads (warps 0-3) convert K: at full width the pass
-      // takes more of the shared-memory bandwidth that the MMA running meanwhile
-      // (X of the next chunk) needs for its operands.
-      if (ci < 128) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int i = ci + 128 * k;
-          const int row = (i & 511) >> 3;
-          cvt8(kt + i * 16, kt + i * 16, ksc[row], row >= lo && row < hi);
-        }
+      for (int k = 0; k < 4; ++k) {
+        const int i = ci + 256 * k;
+        const int row = (i & 511) >> 3;
+        cvt8(kt + i * 16, kt + i * 16, ksc[row], row >= lo && row < hi);
       }
       fence_proxy_async();
       mbar_arrive(&sh.kt_ready[eq]);
