@@ -54,8 +54,8 @@ int encode_tokens_map(CUtensorMap* map, const void* base, int64_t T, int64_t H, 
   return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_CUDA;
 }
 
-// [T, H, D] bf16 tokens with 32 x 1 x 32 boxes and no swizzle: one warp's block
-// of outputs (32 tokens x 32 columns, 64-byte rows) per store.
+// [T, H, D] bf16 tokens with 32 x 1 x 32 boxes and the 64-byte swizzle: one
+// warp's block of outputs (32 tokens x 32 columns, 64-byte rows) per store.
 int encode_tokens_map_32(CUtensorMap* map, const void* base, int64_t T, int64_t H, int64_t D) {
   auto fn = encode_fn();
   if (!fn) return GDN_ERR_CUDA;
@@ -64,7 +64,7 @@ int encode_tokens_map_32(CUtensorMap* map, const void* base, int64_t T, int64_t 
   cuuint32_t box[3] = {32, 1, 32};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -308,6 +308,32 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
       : "memory");
 }
 
+// Load a 16-lane x 32-column fp32 block (four 16 x 8 repeats) in the fragment
+// layout of the 16x256b shape, and wait for it: in repeat j, thread i holds
+// columns 8 j + 2 (i % 4) and + 1 of lane i / 4 (r[4 j], r[4 j + 1]) and of lane
+// i / 4 + 8 (r[4 j + 2], r[4 j + 3]).  taddr's lane is the first of the 16.
+__device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Four 8 x 8 b16 matrices in the fragment layout above (thread i: row i / 4,
+// elements 2 (i % 4) and + 1 of each) stored transposed: row k of matrix m
+// (column k of the fragment) goes to the 16 bytes at thread 8 m + k's address.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t m0, uint32_t m1, uint32_t m2,
+                                                  uint32_t m3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(m0),
+               "r"(m1), "r"(m2), "r"(m3)
+               : "memory");
+}
+
 // Load 64 consecutive fp32 columns of this thread's TMEM lane and wait for them.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&r)[64]) {
   uint32_t* u = reinterpret_cast<uint32_t*>(r);
@@ -390,7 +416,7 @@ int encode_tokens_map(CUtensorMap* map, const void* base, int64_t T, int64_t H, 
 // Encode a 2-D fp16 tensor map over [rows, cols] (cols a multiple of 64) with
 // a box of 64 x 64 and 128-byte swizzle.
 int encode_tiles_map_f16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols);
-int encode_tokens_map_32(CUtensorMap* map, const void* base, int64_t T, int64_t H, int64_t D);
+int encode_tokens_map_32(CUtensorMap* map, const void* base, int64_t T, int64_t H, int64_t D);  // 64B swizzle
 
 inline int launch_status() { return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
 

@@ -679,25 +679,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = ck_rows[a_end / N - 1 - first_ck];
         if (row >= 0) store_state(ck_pool, row);
       }
-      // Outputs of chunk c: column v of O^T for this thread's 32 tokens.  In a
-      // full chunk each warp stages its 32 x 32 block (64-byte rows, a warp's
-      // stores fill a row) and stores it with one TMA store of its own, so no
-      // warp waits for another; a partial chunk (first / last of a sequence) is
+      // Outputs of chunk c (columns of O^T).  In a full chunk each warp reads its
+      // 32 x 32 block (rows v of its lane quarter x 32 tokens) as 16-lane
+      // fragments, which stmatrix stores transposed into a 64B-swizzled staging
+      // block (row t: the warp's 32 values v of token t, 16 bytes per store row
+      // and no bank conflicts), sent with one TMA store of its own, so no warp
+      // waits for another.  A partial chunk (first / last of a sequence) is
       // stored element by element, so that no row of another sequence is touched.
       if (!cwait(&sh.bar_o[e], ph)) break;
       {
-        float o[32];
-        tmem_ld32(oh + 32 * hc, o);
-        tc_fence_before();
-        mbar_arrive(&sh.o_read[e]);
         const int lo = chunk_lo(c), hi = chunk_hi(c), tf = chunk_tf(c);
         if (lo == 0 && hi == kChunk) {
+          uint32_t f[2][16];
+          tmem_ld16x256_x4(oh + 32 * hc, f[0]);               // lanes 32 wq + 0..15
+          tmem_ld16x256_x4(oh + 32 * hc + (16u << 16), f[1]);  // lanes 32 wq + 16..31
+          tc_fence_before();
+          mbar_arrive(&sh.o_read[e]);
           uint8_t* stg = sm + OFF_OST + warp * 2048;
           if (lane == 0) bulk_wait_read();  // this warp's previous store has read the block
           __syncwarp();
+          const float sc = a.scale;
+          const int mi = lane >> 3, k = lane & 7;  // this thread's row address: matrix mi, row k
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            *reinterpret_cast<__nv_bfloat16*>(stg + i * 64 + lane * 2) = __float2bfloat16_rn(a.scale * o[i]);
+          for (int g = 0; g < 2; ++g) {
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              uint32_t m[4];
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                const int j = 2 * jj + q;  // tokens 8 j .. 8 j + 7
+                m[2 * q] = pack_bf162(sc * __uint_as_float(f[g][4 * j]), sc * __uint_as_float(f[g][4 * j + 1]));
+                m[2 * q + 1] =
+                    pack_bf162(sc * __uint_as_float(f[g][4 * j + 2]), sc * __uint_as_float(f[g][4 * j + 3]));
+              }
+              // matrix mi: tokens 8 (2 jj + mi / 2) .., rows v 16 g + 8 (mi % 2) ..
+              const int t = 8 * (2 * jj + (mi >> 1)) + k;
+              const int piece = 2 * g + (mi & 1);
+              stmatrix_x4_trans(smem_u32(stg + t * 64 + ((piece ^ ((t >> 1) & 3)) << 4)), m[0], m[1], m[2], m[3]);
+            }
+          }
           fence_proxy_async();
           __syncwarp();
           if (lane == 0) {
@@ -705,6 +725,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_commit();
           }
         } else {
+          float o[32];
+          tmem_ld32(oh + 32 * hc, o);
+          tc_fence_before();
+          mbar_arrive(&sh.o_read[e]);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int t = 32 * hc + i;
