@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(kUtThreads, 3)
       uint8_t* arow = sm + XB + half * 8192;
       uint8_t* a21 = sm + XB + 16384 + half * 4096;
       const bool lower = t >= 32;  // warp-uniform
-  #pragma unroll
+#pragma unroll
       for (int q = 0; q < 4; ++q) {
         if (q >= 2 && !lower) break;
         float out[16];
@@ -339,10 +339,10 @@ __global__ void __launch_bounds__(kUtThreads, 3)
           // The block's gate values come into registers together (shared-memory
           // loads would otherwise wait behind the previous block's stores).
           float eb[16];
-  #pragma unroll
+#pragma unroll
           for (int jj = 0; jj < 16; ++jj) eb[jj] = sh.e[r0 + 16 * q + jj];
           float cur = bv * __expf(Gt - sh.G[r0 + jstart]);
-  #pragma unroll
+#pragma unroll
           for (int jj = 15; jj >= 0; --jj) {
             const int j = 16 * q + jj;
             const bool in = (j <= jstart) && (j >= lo);
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kUtThreads, 3)
             if (j <= jstart) cur *= eb[jj];
           }
         } else {
-  #pragma unroll
+#pragma unroll
           for (int jj = 0; jj < 16; ++jj) out[jj] = 0.f;
         }
         if (lower && q < 2) {
@@ -358,16 +358,13 @@ __global__ void __launch_bounds__(kUtThreads, 3)
           *reinterpret_cast<uint4*>(a21 + swz(t - 32, 2 * q + 1)) = pack8h(&out[8]);
         } else {
           const int qb = 4 * (q & 1);
-  #pragma unroll
+#pragma unroll
           for (int k = 0; k < 4; ++k)
             *reinterpret_cast<float4*>(arow + af(t, qb + k)) =
                 make_float4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
         }
       }
-      if (lower) {
-  #pragma unroll
-        for (int cc = 4; cc < 8; ++cc) *reinterpret_cast<uint4*>(a21 + swz(t - 32, cc)) = make_uint4(0u, 0u, 0u, 0u);
-      }
+      // (columns 32-63 of the A21 tile only feed products that are discarded)
     }
     fence_proxy_async();
     tc_fence_before();
@@ -378,14 +375,13 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     float x[32];
     if (ok) solve32(sm + XB + half * 8192 + bk * 32 * 128, lane, x);
     __syncthreads();  // every read of the fp32 blocks is done: the space becomes T_d
+    // Only the diagonal blocks are written: the rounds below read the blocks
+    // off the diagonal only into products that are discarded.
     if (ok) {
       uint8_t* td = sm + XB + half * 8192;
       const int col = 32 * bk + lane;
-  #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        st_h(td, 32 * bk + i, col, x[i]);
-        st_h(td, 32 * (1 - bk) + i, col, 0.f);
-      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) st_h(td, 32 * bk + i, col, x[i]);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -405,10 +401,10 @@ __global__ void __launch_bounds__(kUtThreads, 3)
       tmem_ld32(lane_addr + r0, d);
       uint8_t* nt = sm + XB + 16384;  // over A21, which round 1 has read
       const int nr = 32 * half + lane;
-  #pragma unroll
+#pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         float nv[8];
-  #pragma unroll
+#pragma unroll
         for (int i = 0; i < 8; ++i) nv[i] = -d[8 * cc + i];
         *reinterpret_cast<uint4*>(nt + swz(nr, cc)) = pack8h(nv);
       }
@@ -432,25 +428,28 @@ __global__ void __launch_bounds__(kUtThreads, 3)
       uint8_t* tile = sm + XB + half * 16384;
       const float bc = sh.bet[tid];
       const int col = 32 * bk + lane;
-  #pragma unroll
+#pragma unroll
       for (int i = 0; i < 32; ++i) st_h(tile, 32 * bk + i, col, x[i] * bc);
-      if (bk == 1) {
-  #pragma unroll
-        for (int i = 0; i < 32; ++i) st_h(tile, i, col, 0.f);
+      // the zero upper-right blocks (rows 0-31, columns 32-63) of both chunks
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int idx = tid + 128 * k;
+        *reinterpret_cast<uint4*>(sm + XB + (idx >> 7) * 16384 + swz((idx >> 2) & 31, 4 + (idx & 3))) =
+            make_uint4(0u, 0u, 0u, 0u);
       }
       if (warp < 2) {  // warp w: T21 of chunk w (TMEM lanes 32 w + i, columns 64 w + j)
         float d[32];
         tmem_ld32(lane_addr + 64 * warp, d);
         uint8_t* tw = sm + XB + warp * 16384;
-  #pragma unroll
+#pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           float v[8];
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < 8; ++i) v[i] = d[8 * cc + i] * sh.bet[64 * warp + 8 * cc + i];
           *reinterpret_cast<uint4*>(tw + swz(32 + lane, cc)) = pack8h(v);
         }
       }
-  #pragma unroll
+#pragma unroll
       for (int k = 0; k < 4; ++k)
         reinterpret_cast<uint4*>(sm + XB + kTile)[tid + 128 * k] = make_uint4(0u, 0u, 0u, 0u);
     }
@@ -476,15 +475,15 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     }
     // -W rows into staging boxes over K^ (the MMA has read it), then TMA stores.
     if (ok) {
-  #pragma unroll
+#pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         float w[64];
         tmem_ld64(lane_addr + 64 * hh, w);
         uint8_t* box = sm + KB + half * 16384 + hh * kTile;
-  #pragma unroll
+#pragma unroll
         for (int c = 0; c < 8; ++c) {
           float nw[8];
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < 8; ++i) nw[i] = -w[8 * c + i];
           *reinterpret_cast<uint4*>(box + swz(t, c)) = pack8h(nw);
         }
