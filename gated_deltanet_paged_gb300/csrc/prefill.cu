@@ -38,7 +38,8 @@
 //   chain: D_X += S0 [-W; Q~]^T or S0 [Q~; -W]^T      (U half: U^T; O half:
 //                                                      (Q~ S0^T)^T)
 //          D_SU = U^T K~;  D_X(O half) += U^T P^T
-// One zero tile serves both [T''; 0] and [0; T''].  Operands are fp16 (an
+// T'' arrives by columns (tile row j = column j), i.e. as an N-major B operand;
+// one zero tile serves both [T''; 0] and [0; T''].  Operands are fp16 (an
 // 11-bit significand keeps written states within 1e-3 relative error; bf16
 // would not) except Q K^T, which uses the bf16 tiles as loaded.
 #include <math.h>
@@ -61,7 +62,7 @@ constexpr uint32_t kTile = 8192;  // 64 rows x 128 B
 constexpr uint32_t OFF_Q = 0;         // 2 x Q bf16 [kb0 | kb1], by chunk parity
 constexpr uint32_t OFF_K = 32768;     // 2 x K [kb0 | kb1]: bf16 -> K~ (fp16), in place; by chunk parity
 constexpr uint32_t OFF_V = 65536;     // 2 x V [kb0 | kb1]: bf16 -> fp16, in place
-constexpr uint32_t OFF_TZT = 98304;   // T''(even chunk) | zero tile | T''(odd chunk)
+constexpr uint32_t OFF_TZT = 98304;   // T''(even chunk) | zero tile | T''(odd chunk), by columns
 constexpr uint32_t OFF_P = 122880;    // 2 x P (rows t, K-major), by chunk parity
 constexpr uint32_t OFF_XA = 139264;   // per K block (32 KB apart): -W (even) | Q~ (even) | Q~ (odd) | -W (odd)
 constexpr uint32_t OFF_OST = 204800;  // outputs of a full chunk: 2 KB per chain warp (32 tokens x 32 columns, bf16)
@@ -368,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     //   D_P  = [Q; .] K^T                      (bf16 from TMA; rows 0-63)
     //   D_X  = V^T [T''; 0]^T or V^T [0; T'']^T  (U~^T into the U half, zeros
     //                                            into the O half)
-    const uint32_t id_m2 = idesc_f16(128, 128, false, false, true, false);
+    const uint32_t id_m2 = idesc_f16(128, 128, false, false, true, true);
     const uint32_t id_qk = idesc_f16(128, 64, true, true, false, false);
     // Q K^T is committed only once the chunk's V conversion is in (m2_ready):
     // the preparation threads learn of it (bar_p) before they can arrive on
@@ -397,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        tc_mma4(tmem + COL_DX + 128 * e, dMN(vslot(p), kTile), 128, dK(OFF_TZT + kTile * e), 2, id_m2, 0);
+        tc_mma4(tmem + COL_DX + 128 * e, dMN(vslot(p), kTile), 128, dMN(OFF_TZT + kTile * e, kTile), 128, id_m2, 0);
         tc_commit(&sh.bar_m2[e]);
       }
     }

@@ -1,6 +1,6 @@
 // ut.cu -- the chunk-local part of chunked GDN prefill: for every 64-token chunk
-// and head, T'' = (I + A)^-1 diag(beta) and -W = -T'' diag(gamma) K, written to
-// the workspace.
+// and head, T'' = (I + A)^-1 diag(beta) (stored by columns: tile row j holds
+// column j) and -W = -T'' diag(gamma) K, written to the workspace.
 //
 // "flashinfer.gdn_paged", chunk_gated_delta_rule: the gated delta rule in
 // chunked (WY / UT) form.  With rows t = 0..63 of a chunk (rows outside the
@@ -22,9 +22,12 @@
 //                             columns = 128 threads, all with equal work):
 //                             x_t = [t = c] - sum_{j<t} A[t][j] x_j
 //   T21 = -T22 A21 T11        the remaining block of T = (I + A)^-1, by two MMAs:
-//                             N21 = -T22 A21, then T21 = N21 T11
-//   T'' = T diag(beta)        written (fp16) into SW128 tiles that are both the
-//                             staging of the T'' stores and the A operand of W
+//                             N21 = -T22 A21, then T21^T = T11^T N21^T (so that
+//                             thread j reads column j of T21 from TMEM)
+//   T'' = T diag(beta)        written (fp16) by columns into SW128 tiles that are
+//                             both the staging of the T'' stores and the
+//                             (M-major) A operand of W: a thread writes its column
+//                             with 16-byte stores
 //   W = [T''_a; 0] K^_a + [0; T''_b] K^_b,  K^ = diag(gamma) K converted to fp16
 //                             in place once the first MMA has read K
 // The per-chunk B operands sit side by side ([X_a | X_b], N = 128) so one MMA
@@ -45,15 +48,13 @@ constexpr uint32_t kTile = 8192;  // 64 rows x 128 B
 //   K region:      K stack (bf16 boxes K_a kb0 | K_b kb0 | K_a kb1 | K_b kb1)
 //                  -> K^ = diag(gamma) K (fp16, in place) -> -W staging
 //   A-tile region: fp32 diagonal blocks of A (8 KB per chunk: rows 0-31 hold A11,
-//                  rows 32-63 hold A22, 128 B per row) -> T_d stack (fp16,
-//                  T_d,a | T_d,b, 64 x 64 SW128 each) in the first 16 KB;
-//                  A21 of both chunks (fp16, MN-major B: 32 rows x 64 columns,
-//                  4 KB each, columns 32-63 zero) -> N21 of both chunks (fp16,
-//                  K-major A rows 0-63, only K 0-31 used) in the second 16 KB;
-//                  as a 128-row A operand N21 reads rows 64-127 from the rest
-//                  of that 16 KB, which stays inside the region whichever
-//                  half of shared memory the region is;
-//                  after the second product T''_a | zero tile | T''_b (24 KB)
+//                  rows 32-63 hold A22, 128 B per row) -> T_d stack (fp16 by
+//                  columns, T_d,a | T_d,b, 64 x 64 SW128 each: tile row j =
+//                  column j) in the first 16 KB; A21 of both chunks (fp16,
+//                  MN-major B: 32 rows x 64 columns, 4 KB each, columns 32-63
+//                  unused) -> N21 of both chunks (fp16, 64 rows: N21_a | N21_b,
+//                  only columns 0-31 used) in the second 16 KB; after the second
+//                  product T''_a | zero tile | T''_b by columns (24 KB)
 // The next item's K lands in this item's A-tile region once its T'' stores
 // have read it; this item's -W staging becomes the next item's A-tile region
 // once the -W stores have read it.
@@ -109,11 +110,6 @@ __device__ __forceinline__ void solve32(const uint8_t* blk, int c, float (&x)[32
     const float s = (s0 + s1) + (s2 + s3);
     x[t] = t > c ? -s : (t == c ? 1.f : 0.f);
   }
-}
-
-// One fp16 element at (row, col) of a 64 x 64 SW128 tile.
-__device__ __forceinline__ void st_h(uint8_t* tile, int row, int col, float v) {
-  *reinterpret_cast<__half*>(tile + row * 128 + (((col >> 3) ^ (row & 7)) << 4) + (col & 7) * 2) = __float2half_rn(v);
 }
 
 // Chunk slot -> {first token of its 64 rows, lo, hi, sequence}; hi <= lo (and
@@ -216,7 +212,8 @@ __global__ void __launch_bounds__(kUtThreads, 3)
   auto dK = [&](uint32_t off) { return sdesc(sbase + off, 16, 1024); };
   auto dMN = [&](uint32_t off, uint32_t lbo) { return sdesc(sbase + off, lbo, 1024); };
   const uint32_t id_bf16 = idesc_f16(128, 128, true, true, false, false);
-  const uint32_t id_mnB = idesc_f16(128, 128, false, false, false, true);
+  const uint32_t id_mnAB = idesc_f16(128, 128, false, false, true, true);
+  const uint32_t id_t21 = idesc_f16(128, 64, false, false, false, false);
 
   // Every thread waits for the MMA; a time-out anywhere aborts the CTA.
   auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -375,23 +372,25 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     float x[32];
     if (ok) solve32(sm + XB + half * 8192 + bk * 32 * 128, lane, x);
     __syncthreads();  // every read of the fp32 blocks is done: the space becomes T_d
+    // T_d is kept by columns (tile row j = column j of T_d, 64 rows t in 128
+    // bytes), so each thread writes its solved column with four 16-byte stores.
     // Only the diagonal blocks are written: the rounds below read the blocks
     // off the diagonal only into products that are discarded.
+    const int jcol = 32 * bk + lane;
     if (ok) {
       uint8_t* td = sm + XB + half * 8192;
-      const int col = 32 * bk + lane;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) st_h(td, 32 * bk + i, col, x[i]);
+      for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(td + swz(jcol, 4 * bk + q)) = pack8h(&x[8 * q]);
     }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
 
-    // ---- N21 = -T22 A21: [T_d,a; T_d,b] (K = 32..63) x [A21_a | A21_b];
-    //      the first half of K^ while it runs ----
+    // ---- N21 = -T22 A21: [T_d,a; T_d,b] (K = 32..63; by columns, so M-major) x
+    //      [A21_a | A21_b]; the first half of K^ while it runs ----
     if (ok && tid == 0) {
       tc_fence_after();
-      tc_mma2(tmem, dK(XB + 64), 2, dMN(XB + 16384, 4096), 128, id_mnB, 0);
+      tc_mma2(tmem, dMN(XB + 32 * 128, 8192), 128, dMN(XB + 16384, 4096), 128, id_mnAB, 0);
       tc_commit(&sh.bar_mma);
     }
     if (ok) khat_half(0);
@@ -413,40 +412,43 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     tc_fence_before();
     __syncthreads();
 
-    // ---- T21 = N21 T11: [N21_a; N21_b] (K = 0..31) x [T_d,a | T_d,b]; the second
-    //      half of K^ while it runs ----
+    // ---- T21^T = T11^T N21^T: [T_d,a by columns; T_d,b by columns] (K = rows
+    //      0..31) x [N21_a; N21_b]^T (N = 64): lane 64 h + j, column 32 h + i holds
+    //      T21[i][j] of chunk h; the second half of K^ while it runs ----
     if (ok && tid == 0) {
       tc_fence_after();
-      tc_mma2(tmem, dK(XB + 16384), 2, dMN(XB, 8192), 128, id_mnB, 0);
+      tc_mma2(tmem, dK(XB), 2, dK(XB + 16384), 2, id_t21, 0);
       tc_commit(&sh.bar_mma);
     }
     if (ok) khat_half(1);
     ok = ok && wait_mma();
 
-    // ---- T'' = T diag(beta) into T''_a | 0 | T''_b (T_d, A21 and N21 are dead) ----
+    // ---- T'' = T diag(beta) by columns (tile row j = column j) into T''_a | 0 |
+    //      T''_b (T_d, A21 and N21 are dead): thread (chunk, bk, lane) writes
+    //      column j = 32 bk + lane, beta_j times its solved block and, for bk = 0,
+    //      T21's column from TMEM; zeros above the diagonal block for bk = 1 ----
     if (ok) {
       uint8_t* tile = sm + XB + half * 16384;
       const float bc = sh.bet[tid];
-      const int col = 32 * bk + lane;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) st_h(tile, 32 * bk + i, col, x[i] * bc);
-      // the zero upper-right blocks (rows 0-31, columns 32-63) of both chunks
+      for (int q = 0; q < 4; ++q) {
+        float v[8];
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int idx = tid + 128 * k;
-        *reinterpret_cast<uint4*>(sm + XB + (idx >> 7) * 16384 + swz((idx >> 2) & 31, 4 + (idx & 3))) =
-            make_uint4(0u, 0u, 0u, 0u);
+        for (int i = 0; i < 8; ++i) v[i] = x[8 * q + i] * bc;
+        *reinterpret_cast<uint4*>(tile + swz(jcol, 4 * bk + q)) = pack8h(v);
       }
-      if (warp < 2) {  // warp w: T21 of chunk w (TMEM lanes 32 w + i, columns 64 w + j)
-        float d[32];
-        tmem_ld32(lane_addr + 64 * warp, d);
-        uint8_t* tw = sm + XB + warp * 16384;
+      if (bk == 1) {
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(tile + swz(jcol, q)) = make_uint4(0u, 0u, 0u, 0u);
+      } else {  // warps 0 and 2: TMEM lanes 64 h + j
+        float d[32];
+        tmem_ld32(lane_addr + 32 * half, d);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
           float v[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = d[8 * cc + i] * sh.bet[64 * warp + 8 * cc + i];
-          *reinterpret_cast<uint4*>(tw + swz(32 + lane, cc)) = pack8h(v);
+          for (int i = 0; i < 8; ++i) v[i] = d[8 * q + i] * bc;
+          *reinterpret_cast<uint4*>(tile + swz(jcol, 4 + q)) = pack8h(v);
         }
       }
 #pragma unroll
@@ -460,8 +462,8 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     // ---- W = [T''_a; 0] K^_a + [0; T''_b] K^_b;  T'' tiles -> workspace ----
     if (ok && tid == 0) {
       tc_fence_after();
-      tc_mma4(tmem, dK(XB), 2, dMN(KB, 16384), 128, id_mnB, 0);
-      tc_mma4(tmem, dK(XB + kTile), 2, dMN(KB + kTile, 16384), 128, id_mnB, 1);
+      tc_mma4(tmem, dMN(XB, kTile), 128, dMN(KB, 16384), 128, id_mnAB, 0);
+      tc_mma4(tmem, dMN(XB + kTile, kTile), 128, dMN(KB + kTile, 16384), 128, id_mnAB, 1);
       tc_commit(&sh.bar_mma);
       for (int hh = 0; hh < 2; ++hh)
         if (hh ? vb : va) tma_store_2d(&tm_t, sm + XB + hh * 16384, 0, ((2 * pair + hh) * H + h) * 64);
