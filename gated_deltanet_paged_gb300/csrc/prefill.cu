@@ -551,6 +551,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int v = 32 * wq + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * wq) << 16);
     bool ok = true;
+    // The lanes of a warp wait on the same barrier phase in step, so a wait
+    // fails for the whole warp at once and the warp-wide TMEM and stmatrix
+    // instructions after it never run with part of the warp.  (Thread 0's
+    // extra wait in kt_part can fail alone; the other lanes then meet the abort
+    // flag in their next wait, before any warp-wide instruction.)
     auto cwait = [&](uint64_t* bar, uint32_t parity) {
       if (ok && !mbar_wait_or_abort(bar, parity, abort_flag)) {
         ok = false;

@@ -76,6 +76,16 @@ def test_ragged_prefixes_and_tails(case, decay):
     print("ragged case %d decay=%g: %r" % (case, decay, errs))
 
 
+def test_long_ragged_sequences():
+    """Long chains next to short ones: 188 and 313 chunks (prefixes 0 and 129,
+    so the second starts with a partial chunk), 47 chunks and 2 chunks, with a
+    page store every 10 chunks."""
+    call, pool = _ragged_case(7, 640, [12000, 3000, 20000, 100], [0, 70, 129, 5])
+    errs = Errors()
+    prefill_paged_both(call, pool.cuda(), pool.numpy().copy(), errs)
+    print("long ragged sequences: %r" % errs)
+
+
 @pytest.mark.parametrize("H", [1, 3, 5])
 def test_head_counts_that_are_not_powers_of_two(H):
     """The chunk-local kernel's work items (chunk pair x head) and the chain's
