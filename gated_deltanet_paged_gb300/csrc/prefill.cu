@@ -33,13 +33,13 @@
 // Per chunk (M = 128 = state rows v, fp32 accumulators in TMEM; the U half of
 // D_X is its columns 0-63 for even chunks, 64-127 for odd ones):
 //   prep : D_P  = [Q; .] K^T                  (bf16 from TMA; P from rows 0-63)
-//          D_X  = V^T [T''; 0]^T or V^T [0; T'']^T   (U~^T into the U half,
-//                                                      zeros into the O half)
+//          D_X(U half) = V^T T''^T                   (U~^T; the chain threads zero
+//                                                      the O half after reading it)
 //   chain: D_X += S0 [-W; Q~]^T or S0 [Q~; -W]^T      (U half: U^T; O half:
 //                                                      (Q~ S0^T)^T)
 //          D_SU = U^T K~;  D_X(O half) += U^T P^T
-// T'' arrives by columns (tile row j = column j), i.e. as an N-major B operand;
-// one zero tile serves both [T''; 0] and [0; T''].  Operands are fp16 (an
+// T'' arrives by columns (tile row j = column j), i.e. as an N-major B operand.
+// Operands are fp16 (an
 // 11-bit significand keeps written states within 1e-3 relative error; bf16
 // would not) except Q K^T, which uses the bf16 tiles as loaded.
 #include <math.h>
@@ -62,7 +62,7 @@ constexpr uint32_t kTile = 8192;  // 64 rows x 128 B
 constexpr uint32_t OFF_Q = 0;         // 2 x Q bf16 [kb0 | kb1], by chunk parity
 constexpr uint32_t OFF_K = 32768;     // 2 x K [kb0 | kb1]: bf16 -> K~ (fp16), in place; by chunk parity
 constexpr uint32_t OFF_V = 65536;     // 2 x V [kb0 | kb1]: bf16 -> fp16, in place
-constexpr uint32_t OFF_TZT = 98304;   // T''(even chunk) | zero tile | T''(odd chunk), by columns
+constexpr uint32_t OFF_TZT = 98304;   // T''(even chunk) | unused 8 KB | T''(odd chunk), by columns
 constexpr uint32_t OFF_P = 122880;    // 2 x P (rows t, K-major), by chunk parity
 constexpr uint32_t OFF_XA = 139264;   // per K block (32 KB apart): -W (even) | Q~ (even) | Q~ (odd) | -W (odd)
 constexpr uint32_t OFF_OST = 204800;  // outputs of a full chunk: 2 KB per chain warp (32 tokens x 32 columns, bf16)
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int first_ck = (ck_rows && N > 0) ? P / N : 0;
   const int slot0 = slot_base(cu_b, b);
 
-  // ---- set-up: barriers, TMEM, the zero tile ----
+  // ---- set-up: barriers, TMEM ----
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.bar_q[i], 1);
@@ -256,7 +256,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&sh.tmem_base, TMEM_COLS);
     tmem_relinquish();
   }
-  reinterpret_cast<uint4*>(sm + OFF_TZT + kTile)[tid] = make_uint4(0u, 0u, 0u, 0u);  // 512 x 16 B
   fence_proxy_async();
   tc_fence_before();
   __syncthreads();
@@ -367,9 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kPrepIssuerWarp) {
     // =========================================================== prep issuer
     //   D_P  = [Q; .] K^T                      (bf16 from TMA; rows 0-63)
-    //   D_X  = V^T [T''; 0]^T or V^T [0; T'']^T  (U~^T into the U half, zeros
-    //                                            into the O half)
-    const uint32_t id_m2 = idesc_f16(128, 128, false, false, true, true);
+    //   D_X(U half) = V^T T''^T                (U~^T)
+    const uint32_t id_m2 = idesc_f16(128, 64, false, false, true, true);
     const uint32_t id_qk = idesc_f16(128, 64, true, true, false, false);
     // Q K^T is committed only once the chunk's V conversion is in (m2_ready):
     // the preparation threads learn of it (bar_p) before they can arrive on
@@ -398,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        tc_mma4(tmem + COL_DX + 128 * e, dMN(vslot(p), kTile), 128, dMN(OFF_TZT + kTile * e, kTile), 128, id_m2, 0);
+        tc_mma4(tmem + COL_DX + 192 * e, dMN(vslot(p), kTile), 128, dMN(tslot(p), kTile), 128, id_m2, 0);
         tc_commit(&sh.bar_m2[e]);
       }
     }
@@ -591,6 +589,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
     };
+    // 32 zero columns of this thread's TMEM lane: the O half of D_X, into which X
+    // accumulates, is zeroed after each read (and before the first chunks).
+    auto zero32 = [&](uint32_t taddr) {
+      uint32_t z[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) z[i] = 0u;
+      tmem_st16(taddr, z);
+      tmem_st16(taddr + 16, z);
+    };
+    zero32(lane_addr + COL_DX + 64 + 32 * hc);   // O half of even chunks
+    zero32(lane_addr + COL_DX + 128 + 32 * hc);  // O half of odd chunks
     stage_state();
     mbar_arrive(&sh.s16_ready);
     // The chain warps' share of the preparation, done while they would otherwise
@@ -699,6 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t f[2][16];
           tmem_ld16x256_x4(oh + 32 * hc, f[0]);               // lanes 32 wq + 0..15
           tmem_ld16x256_x4(oh + 32 * hc + (16u << 16), f[1]);  // lanes 32 wq + 16..31
+          zero32(oh + 32 * hc);
           tc_fence_before();
           mbar_arrive(&sh.o_read[e]);
           uint8_t* stg = sm + OFF_OST + warp * 2048;
@@ -733,6 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           float o[32];
           tmem_ld32(oh + 32 * hc, o);
+          zero32(oh + 32 * hc);
           tc_fence_before();
           mbar_arrive(&sh.o_read[e]);
 #pragma unroll
