@@ -52,12 +52,14 @@ def _load():
             i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
             lib.oracle_prefill_slots.argtypes = [i32, P, P, P, P, i32, P, P, P, P]
             lib.oracle_decode_slots.argtypes = [i32, P, P, P, i32, P, P]
-            lib.oracle_chunk_gdn.argtypes = [i32, P, i32, i32, i32, f64, P, P, P, P, P, P,
-                                             P, P, P, P, P, P, P, P, i32, i64, P, P, P]
-            lib.oracle_decode.argtypes = [i32, i32, i32, i32, f64, P, P, P, P, P, P, P, i64,
-                                          P, P, P, P]
-            for fn in (lib.oracle_prefill_slots, lib.oracle_decode_slots, lib.oracle_chunk_gdn,
-                       lib.oracle_decode):
+            lib.oracle_chunk_gdn_st.argtypes = [i32, P, i32, i32, i32, f64, P, P, P, P, P, P,
+                                                P, P, P, P, P, P, P, P, i32, i64, P, P, P, i32]
+            lib.oracle_decode_st.argtypes = [i32, i32, i32, i32, f64, P, P, P, P, P, P, P, i64,
+                                             P, P, P, P, i32]
+            lib.oracle_double_to_bf16.argtypes = [f64]
+            lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+            for fn in (lib.oracle_prefill_slots, lib.oracle_decode_slots, lib.oracle_chunk_gdn_st,
+                       lib.oracle_decode_st):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -116,9 +118,23 @@ def decode_slots(page_indptr, page_indices, last_page_len, page_size):
 def _row_stride(pool, H, K, V):
     if pool is None:
         return H * V * K
-    if pool.dtype != np.float32 or not pool.flags.c_contiguous:
-        raise TypeError("pools must be C-contiguous float32")
+    if pool.dtype not in (np.float32, np.uint16) or not pool.flags.c_contiguous:
+        raise TypeError("pools must be C-contiguous float32, or uint16 holding bf16 bits")
     return int(np.prod(pool.shape[1:]))
+
+
+def _state_bf16(pools):
+    """1 when the pools hold bf16 bits (uint16), 0 for float32; all alike."""
+    kinds = {p.dtype for p in pools if p is not None}
+    if len(kinds) > 1:
+        raise TypeError("pools must share one element type")
+    return int(kinds == {np.dtype(np.uint16)})
+
+
+def double_to_bf16_bits(x: float) -> int:
+    """The bf16 value nearest to x (ties to even) as bits, as the oracle stores
+    states in a bf16 pool."""
+    return int(_load().oracle_double_to_bf16(float(x)))
 
 
 def chunk_gated_delta_rule(q, k, v, g, beta, cu_seqlens, scale, *, initial_state=None,
@@ -129,8 +145,9 @@ def chunk_gated_delta_rule(q, k, v, g, beta, cu_seqlens, scale, *, initial_state
     """Prefill with slot arguments, token by token in fp64.
 
     q, k: uint16 [T, H, K] (bf16 bits); v: uint16 [T, H, V]; g, beta: float32
-    [T, H]; pools: float32 [rows, H, V, K] arrays updated in place (they may be
-    the same array).  ``chains`` (bool [num_seqs, H]) restricts the work to some
+    [T, H]; pools: float32 [rows, H, V, K] arrays, or uint16 ones holding bf16
+    bits (states then rounded to bf16, ties to even), updated in place (they may
+    be the same array).  ``chains`` (bool [num_seqs, H]) restricts the work to some
     (sequence, head) chains.  Returns (o float64 [T, H, V], out_written,
     ckpt_written) where the last two flag the rows stored (or None).
     """
@@ -151,11 +168,11 @@ def chunk_gated_delta_rule(q, k, v, g, beta, cu_seqlens, scale, *, initial_state
     mask = None if chains is None else np.ascontiguousarray(chains, dtype=np.uint8).reshape(-1)
     si, osi, csi, ccs, pl = map(_i32, (state_indices, output_state_indices, checkpoint_state_indices,
                                       checkpoint_cu_starts, prefix_lens))
-    rc = _load().oracle_chunk_gdn(
+    rc = _load().oracle_chunk_gdn_st(
         num_seqs, _ptr(cu), H, K, V, float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
         _ptr(o), _ptr(initial_state), _ptr(si), _ptr(output_state), _ptr(osi),
         _ptr(state_checkpoints), _ptr(csi), _ptr(ccs), _ptr(pl), int(checkpoint_every_n_tokens),
-        stride, _ptr(mask), _ptr(out_written), _ptr(ckpt_written))
+        stride, _ptr(mask), _ptr(out_written), _ptr(ckpt_written), _state_bf16(pools))
     if rc != 0:
         raise ValueError("oracle_chunk_gdn failed (%d)" % rc)
     return o, out_written, ckpt_written
@@ -181,8 +198,8 @@ def chunk_gated_delta_rule_paged(q, k, v, g, beta, cu_seqlens, state_pool, page_
 def gated_delta_rule_decode(q, k, v, g, beta, state_pool, initial_state_indices,
                             output_state_indices, scale, chains=None):
     """One token per sequence on explicit read / write rows.  q, k: uint16
-    [B, H, K]; v: uint16 [B, H, V]; g, beta: float32 [B, H].  Returns
-    (o float64 [B, H, V], written)."""
+    [B, H, K]; v: uint16 [B, H, V]; g, beta: float32 [B, H]; state_pool float32,
+    or uint16 holding bf16 bits.  Returns (o float64 [B, H, V], written)."""
     q, k, v = _bits(q), _bits(k), _bits(v)
     g, beta = _f32(g), _f32(beta)
     B, H, K = q.shape
@@ -192,9 +209,9 @@ def gated_delta_rule_decode(q, k, v, g, beta, state_pool, initial_state_indices,
     written = np.zeros(state_pool.shape[0], np.uint8)
     isi, osi = _i32(initial_state_indices), _i32(output_state_indices)
     mask = None if chains is None else np.ascontiguousarray(chains, dtype=np.uint8).reshape(-1)
-    rc = _load().oracle_decode(B, H, K, V, float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-                               _ptr(beta), _ptr(o), _ptr(state_pool), stride, _ptr(isi), _ptr(osi),
-                               _ptr(mask), _ptr(written))
+    rc = _load().oracle_decode_st(B, H, K, V, float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                  _ptr(beta), _ptr(o), _ptr(state_pool), stride, _ptr(isi), _ptr(osi),
+                                  _ptr(mask), _ptr(written), _state_bf16([state_pool]))
     if rc != 0:
         raise ValueError("oracle_decode failed (%d)" % rc)
     return o, written

@@ -34,9 +34,12 @@
  *
  * Conventions: q, k are [T, H, K] and v is [T, H, V], as raw bf16 bits
  * (uint16) converted exactly to fp64; g, beta are [T, H] fp32; the output o is
- * [T, H, V] fp64; every pool row is a dense [H, V, K] fp32 block at
- * row * row_stride elements.  Stores round fp64 -> fp32 to nearest even.
+ * [T, H, V] fp64; every pool row is a dense [H, V, K] block at row * row_stride
+ * elements, of fp32 or (the _st entry points with state_bf16 = 1) of bf16 bits.
+ * Stores round the fp64 state to the nearest fp32 or bf16 value, ties to even;
+ * loads convert exactly.
  */
+#include <fenv.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -48,6 +51,26 @@ static double bf16_bits_to_double(uint16_t h)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* The bf16 value nearest to x, ties to even, as bits: 8 significant bits, the
+ * exponent range of fp32 (quantum 2^-133 below 2^-126), +-inf past the largest
+ * finite value.  Rounds x itself, not an fp32 copy of it. */
+uint16_t oracle_double_to_bf16(double x)
+{
+    if (isnan(x)) return (uint16_t)0x7FC0;
+    double r = x;
+    if (x != 0.0 && !isinf(x)) {
+        int e;
+        frexp(fabs(x), &e); /* |x| = m 2^e, m in [0.5, 1) */
+        int qexp = e - 8;   /* the quantum of an 8-bit significand */
+        if (qexp < -133) qexp = -133;
+        r = ldexp(nearbyint(ldexp(x, -qexp)), qexp); /* default mode: nearest, ties to even */
+    }
+    float f = (float)r; /* exact: r has at most 8 significant bits (or overflows to inf) */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -167,18 +190,30 @@ static void gdn_token(double *S, int32_t K, int32_t V, const double *q, const do
     }
 }
 
-static void load_state(double *S, const float *pool, int64_t row, int64_t row_stride,
+static void load_state(double *S, const void *pool, int bf16, int64_t row, int64_t row_stride,
                        int32_t h, int32_t K, int32_t V)
 {
-    const float *src = pool + row * row_stride + (int64_t)h * V * K;
-    for (int64_t i = 0; i < (int64_t)V * K; ++i) S[i] = (double)src[i];
+    int64_t off = row * row_stride + (int64_t)h * V * K;
+    if (bf16) {
+        const uint16_t *src = (const uint16_t *)pool + off;
+        for (int64_t i = 0; i < (int64_t)V * K; ++i) S[i] = bf16_bits_to_double(src[i]);
+    } else {
+        const float *src = (const float *)pool + off;
+        for (int64_t i = 0; i < (int64_t)V * K; ++i) S[i] = (double)src[i];
+    }
 }
 
-static void store_state(const double *S, float *pool, int64_t row, int64_t row_stride,
+static void store_state(const double *S, void *pool, int bf16, int64_t row, int64_t row_stride,
                         int32_t h, int32_t K, int32_t V)
 {
-    float *dst = pool + row * row_stride + (int64_t)h * V * K;
-    for (int64_t i = 0; i < (int64_t)V * K; ++i) dst[i] = (float)S[i];
+    int64_t off = row * row_stride + (int64_t)h * V * K;
+    if (bf16) {
+        uint16_t *dst = (uint16_t *)pool + off;
+        for (int64_t i = 0; i < (int64_t)V * K; ++i) dst[i] = oracle_double_to_bf16(S[i]);
+    } else {
+        float *dst = (float *)pool + off;
+        for (int64_t i = 0; i < (int64_t)V * K; ++i) dst[i] = (float)S[i];
+    }
 }
 
 static void mark(uint8_t *flags, int64_t row)
@@ -203,17 +238,19 @@ static void mark(uint8_t *flags, int64_t row)
  * Checkpoint arguments may be NULL (no checkpoints); prefix_lens NULL means 0.
  * chain_mask (optional, [num_seqs * H]) selects the chains to compute; output
  * rows of skipped chains are left as they are.  out_written / ckpt_written
- * (optional) get a 1 for every row stored. */
-int oracle_chunk_gdn(int32_t num_seqs, const int32_t *cu_seqlens, int32_t H, int32_t K,
-                     int32_t V, double scale, const uint16_t *q, const uint16_t *k,
-                     const uint16_t *v, const float *g, const float *beta, double *o,
-                     const float *initial_state, const int32_t *state_indices,
-                     float *output_state, const int32_t *output_state_indices,
-                     float *state_checkpoints, const int32_t *checkpoint_state_indices,
-                     const int32_t *checkpoint_cu_starts, const int32_t *prefix_lens,
-                     int32_t N, int64_t row_stride, const uint8_t *chain_mask,
-                     uint8_t *out_written, uint8_t *ckpt_written)
+ * (optional) get a 1 for every row stored.  state_bf16 selects bf16 pools
+ * (row_stride then counts bf16 elements). */
+int oracle_chunk_gdn_st(int32_t num_seqs, const int32_t *cu_seqlens, int32_t H, int32_t K,
+                        int32_t V, double scale, const uint16_t *q, const uint16_t *k,
+                        const uint16_t *v, const float *g, const float *beta, double *o,
+                        const void *initial_state, const int32_t *state_indices,
+                        void *output_state, const int32_t *output_state_indices,
+                        void *state_checkpoints, const int32_t *checkpoint_state_indices,
+                        const int32_t *checkpoint_cu_starts, const int32_t *prefix_lens,
+                        int32_t N, int64_t row_stride, const uint8_t *chain_mask,
+                        uint8_t *out_written, uint8_t *ckpt_written, int32_t state_bf16)
 {
+    if (fegetround() != FE_TONEAREST) return -3;
     int use_ckpt = state_checkpoints && checkpoint_state_indices && checkpoint_cu_starts;
     if (use_ckpt && N <= 0) return -1;
     int64_t nchains = (int64_t)num_seqs * H;
@@ -241,7 +278,7 @@ int oracle_chunk_gdn(int32_t num_seqs, const int32_t *cu_seqlens, int32_t H, int
 
             memset(S, 0, sizeof(double) * (size_t)V * K);
             if (initial_state && state_indices && state_indices[b] >= 0)
-                load_state(S, initial_state, state_indices[b], row_stride, h, K, V);
+                load_state(S, initial_state, state_bf16, state_indices[b], row_stride, h, K, V);
 
             int64_t j = 0; /* checkpoints taken so far by this call */
             for (int64_t n = 1; n <= len; ++n) {
@@ -257,13 +294,13 @@ int oracle_chunk_gdn(int32_t num_seqs, const int32_t *cu_seqlens, int32_t H, int
                     int32_t row = checkpoint_state_indices[checkpoint_cu_starts[b] + j];
                     ++j;
                     if (row >= 0) {
-                        store_state(S, state_checkpoints, row, row_stride, h, K, V);
+                        store_state(S, state_checkpoints, state_bf16, row, row_stride, h, K, V);
                         mark(ckpt_written, row);
                     }
                 }
             }
             if (output_state && output_state_indices && output_state_indices[b] >= 0) {
-                store_state(S, output_state, output_state_indices[b], row_stride, h, K, V);
+                store_state(S, output_state, state_bf16, output_state_indices[b], row_stride, h, K, V);
                 mark(out_written, output_state_indices[b]);
             }
         }
@@ -276,16 +313,34 @@ int oracle_chunk_gdn(int32_t num_seqs, const int32_t *cu_seqlens, int32_t H, int
     return failed ? -2 : 0;
 }
 
+int oracle_chunk_gdn(int32_t num_seqs, const int32_t *cu_seqlens, int32_t H, int32_t K,
+                     int32_t V, double scale, const uint16_t *q, const uint16_t *k,
+                     const uint16_t *v, const float *g, const float *beta, double *o,
+                     const float *initial_state, const int32_t *state_indices,
+                     float *output_state, const int32_t *output_state_indices,
+                     float *state_checkpoints, const int32_t *checkpoint_state_indices,
+                     const int32_t *checkpoint_cu_starts, const int32_t *prefix_lens,
+                     int32_t N, int64_t row_stride, const uint8_t *chain_mask,
+                     uint8_t *out_written, uint8_t *ckpt_written)
+{
+    return oracle_chunk_gdn_st(num_seqs, cu_seqlens, H, K, V, scale, q, k, v, g, beta, o,
+                               initial_state, state_indices, output_state, output_state_indices,
+                               state_checkpoints, checkpoint_state_indices, checkpoint_cu_starts,
+                               prefix_lens, N, row_stride, chain_mask, out_written, ckpt_written, 0);
+}
+
 /* Single-token decode (decode paragraph): for every (b, h), read row
  * initial_state_indices[b] (-1 = zero state), apply one token and store the new
  * state to row output_state_indices[b] (in place when the two are equal).
- * q, k are [B, H, K], v [B, H, V], g and beta [B, H], o [B, H, V]. */
-int oracle_decode(int32_t batch, int32_t H, int32_t K, int32_t V, double scale,
-                  const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g,
-                  const float *beta, double *o, float *pool, int64_t row_stride,
-                  const int32_t *initial_state_indices, const int32_t *output_state_indices,
-                  const uint8_t *chain_mask, uint8_t *written)
+ * q, k are [B, H, K], v [B, H, V], g and beta [B, H], o [B, H, V].  state_bf16
+ * selects a bf16 pool. */
+int oracle_decode_st(int32_t batch, int32_t H, int32_t K, int32_t V, double scale,
+                     const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g,
+                     const float *beta, double *o, void *pool, int64_t row_stride,
+                     const int32_t *initial_state_indices, const int32_t *output_state_indices,
+                     const uint8_t *chain_mask, uint8_t *written, int32_t state_bf16)
 {
+    if (fegetround() != FE_TONEAREST) return -3;
     int64_t nchains = (int64_t)batch * H;
     int failed = 0;
 #pragma omp parallel
@@ -306,7 +361,7 @@ int oracle_decode(int32_t batch, int32_t H, int32_t K, int32_t V, double scale,
             if (chain_mask && !chain_mask[c]) continue;
             memset(S, 0, sizeof(double) * (size_t)V * K);
             if (initial_state_indices[b] >= 0)
-                load_state(S, pool, initial_state_indices[b], row_stride, h, K, V);
+                load_state(S, pool, state_bf16, initial_state_indices[b], row_stride, h, K, V);
             for (int32_t x = 0; x < K; ++x) {
                 qd[x] = bf16_bits_to_double(q[c * K + x]);
                 kd[x] = bf16_bits_to_double(k[c * K + x]);
@@ -314,7 +369,7 @@ int oracle_decode(int32_t batch, int32_t H, int32_t K, int32_t V, double scale,
             for (int32_t x = 0; x < V; ++x) vd[x] = bf16_bits_to_double(v[c * V + x]);
             gdn_token(S, K, V, qd, kd, vd, (double)g[c], (double)beta[c], scale, o + c * V, u);
             if (output_state_indices[b] >= 0) {
-                store_state(S, pool, output_state_indices[b], row_stride, h, K, V);
+                store_state(S, pool, state_bf16, output_state_indices[b], row_stride, h, K, V);
                 mark(written, output_state_indices[b]);
             }
         }
@@ -325,4 +380,14 @@ int oracle_decode(int32_t batch, int32_t H, int32_t K, int32_t V, double scale,
         free(u);
     }
     return failed ? -2 : 0;
+}
+
+int oracle_decode(int32_t batch, int32_t H, int32_t K, int32_t V, double scale,
+                  const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *g,
+                  const float *beta, double *o, float *pool, int64_t row_stride,
+                  const int32_t *initial_state_indices, const int32_t *output_state_indices,
+                  const uint8_t *chain_mask, uint8_t *written)
+{
+    return oracle_decode_st(batch, H, K, V, scale, q, k, v, g, beta, o, pool, row_stride,
+                            initial_state_indices, output_state_indices, chain_mask, written, 0);
 }

@@ -466,3 +466,97 @@ def test_rows_outside_write_set_keep_their_bits():
         for j in range(P // ps, (P + L + ps - 1) // ps if L else P // ps):
             expect.add(int(indices[indptr[bb] + j]))
     assert set(np.flatnonzero(written).tolist()) == expect
+
+
+# ---------------------------------------------------------------------------
+# bf16 state pools: states rounded to the nearest bf16 value, ties to even.
+# ---------------------------------------------------------------------------
+
+def _bf16_from_bits(bits):
+    return (np.asarray(bits, np.uint32) << 16).view(np.float32)
+
+
+def test_bf16_rounding_by_hand():
+    """The store rounding, on values whose nearest bf16 (8 significant bits,
+    ties to even) is worked out by hand: ties go to the even significand,
+    anything past a tie goes up, the fp32 exponent range with a 2^-133 quantum
+    below 2^-126, overflow to infinity past the largest finite value."""
+    cases = [
+        (1.0, 0x3F80),
+        (1 + 2.0 ** -8, 0x3F80),                 # tie between 1 and 1 + 2^-7: even is 1
+        (1 + 3 * 2.0 ** -8, 0x3F82),             # tie between 1 + 2^-7 and 1 + 2^-6: even is the latter
+        (1 + 2.0 ** -8 + 2.0 ** -30, 0x3F81),    # just past the tie
+        (-(1 + 2.0 ** -8 + 2.0 ** -40), 0xBF81),
+        (0.0, 0x0000),
+        (-0.0, 0x8000),
+        (1.5 * 2.0 ** -130, 0x000C),             # 12 quanta of 2^-133
+        (2.0 ** -134, 0x0000),                   # half a quantum: tie to the even 0
+        (3 * 2.0 ** -134, 0x0002),               # 1.5 quanta: tie to 2
+        ((2 - 2.0 ** -7) * 2.0 ** 127, 0x7F7F),  # the largest finite bf16
+        ((2 - 2.0 ** -8) * 2.0 ** 127, 0x7F80),  # its tie with 2^128 rounds to even: infinity
+        (float("inf"), 0x7F80),
+    ]
+    for x, want in cases:
+        assert oracle.double_to_bf16_bits(x) == want, (x, hex(oracle.double_to_bf16_bits(x)), hex(want))
+
+
+def test_bf16_pool_keeps_a_state_it_does_not_change():
+    """beta = 0 and g = 0 leave S as it is, so a bf16 pool row read, updated and
+    written back keeps its bits (bf16 -> fp64 -> bf16 is exact), in place and to
+    another row, and o = scale S q from those values."""
+    H, K, V = 2, 128, 128
+    rng = np.random.default_rng(11)
+    pool = (rng.standard_normal((3, H, V, K)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    q, k, v, _, _ = draw(1, H, 12)
+    zeros = np.zeros((1, H), np.float32)
+    before = pool.copy()
+    o, written = oracle.gated_delta_rule_decode(q, k, v, zeros, zeros, pool, [0], [2], SCALE)
+    assert written.tolist() == [0, 0, 1]
+    assert (pool[2] == before[0]).all() and (pool[:2] == before[:2]).all()
+    S = _bf16_from_bits(before[0]).astype(np.float64)
+    qd = bits_to_f64(q[0])
+    for h in range(H):
+        assert np.allclose(o[0, h], SCALE * S[h] @ qd[h], rtol=0, atol=1e-12)
+
+
+def test_bf16_pool_stores_the_nearest_value():
+    """g = 0, beta = 1, k = e_i writes v into column i; with v = 1 + 2^-8 and
+    1 + 3 2^-8 (bf16 ties) the bf16 pool holds 1 and 1 + 2^-6, while an fp32
+    pool holds the values exactly."""
+    K = V = 128
+    H, T = 1, 1
+    kk = np.zeros((T, H, K), np.float32)
+    kk[0, 0, 5] = 1.0
+    vv = np.zeros((T, H, V), np.float32)
+    vv[0, 0, 0::2] = 1 + 2.0 ** -8
+    vv[0, 0, 1::2] = 1 + 3 * 2.0 ** -8
+    to_bits = lambda a: (a.view(np.uint32) >> 16).astype(np.uint16)
+    # v is passed as bf16 bits; 1 + 2^-8 is not a bf16 value, so feed it through
+    # the state instead: start from S with column 5 equal to those values and
+    # apply beta = 0 (S unchanged) into a bf16 pool.
+    S0 = np.zeros((1, H, V, K), np.float32)
+    S0[0, 0, :, 5] = vv[0, 0]
+    f32_pool = S0.copy()
+    bf_pool = np.zeros((1, H, V, K), np.uint16)
+    zeros = np.zeros((T, H), np.float32)
+    q = to_bits(np.zeros((T, H, K), np.float32))
+    oracle.chunk_gated_delta_rule(q, to_bits(kk), q[:, :, :V], zeros, zeros, [0, T], SCALE,
+                                  initial_state=f32_pool, state_indices=[0], output_state=f32_pool,
+                                  output_state_indices=[0])
+    assert (f32_pool[0, 0, :, 5] == vv[0, 0]).all()
+    # same state, bf16 pool as the output (the read pool is the fp32 one)
+    with pytest.raises(TypeError):
+        oracle.chunk_gated_delta_rule(q, to_bits(kk), q[:, :, :V], zeros, zeros, [0, T], SCALE,
+                                      initial_state=S0, state_indices=[0], output_state=bf_pool,
+                                      output_state_indices=[0])
+    # a bf16 pool both read (zero row -1) and written: column 5 = beta v with
+    # beta = 1 + 2^-8 and v = 1 gives 1 + 2^-8 -> 1 (tie, even), with beta =
+    # 1 + 3 2^-8 it gives 1 + 2^-6
+    for beta, want in ((1 + 2.0 ** -8, 0x3F80), (1 + 3 * 2.0 ** -8, 0x3F82)):
+        bf_pool[:] = 0
+        ones_v = to_bits(np.ones((T, H, V), np.float32))
+        oracle.chunk_gated_delta_rule(q, to_bits(kk), ones_v, zeros, np.full((T, H), beta, np.float32), [0, T],
+                                      SCALE, initial_state=bf_pool, state_indices=[-1], output_state=bf_pool,
+                                      output_state_indices=[0])
+        assert (bf_pool[0, 0, :, 5] == want).all()
+        assert (np.delete(bf_pool[0, 0], 5, axis=1) == 0).all()
