@@ -39,6 +39,7 @@ FLOP_PER_TOKEN_HEAD = 10 * 64 * 128 + 6 * 128 * 128      # 180,224 (tensor-core 
 BYTES_PER_TOKEN_HEAD = 2 * (2 * K + 2 * V) + 8           # q, k, v, o bf16 + g, beta fp32 = 1032
 STATE_BYTES = V * K * 4                                   # one (row, head) state, fp32
 DECODE_BYTES_PER_SEQ_HEAD = 2 * STATE_BYTES + 2 * (2 * K + 2 * V) + 8   # 132,104
+DECODE_BF16_BYTES_PER_SEQ_HEAD = 2 * (V * K * 2) + 2 * (2 * K + 2 * V) + 8   # 66,568: bf16 state pool
 
 # DRAM bytes (read + write) of one paged prefill call per new token, over all heads:
 # ncu capture of the 4 x 8192-token case (ut_kernel 0.622 GB + prefill_kernel 1.516 GB
@@ -282,30 +283,34 @@ def _bench_decode(args, gdn, workloads, dev, stream, barrier, max_over_ranks, ra
     od = torch.empty(DECODE["B"], H, V, dtype=torch.bfloat16, device=dev)
     dslots = gdn.gdn_paged_decode_slots(dc.page_indptr, dc.page_indices, dc.last_page_len)
 
-    def decode_step(ev=None):
+    def decode_step(pool, ev=None):
         gdn.gdn_paged_decode_slots(dc.page_indptr, dc.page_indices, dc.last_page_len, out=dslots)
         if ev is not None:
             ev[0].record(stream)
-        gdn.gdn_gated_delta_rule_decode_paged(dc.q, dc.k, dc.v, dc.g, dc.beta, dpool, dc.page_indices,
+        gdn.gdn_gated_delta_rule_decode_paged(dc.q, dc.k, dc.v, dc.g, dc.beta, pool, dc.page_indices,
                                               dc.page_indptr, dc.last_page_len, scale=SCALE, slots=dslots, o=od)
         if ev is not None:
             ev[1].record(stream)
 
     dsteps = max(args.steps, 200)
-    for _ in range(max(args.warmup, 3)):
-        decode_step()
-    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(dsteps)]
-    with ClockSampler(dev.index) as clk:
-        barrier()
-        torch.cuda.synchronize(dev)
-        start.record(stream)
-        for i in range(dsteps):
-            decode_step(dev_ev[i])
-        stop.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier()
-    ms_decode = max_over_ranks(start.elapsed_time(stop) / dsteps)
-    dkernel_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
+
+    def timed(pool):
+        for _ in range(max(args.warmup, 3)):
+            decode_step(pool)
+        dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(dsteps)]
+        with ClockSampler(dev.index) as clk:
+            barrier()
+            torch.cuda.synchronize(dev)
+            start.record(stream)
+            for i in range(dsteps):
+                decode_step(pool, dev_ev[i])
+            stop.record(stream)
+            torch.cuda.synchronize(dev)
+            barrier()
+        return (max_over_ranks(start.elapsed_time(stop) / dsteps),
+                statistics.mean(a.elapsed_time(b) for a, b in dev_ev), clk.summary())
+
+    ms_decode, dkernel_ms, dclocks = timed(dpool)
     decode_bytes = DECODE["B"] * H * DECODE_BYTES_PER_SEQ_HEAD
     ach = decode_bytes / (dkernel_ms * 1e-3) / 1e9
     dec = {"metric": "decode seq/s", "value": DECODE["B"] * world / (ms_decode * 1e-3), "unit": "seq/s",
@@ -314,15 +319,28 @@ def _bench_decode(args, gdn, workloads, dev, stream, barrier, max_over_ranks, ra
                        "25% open a page, 10,000-page pool (step = decode slots + decode)",
            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                         "algorithmic_bytes": decode_bytes},
-           "clocks": clk.summary()}
+           "clocks": dclocks}
+    # The same batch on a bf16 state pool (the fp32 pool's values cut to bf16):
+    # half the state bytes, fp32 arithmetic on the chip.
+    bpool = (dpool.view(torch.int32) >> 16).to(torch.int16).view(torch.bfloat16)
+    ms_b, kms_b, clk_b = timed(bpool)
+    del bpool
+    bytes_b = DECODE["B"] * H * DECODE_BF16_BYTES_PER_SEQ_HEAD
+    ach_b = bytes_b / (kms_b * 1e-3) / 1e9
+    dec["bf16_state_pool"] = {
+        "value": DECODE["B"] * world / (ms_b * 1e-3), "unit": "seq/s", "ms_per_step": ms_b, "kernel_ms": kms_b,
+        "steps": dsteps, "roofline": {"bound": "hbm", "achieved": ach_b, "peak": hbm, "unit": "GB/s",
+                                      "frac": ach_b / hbm, "algorithmic_bytes": bytes_b},
+        "clocks": clk_b}
     if "metric" in line:
         line["decode"] = dec
     else:  # decode-only run: the decode measurement is the line
         line.update({"metric": METRIC, "value": dec["value"], "unit": "seq/s", "n_gpus": world, "steps": dsteps,
                      "warmup": max(args.warmup, 3), "ms_per_step": ms_decode, "higher_is_better": True,
                      "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
-                     "config": {"workload": dec["workload"]}, "roofline": dec["roofline"], "clocks": dec["clocks"]})
-    return 2 * dsteps
+                     "config": {"workload": dec["workload"]}, "roofline": dec["roofline"], "clocks": dec["clocks"],
+                     "bf16_state_pool": dec["bf16_state_pool"]})
+    return 4 * dsteps  # slots + decode, fp32 and bf16 pools
 
 
 # ---------------------------------------------------------------------------

@@ -74,6 +74,12 @@ def library():
                                                      P, i32, P, P, i32, P, P, P, sz, P, P],
                 "gdn_gated_delta_rule_decode_paged": [P, P, P, P, P, P, i32, i32, i32, i32, f32,
                                                       P, i32, P, P, P, P, P, P],
+                "gdn_chunk_gated_delta_rule_ex": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32,
+                                                  P, P, P, P, P, P, P, P, i32, i64, i32, P, sz, P, P],
+                "gdn_chunk_gated_delta_rule_paged_ex": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32,
+                                                        P, i32, i32, P, P, i32, P, P, P, sz, P, P],
+                "gdn_gated_delta_rule_decode_paged_ex": [P, P, P, P, P, P, i32, i32, i32, i32, f32,
+                                                         P, i32, i32, P, P, P, P, P, P],
             }
             for name, args in sig.items():
                 fn = getattr(lib, name)
@@ -116,6 +122,21 @@ def _opt(t, dtype, name):
 def _check(fn, status):
     if status != 0:
         raise GdnError(fn, status)
+
+
+# State pool element types (GDN_STATE_F32 / GDN_STATE_BF16 of the C header).
+_STATE_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+
+def _state_dtype(pools, names):
+    """The pools' common element type code; fp32 or bf16 pools, all alike."""
+    kinds = {p.dtype for p in pools if p is not None}
+    if len(kinds) > 1:
+        raise TypeError("%s must share one dtype" % ", ".join(names))
+    kind = kinds.pop() if kinds else torch.float32
+    if kind not in _STATE_DTYPES:
+        raise TypeError("state pools must be float32 or bfloat16, got %s" % kind)
+    return _STATE_DTYPES[kind]
 
 
 def gdn_status_string(status: int) -> str:
@@ -197,9 +218,11 @@ def gdn_chunk_gated_delta_rule(q, k, v, g, beta, cu_seqlens, *, scale=0.0, initi
     gdn_prefill_workspace_bytes(num_seqs, T, H) bytes."""
     T, H, K, V = _tokens(q, k, v, g, beta)
     _need(cu_seqlens, torch.int32, "cu_seqlens")
-    f32, i32 = torch.float32, torch.int32
-    pools = [_opt(p, f32, n) for p, n in ((initial_state, "initial_state"), (output_state, "output_state"),
-                                          (state_checkpoints, "state_checkpoints"))]
+    i32 = torch.int32
+    pool_names = ("initial_state", "output_state", "state_checkpoints")
+    sd = _state_dtype((initial_state, output_state, state_checkpoints), pool_names)
+    pdt = torch.bfloat16 if sd else torch.float32
+    pools = [_opt(p, pdt, n) for p, n in zip((initial_state, output_state, state_checkpoints), pool_names)]
     stride = 0
     for p in pools:
         if p is not None:
@@ -208,14 +231,17 @@ def gdn_chunk_gated_delta_rule(q, k, v, g, beta, cu_seqlens, *, scale=0.0, initi
         o = torch.empty(T, H, V, dtype=torch.bfloat16, device=q.device)
     _need(o, torch.bfloat16, "o", 3)
     ws = _workspace(workspace, cu_seqlens.numel() - 1, T, H, q.device)
-    _check("gdn_chunk_gated_delta_rule", library().gdn_chunk_gated_delta_rule(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(o), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, H,
-        K, V, float(scale), _ptr(pools[0]), _ptr(_opt(state_indices, i32, "state_indices")), _ptr(pools[1]),
-        _ptr(_opt(output_state_indices, i32, "output_state_indices")), _ptr(pools[2]),
-        _ptr(_opt(checkpoint_state_indices, i32, "checkpoint_state_indices")),
-        _ptr(_opt(checkpoint_cu_starts, i32, "checkpoint_cu_starts")), _ptr(_opt(prefix_lens, i32, "prefix_lens")),
-        int(checkpoint_every_n_tokens), stride, _ptr(ws), ws.numel(), _ptr(_opt(err_word, i32, "err_word")),
-        _stream(q)))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(o), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, H,
+            K, V, float(scale), _ptr(pools[0]), _ptr(_opt(state_indices, i32, "state_indices")), _ptr(pools[1]),
+            _ptr(_opt(output_state_indices, i32, "output_state_indices")), _ptr(pools[2]),
+            _ptr(_opt(checkpoint_state_indices, i32, "checkpoint_state_indices")),
+            _ptr(_opt(checkpoint_cu_starts, i32, "checkpoint_cu_starts")), _ptr(_opt(prefix_lens, i32, "prefix_lens")),
+            int(checkpoint_every_n_tokens), stride)
+    tail = (_ptr(ws), ws.numel(), _ptr(_opt(err_word, i32, "err_word")), _stream(q))
+    if sd:
+        _check("gdn_chunk_gated_delta_rule_ex", library().gdn_chunk_gated_delta_rule_ex(*args, sd, *tail))
+    else:
+        _check("gdn_chunk_gated_delta_rule", library().gdn_chunk_gated_delta_rule(*args, *tail))
     return o
 
 
@@ -228,7 +254,8 @@ def gdn_chunk_gated_delta_rule_paged(q, k, v, g, beta, cu_seqlens, state_pool, p
     T, H, K, V = _tokens(q, k, v, g, beta)
     i32 = torch.int32
     _need(cu_seqlens, i32, "cu_seqlens")
-    _need(state_pool, torch.float32, "state_pool", 4)
+    sd = _state_dtype((state_pool,), ("state_pool",))
+    _need(state_pool, torch.bfloat16 if sd else torch.float32, "state_pool", 4)
     for t, n in ((page_indices, "page_indices"), (page_indptr, "page_indptr"), (last_page_len, "last_page_len")):
         _need(t, i32, n)
     if o is None:
@@ -239,11 +266,15 @@ def gdn_chunk_gated_delta_rule_paged(q, k, v, g, beta, cu_seqlens, state_pool, p
     if slots is not None:
         sl = _PrefillSlots(*[_ptr(_need(slots[n], i32, n)) for n in
                              ("state_indices", "output_state_indices", "checkpoint_cu_starts", "prefix_lens")])
-    _check("gdn_chunk_gated_delta_rule_paged", library().gdn_chunk_gated_delta_rule_paged(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(o), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, H,
-        K, V, float(scale), _ptr(state_pool), state_pool.shape[0], _ptr(page_indices), _ptr(page_indptr),
-        int(page_size), _ptr(last_page_len), None if sl is None else ctypes.byref(sl), _ptr(ws), ws.numel(),
-        _ptr(_opt(err_word, i32, "err_word")), _stream(q)))
+    head = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(o), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, H,
+            K, V, float(scale), _ptr(state_pool))
+    rest = (state_pool.shape[0], _ptr(page_indices), _ptr(page_indptr), int(page_size), _ptr(last_page_len),
+            None if sl is None else ctypes.byref(sl), _ptr(ws), ws.numel(), _ptr(_opt(err_word, i32, "err_word")),
+            _stream(q))
+    if sd:
+        _check("gdn_chunk_gated_delta_rule_paged_ex", library().gdn_chunk_gated_delta_rule_paged_ex(*head, sd, *rest))
+    else:
+        _check("gdn_chunk_gated_delta_rule_paged", library().gdn_chunk_gated_delta_rule_paged(*head, *rest))
     return o
 
 
@@ -254,7 +285,8 @@ def gdn_gated_delta_rule_decode_paged(q, k, v, g, beta, state_pool, page_indices
     (optional).  Returns o (bf16 [B, H, V])."""
     B, H, K, V = _tokens(q, k, v, g, beta)
     i32 = torch.int32
-    _need(state_pool, torch.float32, "state_pool", 4)
+    sd = _state_dtype((state_pool,), ("state_pool",))
+    _need(state_pool, torch.bfloat16 if sd else torch.float32, "state_pool", 4)
     for t, n in ((page_indices, "page_indices"), (page_indptr, "page_indptr"), (last_page_len, "last_page_len")):
         _need(t, i32, n)
     if o is None:
@@ -263,8 +295,11 @@ def gdn_gated_delta_rule_decode_paged(q, k, v, g, beta, state_pool, page_indices
     sl = None
     if slots is not None:
         sl = _DecodeSlots(*[_ptr(_need(slots[n], i32, n)) for n in ("initial_state_indices", "output_state_indices")])
-    _check("gdn_gated_delta_rule_decode_paged", library().gdn_gated_delta_rule_decode_paged(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(o), B, H, K, V, float(scale), _ptr(state_pool),
-        state_pool.shape[0], _ptr(page_indices), _ptr(page_indptr), _ptr(last_page_len),
-        None if sl is None else ctypes.byref(sl), _ptr(_opt(err_word, i32, "err_word")), _stream(q)))
+    head = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(o), B, H, K, V, float(scale), _ptr(state_pool))
+    rest = (state_pool.shape[0], _ptr(page_indices), _ptr(page_indptr), _ptr(last_page_len),
+            None if sl is None else ctypes.byref(sl), _ptr(_opt(err_word, i32, "err_word")), _stream(q))
+    if sd:
+        _check("gdn_gated_delta_rule_decode_paged_ex", library().gdn_gated_delta_rule_decode_paged_ex(*head, sd, *rest))
+    else:
+        _check("gdn_gated_delta_rule_decode_paged", library().gdn_gated_delta_rule_decode_paged(*head, *rest))
     return o

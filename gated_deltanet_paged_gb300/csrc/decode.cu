@@ -1,8 +1,9 @@
 // decode.cu -- single-token paged GDN decode ("flashinfer.gdn_paged",
 // gated_delta_rule_decode_paged and the decode paragraph).
 //
-// For every (sequence b, head h) the 128 x 128 fp32 state is read once from
-// its read row, updated and written once to its write row:
+// For every (sequence b, head h) the 128 x 128 state (fp32, or bf16 in a bf16
+// pool: carried in fp32 and rounded to the nearest bf16 on the way out) is read
+// once from its read row, updated and written once to its write row:
 //     S' = e S + beta (v - e S k) k^T,   o = scale S' q = scale (e S q + d (k.q))
 // with e = exp(g) and d = beta (v - e S k) per state row.  The kernel is a
 // streaming read-update-write bound by HBM bandwidth: each warp owns 16 rows,
@@ -27,7 +28,7 @@ struct DecodeArgs {
   const float* g;
   const float* beta;
   __nv_bfloat16* o;
-  float* pool;
+  void* pool;  // float or __nv_bfloat16 elements (the kernel's template argument)
   int64_t row_stride;
   int32_t H;
   int32_t num_pages;
@@ -65,6 +66,19 @@ __device__ __forceinline__ void bf16x4(const __nv_bfloat16* p, float (&f)[4]) {
   f[3] = b.y;
 }
 
+// Four consecutive state values of one row: 16 bytes of fp32 or 8 of bf16.
+__device__ __forceinline__ float4 load4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 u = __ldcs(reinterpret_cast<const uint2*>(p));
+  const float2 a = gdn::unpack_bf162(u.x), b = gdn::unpack_bf162(u.y);
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void store4(float* p, float4 x) { __stcs(reinterpret_cast<float4*>(p), x); }
+__device__ __forceinline__ void store4(__nv_bfloat16* p, float4 x) {
+  __stcs(reinterpret_cast<uint2*>(p), make_uint2(gdn::pack_bf162(x.x, x.y), gdn::pack_bf162(x.z, x.w)));
+}
+
+template <typename St>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a) {
   const int bh = blockIdx.x;
   const int b = bh / a.H, h = bh % a.H;
@@ -100,12 +114,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
   const int r0 = warp * kRowsPerWarp;
   const int64_t head_off = static_cast<int64_t>(h) * gdn::kDimV * gdn::kDimK;
 
+  St* const pool = static_cast<St*>(a.pool);
   float4 s[kRowsPerWarp];
   if (in_row >= 0) {
-    const float4* src =
-        reinterpret_cast<const float4*>(a.pool + in_row * a.row_stride + head_off + r0 * gdn::kDimK) + lane;
+    const St* src = pool + in_row * a.row_stride + head_off + r0 * gdn::kDimK + 4 * lane;
 #pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) s[i] = __ldcs(src + i * (gdn::kDimK / 4));
+    for (int i = 0; i < kRowsPerWarp; ++i) s[i] = load4(src + i * gdn::kDimK);
   } else {
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -136,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
         __float2bfloat16_rn(a.scale * (e * red + d_row * kq));
 
   if (out_row >= 0) {
-    float4* dst = reinterpret_cast<float4*>(a.pool + out_row * a.row_stride + head_off + r0 * gdn::kDimK) + lane;
+    St* dst = pool + out_row * a.row_stride + head_off + r0 * gdn::kDimK + 4 * lane;
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
       const float di = __shfl_sync(0xffffffffu, d, 2 * i);
@@ -145,20 +159,22 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
       n.y = e * s[i].y + di * kk[1];
       n.z = e * s[i].z + di * kk[2];
       n.w = e * s[i].w + di * kk[3];
-      __stcs(dst + i * (gdn::kDimK / 4), n);
+      store4(dst + i * gdn::kDimK, n);
     }
   }
 }
 
 }  // namespace
 
-extern "C" int gdn_gated_delta_rule_decode_paged(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
-                                                 const float* g, const float* beta, gdn_bf16* o, int32_t batch,
-                                                 int32_t H, int32_t K, int32_t V, float scale, float* state_pool,
-                                                 int32_t num_pages, const int32_t* page_indices,
-                                                 const int32_t* page_indptr, const int32_t* last_page_len,
-                                                 const gdn_decode_slots* slots, int32_t* err_word, void* stream) {
+extern "C" int gdn_gated_delta_rule_decode_paged_ex(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                                                    const float* g, const float* beta, gdn_bf16* o, int32_t batch,
+                                                    int32_t H, int32_t K, int32_t V, float scale, void* state_pool,
+                                                    int32_t state_dtype, int32_t num_pages,
+                                                    const int32_t* page_indices, const int32_t* page_indptr,
+                                                    const int32_t* last_page_len, const gdn_decode_slots* slots,
+                                                    int32_t* err_word, void* stream) {
   if (batch < 0 || H < 1 || num_pages < 1) return GDN_ERR_INVALID_ARGUMENT;
+  if (state_dtype != GDN_STATE_F32 && state_dtype != GDN_STATE_BF16) return GDN_ERR_INVALID_ARGUMENT;
   if (K != gdn::kDimK || V != gdn::kDimV) return GDN_ERR_UNSUPPORTED;
   if (!q || !k || !v || !g || !beta || !o || !state_pool) return GDN_ERR_INVALID_ARGUMENT;
   if (slots) {
@@ -194,6 +210,21 @@ extern "C" int gdn_gated_delta_rule_decode_paged(const gdn_bf16* q, const gdn_bf
   a.pages = page_indices;
   a.last_len = last_page_len;
   a.err_word = err_word;
-  decode_kernel<<<batch * H, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (state_dtype == GDN_STATE_BF16)
+    decode_kernel<__nv_bfloat16><<<batch * H, kThreads, 0, st>>>(a);
+  else
+    decode_kernel<float><<<batch * H, kThreads, 0, st>>>(a);
   return gdn_host::launch_status();
+}
+
+extern "C" int gdn_gated_delta_rule_decode_paged(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                                                 const float* g, const float* beta, gdn_bf16* o, int32_t batch,
+                                                 int32_t H, int32_t K, int32_t V, float scale, float* state_pool,
+                                                 int32_t num_pages, const int32_t* page_indices,
+                                                 const int32_t* page_indptr, const int32_t* last_page_len,
+                                                 const gdn_decode_slots* slots, int32_t* err_word, void* stream) {
+  return gdn_gated_delta_rule_decode_paged_ex(q, k, v, g, beta, o, batch, H, K, V, scale, state_pool, GDN_STATE_F32,
+                                              num_pages, page_indices, page_indptr, last_page_len, slots, err_word,
+                                              stream);
 }

@@ -563,9 +563,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       return ok;
     };
     float S[64];
-    if (in_row >= 0) {
-      const float4* src =
-          reinterpret_cast<const float4*>(init_pool + in_row * a.row_stride + head_off + v * kDimK + 64 * hc);
+    // Element offset of this thread's 64 state values (row v, columns 64 hc ..)
+    // in pool row `row`; pools hold fp32 or (state_bf16) bf16 elements.
+    auto state_off = [&](int row) { return row * a.row_stride + head_off + v * kDimK + 64 * hc; };
+    if (in_row >= 0 && a.state_bf16) {
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(init_pool) +
+                                                        state_off(in_row));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 x = src[i];
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = unpack_bf162(w[j]);
+          S[8 * i + 2 * j] = f.x;
+          S[8 * i + 2 * j + 1] = f.y;
+        }
+      }
+    } else if (in_row >= 0) {
+      const float4* src = reinterpret_cast<const float4*>(init_pool + state_off(in_row));
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float4 x = src[i];
@@ -651,7 +667,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     auto store_state = [&](float* pool, int row) {
-      float4* dst = reinterpret_cast<float4*>(pool + row * a.row_stride + head_off + v * kDimK + 64 * hc);
+      if (a.state_bf16) {  // nearest bf16, ties to even
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pool) + state_off(row));
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          dst[i] = make_uint4(pack_bf162(S[8 * i], S[8 * i + 1]), pack_bf162(S[8 * i + 2], S[8 * i + 3]),
+                              pack_bf162(S[8 * i + 4], S[8 * i + 5]), pack_bf162(S[8 * i + 6], S[8 * i + 7]));
+        return;
+      }
+      float4* dst = reinterpret_cast<float4*>(pool + state_off(row));
 #pragma unroll
       for (int i = 0; i < 16; ++i) dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
     };
@@ -839,6 +863,54 @@ extern "C" size_t gdn_prefill_workspace_bytes(int32_t num_seqs, int32_t total_to
   return gdn::workspace_bytes(total_tokens, num_seqs, H);
 }
 
+extern "C" int gdn_chunk_gated_delta_rule_ex(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                                             const float* g, const float* beta, gdn_bf16* o,
+                                             const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                                             int32_t H, int32_t K, int32_t V, float scale, const void* initial_state,
+                                             const int32_t* state_indices, void* output_state,
+                                             const int32_t* output_state_indices, void* state_checkpoints,
+                                             const int32_t* checkpoint_state_indices,
+                                             const int32_t* checkpoint_cu_starts, const int32_t* prefix_lens,
+                                             int32_t checkpoint_every_n_tokens, int64_t pool_row_stride,
+                                             int32_t state_dtype, void* workspace, size_t workspace_bytes,
+                                             int32_t* err_word, void* stream) {
+  int rc = check_common(q, k, v, g, beta, o, cu_seqlens, num_seqs, total_tokens, H, K, V);
+  if (rc != GDN_OK) return rc;
+  if (state_dtype != GDN_STATE_F32 && state_dtype != GDN_STATE_BF16) return GDN_ERR_INVALID_ARGUMENT;
+  if ((state_indices != nullptr) != (initial_state != nullptr)) return GDN_ERR_INVALID_ARGUMENT;
+  if ((output_state_indices != nullptr) != (output_state != nullptr)) return GDN_ERR_INVALID_ARGUMENT;
+  const int nck = (state_checkpoints != nullptr) + (checkpoint_state_indices != nullptr) +
+                  (checkpoint_cu_starts != nullptr);
+  if (nck != 0 && nck != 3) return GDN_ERR_INVALID_ARGUMENT;
+  if (nck == 3 && (!prefix_lens || checkpoint_every_n_tokens <= 0 || checkpoint_every_n_tokens % kChunk != 0))
+    return GDN_ERR_INVALID_ARGUMENT;
+  const bool any_pool = initial_state || output_state || state_checkpoints;
+  const int64_t stride_unit = state_dtype == GDN_STATE_BF16 ? 8 : 4;  // 16-byte rows
+  if (any_pool &&
+      (pool_row_stride < static_cast<int64_t>(H) * kDimV * kDimK || pool_row_stride % stride_unit != 0))
+    return GDN_ERR_INVALID_ARGUMENT;
+  using gdn_host::aligned16;
+  if ((initial_state && !aligned16(initial_state)) || (output_state && !aligned16(output_state)) ||
+      (state_checkpoints && !aligned16(state_checkpoints)))
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (num_seqs == 0 || total_tokens == 0) return GDN_OK;
+
+  PrefillArgs a;
+  fill_common(a, g, beta, o, cu_seqlens, num_seqs, total_tokens, H, scale, err_word);
+  a.initial_state = static_cast<const float*>(initial_state);
+  a.state_indices = state_indices;
+  a.output_state = static_cast<float*>(output_state);
+  a.output_state_indices = output_state_indices;
+  a.state_checkpoints = static_cast<float*>(state_checkpoints);
+  a.checkpoint_state_indices = checkpoint_state_indices;
+  a.checkpoint_cu_starts = checkpoint_cu_starts;
+  a.prefix_lens = prefix_lens;
+  a.N = nck ? checkpoint_every_n_tokens : 0;
+  a.row_stride = any_pool ? pool_row_stride : 0;
+  a.state_bf16 = state_dtype == GDN_STATE_BF16;
+  return launch(a, q, k, v, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" int gdn_chunk_gated_delta_rule(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const float* g,
                                           const float* beta, gdn_bf16* o, const int32_t* cu_seqlens,
                                           int32_t num_seqs, int32_t total_tokens, int32_t H, int32_t K, int32_t V,
@@ -849,50 +921,25 @@ extern "C" int gdn_chunk_gated_delta_rule(const gdn_bf16* q, const gdn_bf16* k, 
                                           int32_t checkpoint_every_n_tokens, int64_t pool_row_stride,
                                           void* workspace, size_t workspace_bytes, int32_t* err_word,
                                           void* stream) {
-  int rc = check_common(q, k, v, g, beta, o, cu_seqlens, num_seqs, total_tokens, H, K, V);
-  if (rc != GDN_OK) return rc;
-  if ((state_indices != nullptr) != (initial_state != nullptr)) return GDN_ERR_INVALID_ARGUMENT;
-  if ((output_state_indices != nullptr) != (output_state != nullptr)) return GDN_ERR_INVALID_ARGUMENT;
-  const int nck = (state_checkpoints != nullptr) + (checkpoint_state_indices != nullptr) +
-                  (checkpoint_cu_starts != nullptr);
-  if (nck != 0 && nck != 3) return GDN_ERR_INVALID_ARGUMENT;
-  if (nck == 3 && (!prefix_lens || checkpoint_every_n_tokens <= 0 || checkpoint_every_n_tokens % kChunk != 0))
-    return GDN_ERR_INVALID_ARGUMENT;
-  const bool any_pool = initial_state || output_state || state_checkpoints;
-  if (any_pool && (pool_row_stride < static_cast<int64_t>(H) * kDimV * kDimK || pool_row_stride % 4 != 0))
-    return GDN_ERR_INVALID_ARGUMENT;
-  using gdn_host::aligned16;
-  if ((initial_state && !aligned16(initial_state)) || (output_state && !aligned16(output_state)) ||
-      (state_checkpoints && !aligned16(state_checkpoints)))
-    return GDN_ERR_INVALID_ARGUMENT;
-  if (num_seqs == 0 || total_tokens == 0) return GDN_OK;
-
-  PrefillArgs a;
-  fill_common(a, g, beta, o, cu_seqlens, num_seqs, total_tokens, H, scale, err_word);
-  a.initial_state = initial_state;
-  a.state_indices = state_indices;
-  a.output_state = output_state;
-  a.output_state_indices = output_state_indices;
-  a.state_checkpoints = state_checkpoints;
-  a.checkpoint_state_indices = checkpoint_state_indices;
-  a.checkpoint_cu_starts = checkpoint_cu_starts;
-  a.prefix_lens = prefix_lens;
-  a.N = nck ? checkpoint_every_n_tokens : 0;
-  a.row_stride = any_pool ? pool_row_stride : 0;
-  return launch(a, q, k, v, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+  return gdn_chunk_gated_delta_rule_ex(q, k, v, g, beta, o, cu_seqlens, num_seqs, total_tokens, H, K, V, scale,
+                                       initial_state, state_indices, output_state, output_state_indices,
+                                       state_checkpoints, checkpoint_state_indices, checkpoint_cu_starts, prefix_lens,
+                                       checkpoint_every_n_tokens, pool_row_stride, GDN_STATE_F32, workspace,
+                                       workspace_bytes, err_word, stream);
 }
 
-extern "C" int gdn_chunk_gated_delta_rule_paged(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
-                                                const float* g, const float* beta, gdn_bf16* o,
-                                                const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens,
-                                                int32_t H, int32_t K, int32_t V, float scale, float* state_pool,
-                                                int32_t num_pages, const int32_t* page_indices,
-                                                const int32_t* page_indptr, int32_t page_size,
-                                                const int32_t* last_page_len, const gdn_prefill_slots* slots,
-                                                void* workspace, size_t workspace_bytes, int32_t* err_word,
-                                                void* stream) {
+extern "C" int gdn_chunk_gated_delta_rule_paged_ex(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                                                   const float* g, const float* beta, gdn_bf16* o,
+                                                   const int32_t* cu_seqlens, int32_t num_seqs,
+                                                   int32_t total_tokens, int32_t H, int32_t K, int32_t V, float scale,
+                                                   void* state_pool, int32_t state_dtype, int32_t num_pages,
+                                                   const int32_t* page_indices, const int32_t* page_indptr,
+                                                   int32_t page_size, const int32_t* last_page_len,
+                                                   const gdn_prefill_slots* slots, void* workspace,
+                                                   size_t workspace_bytes, int32_t* err_word, void* stream) {
   int rc = check_common(q, k, v, g, beta, o, cu_seqlens, num_seqs, total_tokens, H, K, V);
   if (rc != GDN_OK) return rc;
+  if (state_dtype != GDN_STATE_F32 && state_dtype != GDN_STATE_BF16) return GDN_ERR_INVALID_ARGUMENT;
   if (page_size <= 0 || page_size % kChunk != 0 || num_pages < 1) return GDN_ERR_INVALID_ARGUMENT;
   if (!state_pool || !gdn_host::aligned16(state_pool)) return GDN_ERR_INVALID_ARGUMENT;
   if (num_seqs > 0 && (!page_indices || !page_indptr || !last_page_len)) return GDN_ERR_INVALID_ARGUMENT;
@@ -903,12 +950,13 @@ extern "C" int gdn_chunk_gated_delta_rule_paged(const gdn_bf16* q, const gdn_bf1
 
   PrefillArgs a;
   fill_common(a, g, beta, o, cu_seqlens, num_seqs, total_tokens, H, scale, err_word);
-  a.initial_state = state_pool;
-  a.output_state = state_pool;
-  a.state_checkpoints = state_pool;
+  a.initial_state = static_cast<const float*>(state_pool);
+  a.output_state = static_cast<float*>(state_pool);
+  a.state_checkpoints = static_cast<float*>(state_pool);
   a.checkpoint_state_indices = page_indices;
   a.N = page_size;
   a.row_stride = static_cast<int64_t>(H) * kDimV * kDimK;
+  a.state_bf16 = state_dtype == GDN_STATE_BF16;
   a.num_pages = num_pages;
   a.page_size = page_size;
   if (slots) {
@@ -922,6 +970,21 @@ extern "C" int gdn_chunk_gated_delta_rule_paged(const gdn_bf16* q, const gdn_bf1
     a.last_len = last_page_len;
   }
   return launch(a, q, k, v, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gdn_chunk_gated_delta_rule_paged(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v,
+                                                const float* g, const float* beta, gdn_bf16* o,
+                                                const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                                                int32_t H, int32_t K, int32_t V, float scale, float* state_pool,
+                                                int32_t num_pages, const int32_t* page_indices,
+                                                const int32_t* page_indptr, int32_t page_size,
+                                                const int32_t* last_page_len, const gdn_prefill_slots* slots,
+                                                void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                                void* stream) {
+  return gdn_chunk_gated_delta_rule_paged_ex(q, k, v, g, beta, o, cu_seqlens, num_seqs, total_tokens, H, K, V, scale,
+                                             state_pool, GDN_STATE_F32, num_pages, page_indices, page_indptr,
+                                             page_size, last_page_len, slots, workspace, workspace_bytes, err_word,
+                                             stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -30,7 +30,8 @@ struct PrefillArgs {
   const int32_t* checkpoint_cu_starts;
   const int32_t* prefix_lens;
   int32_t N;
-  int64_t row_stride;
+  int64_t row_stride;  // elements of the pools' type
+  int32_t state_bf16;  // pools of bf16 (states widened on load, rounded to nearest on store), else fp32
   // Paged mode without precomputed slots: rows come from the page table.
   const int32_t* indptr;
   const int32_t* pages;

@@ -19,9 +19,10 @@
  *   - Token layout is packed varlen: q, k are [T, H, K], v and o are [T, H, V],
  *     g and beta are [T, H] (fp32, g is the log-space gate applied as exp(g)).
  *     Decode uses [B, H, .] (the same memory as [B, 1, H, .]).
- *   - The state pool is fp32 [rows, H, V, K]; one row is a dense [H, V, K]
- *     block at row * pool_row_stride elements.  Page j of a sequence holds the
- *     state after the last token of that page.
+ *   - The state pool is fp32 [rows, H, V, K] (or bf16 through the _ex calls,
+ *     see GDN_STATE_BF16); one row is a dense [H, V, K] block at
+ *     row * pool_row_stride elements.  Page j of a sequence holds the state
+ *     after the last token of that page.
  *   - Page tables are CSR: sequence b owns page_indices[page_indptr[b] ..
  *     page_indptr[b+1]) (any ids, any order) and has
  *     (num_pages_b - 1) * page_size + last_page_len[b] tokens AFTER the call;
@@ -59,6 +60,15 @@ typedef uint16_t gdn_bf16; /* raw bfloat16 bit pattern */
 #define GDN_ERR_INVALID_ARGUMENT (-1) /* null pointer, bad scalar, misalignment */
 #define GDN_ERR_UNSUPPORTED (-2)      /* K or V other than 128, no sm_103a device */
 #define GDN_ERR_CUDA (-3)             /* a CUDA launch or driver call failed */
+
+/* Element type of a state pool (the state_dtype of the _ex calls).  The pages
+ * ask for a state dtype that prefill and decode both support.  With
+ * GDN_STATE_BF16 the kernels still carry every state in fp32 on the chip; a
+ * state read from the pool is widened exactly, and a stored state is rounded
+ * to the nearest bf16 value (ties to even).  pool_row_stride then counts bf16
+ * elements. */
+#define GDN_STATE_F32 0
+#define GDN_STATE_BF16 1
 
 #define GDN_DEVERR_PAGE_ID 1       /* a page id outside [0, num_pages) */
 #define GDN_DEVERR_PAGE_TABLE 2    /* no page, last_page_len outside 1..page_size, more new tokens than tokens, or tokens past total_tokens */
@@ -209,6 +219,42 @@ int gdn_gated_delta_rule_decode_paged(const gdn_bf16 *q, const gdn_bf16 *k, cons
                                       const int32_t *page_indices, const int32_t *page_indptr,
                                       const int32_t *last_page_len, const gdn_decode_slots *slots,
                                       int32_t *err_word, void *stream);
+
+/* The three calls above with the pool element type as an argument
+ * (state_dtype: GDN_STATE_F32 or GDN_STATE_BF16; anything else is
+ * GDN_ERR_INVALID_ARGUMENT).  Pools are passed untyped; every pool of one call
+ * has that element type.  For bf16 pools pool_row_stride (elements) must be a
+ * multiple of 8, so rows stay 16-byte aligned.  The fp32 calls above are these
+ * with GDN_STATE_F32. */
+int gdn_chunk_gated_delta_rule_ex(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                                  const float *g, const float *beta, gdn_bf16 *o,
+                                  const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                                  int32_t H, int32_t K, int32_t V, float scale,
+                                  const void *initial_state, const int32_t *state_indices,
+                                  void *output_state, const int32_t *output_state_indices,
+                                  void *state_checkpoints, const int32_t *checkpoint_state_indices,
+                                  const int32_t *checkpoint_cu_starts, const int32_t *prefix_lens,
+                                  int32_t checkpoint_every_n_tokens, int64_t pool_row_stride,
+                                  int32_t state_dtype, void *workspace, size_t workspace_bytes,
+                                  int32_t *err_word, void *stream);
+int gdn_chunk_gated_delta_rule_paged_ex(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                                        const float *g, const float *beta, gdn_bf16 *o,
+                                        const int32_t *cu_seqlens, int32_t num_seqs,
+                                        int32_t total_tokens, int32_t H, int32_t K, int32_t V,
+                                        float scale, void *state_pool, int32_t state_dtype,
+                                        int32_t num_pages, const int32_t *page_indices,
+                                        const int32_t *page_indptr, int32_t page_size,
+                                        const int32_t *last_page_len, const gdn_prefill_slots *slots,
+                                        void *workspace, size_t workspace_bytes, int32_t *err_word,
+                                        void *stream);
+int gdn_gated_delta_rule_decode_paged_ex(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
+                                         const float *g, const float *beta, gdn_bf16 *o,
+                                         int32_t batch, int32_t H, int32_t K, int32_t V,
+                                         float scale, void *state_pool, int32_t state_dtype,
+                                         int32_t num_pages, const int32_t *page_indices,
+                                         const int32_t *page_indptr, const int32_t *last_page_len,
+                                         const gdn_decode_slots *slots, int32_t *err_word,
+                                         void *stream);
 
 /* Bytes of device workspace a prefill call over num_seqs sequences,
  * total_tokens new tokens and H heads needs (0 for invalid arguments).  The

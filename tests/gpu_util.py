@@ -4,7 +4,10 @@ and through the oracle on the same inputs, and compare.
 Acceptance (written here once, used by every GPU test):
   - slots, page tables, untouched pool rows: bit-exact;
   - outputs o: max-abs difference <= 1e-2 against the fp64 oracle;
-  - every written state: relative Frobenius error <= 1e-3 per (row, head).
+  - every written state: relative Frobenius error <= 1e-3 per (row, head);
+    in a bf16 pool <= 5e-3: both sides round their state to the nearest bf16
+    (the oracle from fp64, the GPU from fp32), which adds at most one bf16
+    step, 2^-8 of the value, to the fp32 bound.
 """
 import numpy as np
 import torch
@@ -15,6 +18,7 @@ from conftest import bf16_bits, f32, i32
 
 O_TOL = 1e-2
 S_TOL = 1e-3
+S_TOL_BF16 = 5e-3
 SCALE = 128 ** -0.5
 
 
@@ -47,23 +51,41 @@ def check_o(o_gpu, o_ref, errs, rows=None):
 
 
 def bits_equal(a, b):
-    return torch.equal(a.view(torch.int32), b.view(torch.int32))
+    it = torch.int16 if a.element_size() == 2 else torch.int32
+    return torch.equal(a.view(it), b.view(it))
+
+
+def bf16_pool_pair(pool_f32):
+    """A bf16 pool for the GPU (torch) and the oracle (uint16 bits) from an fp32
+    pool: each value cut to its top 16 bits (NaN sentinels stay NaN)."""
+    bits = (pool_f32.view(torch.int32) >> 16).to(torch.int16)
+    return bits.view(torch.bfloat16), bits.cpu().numpy().view(np.uint16).copy()
+
+
+def _pool_f64(p):
+    """fp32 or bf16 pool (torch or numpy uint16 bits) as float64 numpy."""
+    if isinstance(p, torch.Tensor):
+        return p.float().cpu().numpy().astype(np.float64)
+    if p.dtype == np.uint16:
+        return (p.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return p.astype(np.float64)
 
 
 def check_pool(pool_after, pool_before, ref_pool, written, errs, label="pool"):
     """Written rows within S_TOL of the oracle; all other rows bit-identical
     to their contents before the call."""
     written = np.flatnonzero(np.asarray(written))
+    tol = S_TOL_BF16 if pool_after.dtype == torch.bfloat16 else S_TOL
     keep = torch.ones(pool_after.shape[0], dtype=torch.bool, device=pool_after.device)
     if len(written):
         w = torch.as_tensor(written, device=pool_after.device)
         keep[w] = False
-        got = pool_after[w].cpu().numpy()
+        got = _pool_f64(pool_after[w])
         assert np.isfinite(got).all(), "%s: non-finite written state" % label
-        e = rel_fro_rows(got, ref_pool[written])
+        e = rel_fro_rows(got, _pool_f64(ref_pool[written]))
         errs.state = max(errs.state, float(e.max()))
-        assert e.max() <= S_TOL, "%s: state rel-fro %.4g > %g (row %d)" % (
-            label, e.max(), S_TOL, written[np.unravel_index(e.argmax(), e.shape)[0]])
+        assert e.max() <= tol, "%s: state rel-fro %.4g > %g (row %d)" % (
+            label, e.max(), tol, written[np.unravel_index(e.argmax(), e.shape)[0]])
     assert bits_equal(pool_after[keep], pool_before[keep]), "%s: a row outside the write set changed" % label
 
 

@@ -12,15 +12,18 @@ import gated_deltanet_paged_gb300 as gdn
 import oracle
 from gated_deltanet_paged_gb300 import workloads
 from conftest import bf16_bits, f32, i32
-from gpu_util import SCALE, Errors, bits_equal, check_o, check_pool, rel_fro_rows, S_TOL, O_TOL
+from gpu_util import SCALE, Errors, bits_equal, check_o, check_pool, rel_fro_rows, S_TOL, S_TOL_BF16, O_TOL
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
-def test_decode_batch_full_size():
+@pytest.mark.parametrize("pool_dtype", ["float32", "bfloat16"])
+def test_decode_batch_full_size(pool_dtype):
+    """The full decode batch (B = 256, H = 32) on its 10,000-row pool, fp32 or
+    bf16 (the same values cut to bf16)."""
     w = workloads.decode_batch("cuda")
     call = w.calls[0]
-    pool = w.pool
+    pool = w.pool if pool_dtype == "float32" else (w.pool.view(torch.int32) >> 16).to(torch.int16).view(torch.bfloat16)
     ip, pi, lpl = (i32(t) for t in (call.page_indptr, call.page_indices, call.last_page_len))
     s = oracle.decode_slots(ip, pi, lpl, call.page_size)
     slots = gdn.gdn_paged_decode_slots(call.page_indptr, call.page_indices, call.last_page_len)
@@ -29,7 +32,8 @@ def test_decode_batch_full_size():
     rows = sorted(set(s["initial_state_indices"].tolist()) | set(s["output_state_indices"].tolist()))
     rows = [r for r in rows if r >= 0]
     remap = {r: i for i, r in enumerate(rows)}
-    local = pool[torch.tensor(rows, device="cuda")].cpu().numpy()
+    local = pool[torch.tensor(rows, device="cuda")].cpu()
+    local = local.view(torch.int16).numpy().view(np.uint16).copy() if pool_dtype == "bfloat16" else local.numpy()
     before = pool.clone()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     o = gdn.gdn_gated_delta_rule_decode_paged(call.q, call.k, call.v, call.g, call.beta, pool, call.page_indices,
@@ -43,14 +47,17 @@ def test_decode_batch_full_size():
     errs = Errors()
     check_o(o, o_ref, errs)
     wrows = [rows[i] for i in np.flatnonzero(written)]
-    got = pool[torch.tensor(wrows, device="cuda")].cpu().numpy()
-    e = rel_fro_rows(got, local[np.flatnonzero(written)])
+    got = pool[torch.tensor(wrows, device="cuda")].float().cpu().numpy()
+    ref = local[np.flatnonzero(written)]
+    if pool_dtype == "bfloat16":
+        ref = (ref.astype(np.uint32) << 16).view(np.float32)
+    e = rel_fro_rows(got, ref)
     errs.state = float(e.max())
-    assert e.max() <= S_TOL
+    assert e.max() <= (S_TOL_BF16 if pool_dtype == "bfloat16" else S_TOL)
     keep = torch.ones(pool.shape[0], dtype=torch.bool, device="cuda")
     keep[torch.tensor(wrows, device="cuda")] = False
     assert bits_equal(pool[keep], before[keep])
-    print("decode batch B=256 H=32: %r" % errs)
+    print("decode batch B=256 H=32 %s pool: %r" % (pool_dtype, errs))
 
 
 def _checkpoint_layout(prefix, lens, N):

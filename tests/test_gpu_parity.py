@@ -10,7 +10,8 @@ import gated_deltanet_paged_gb300 as gdn
 import oracle
 from gated_deltanet_paged_gb300 import workloads
 from conftest import bf16_bits, f32, i32
-from gpu_util import (SCALE, Errors, bits_equal, check_o, check_pool, decode_paged_both, prefill_paged_both)
+from gpu_util import (SCALE, Errors, bf16_pool_pair, bits_equal, check_o, check_pool, decode_paged_both,
+                      prefill_paged_both)
 
 pytestmark = pytest.mark.gpu
 
@@ -27,6 +28,38 @@ def test_tiny_workload(decay, use_slots):
         else:
             decode_paged_both(call, pool_gpu, pool_ora, errs, use_slots)
     print("tiny decay=%g slots=%s: %r" % (decay, use_slots, errs))
+
+
+@pytest.mark.parametrize("decay", [1.0, 0.01])
+def test_bf16_pool_tiny_workload(decay):
+    """The tiny workload (prefill from empty and non-empty prefixes, then
+    decode) on a bf16 state pool, through the paged prefill and decode calls."""
+    w = workloads.tiny("cpu", decay)
+    pool_gpu, pool_ora = bf16_pool_pair(w.pool)
+    pool_gpu = pool_gpu.cuda()
+    errs = Errors()
+    for call in w.calls:
+        if call.kind == "prefill":
+            prefill_paged_both(call, pool_gpu, pool_ora, errs)
+        else:
+            decode_paged_both(call, pool_gpu, pool_ora, errs, use_slots=True)
+    print("tiny decay=%g bf16 pool: %r" % (decay, errs))
+
+
+@pytest.mark.parametrize("decay", [1.0, 0.01])
+def test_bf16_pool_worked_example(decay):
+    """The worked 2500-token example on a bf16 pool: page 12 written, pages 7
+    and 3 bit-unchanged by the second call."""
+    w = workloads.worked_example("cpu", decay)
+    pool_gpu, pool_ora = bf16_pool_pair(w.pool)
+    pool_gpu = pool_gpu.cuda()
+    errs = Errors()
+    prefill_paged_both(w.calls[0], pool_gpu, pool_ora, errs)
+    kept = pool_gpu[[7, 3]].clone()
+    _, written = prefill_paged_both(w.calls[1], pool_gpu, pool_ora, errs)
+    assert np.flatnonzero(written).tolist() == [12]
+    assert bits_equal(pool_gpu[[7, 3]], kept)
+    print("worked example decay=%g bf16 pool: %r" % (decay, errs))
 
 
 @pytest.mark.parametrize("decay", [1.0, 0.01])
@@ -126,8 +159,10 @@ def test_split_prompt_matches_single_call_on_gpu():
     assert e.max().item() <= 1e-3
 
 
-def test_general_slot_api_minus_one_rows():
-    """Read row -1 = zero state; write and checkpoint rows of -1 are skipped."""
+@pytest.mark.parametrize("pool_dtype", ["float32", "bfloat16"])
+def test_general_slot_api_minus_one_rows(pool_dtype):
+    """Read row -1 = zero state; write and checkpoint rows of -1 are skipped
+    (fp32 and bf16 pools)."""
     H, N = 2, 64
     lens = [150, 90, 200]
     prefixes = [0, 30, 64]
@@ -146,7 +181,12 @@ def test_general_slot_api_minus_one_rows():
     cki[-1] = -1
     ck = workloads.sentinel_pool(sum(counts), H, "cpu")
     dev = lambda t: t.cuda()
-    pool_g, ck_g = pool.cuda(), ck.cuda()
+    if pool_dtype == "bfloat16":
+        (pool_g, pool_o), (ck_g, ck_o) = bf16_pool_pair(pool), bf16_pool_pair(ck)
+        pool_g, ck_g = pool_g.cuda(), ck_g.cuda()
+    else:
+        pool_g, ck_g = pool.cuda(), ck.cuda()
+        pool_o, ck_o = pool.numpy().copy(), ck.numpy().copy()
     pb, cb = pool_g.clone(), ck_g.clone()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     o = gdn.gdn_chunk_gated_delta_rule(dev(q), dev(k), dev(v), dev(g), dev(b), dev(cu), scale=SCALE,
@@ -156,7 +196,6 @@ def test_general_slot_api_minus_one_rows():
                                        prefix_lens=dev(P), checkpoint_every_n_tokens=N, err_word=err)
     torch.cuda.synchronize()
     assert err.item() == 0
-    pool_o, ck_o = pool.numpy().copy(), ck.numpy().copy()
     o_ref, w_out, w_ck = oracle.chunk_gated_delta_rule(
         bf16_bits(q), bf16_bits(k), bf16_bits(v), f32(g), f32(b), i32(cu), SCALE, initial_state=pool_o,
         state_indices=i32(si), output_state=pool_o, output_state_indices=i32(osi), state_checkpoints=ck_o,
