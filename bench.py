@@ -311,6 +311,26 @@ def _bench_decode(args, gdn, workloads, dev, stream, barrier, max_over_ranks, ra
                 statistics.mean(a.elapsed_time(b) for a, b in dev_ev), clk.summary())
 
     ms_decode, dkernel_ms, dclocks = timed(dpool)
+
+    # Copy-on-write forks of 256 pool rows (2 MB each) into rows no sequence
+    # uses: the row utility's bit-exact copy, HBM-bound.
+    used = set(dslots["initial_state_indices"].tolist()) | set(dslots["output_state_indices"].tolist())
+    free = [r for r in torch.randperm(dpool.shape[0], generator=torch.Generator().manual_seed(1240)).tolist()
+            if r not in used][:DECODE["B"]]
+    csrc = dslots["output_state_indices"].clone()
+    cdst = torch.tensor(free, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        gdn.gdn_pool_copy_rows(dpool, csrc, cdst)
+    cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+    torch.cuda.synchronize(dev)
+    for a_, b_ in cev:
+        a_.record(stream)
+        gdn.gdn_pool_copy_rows(dpool, csrc, cdst)
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    copy_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in cev)
+    copy_bytes = 2 * DECODE["B"] * H * STATE_BYTES
+    copy_ach = copy_bytes / (copy_ms * 1e-3) / 1e9
     decode_bytes = DECODE["B"] * H * DECODE_BYTES_PER_SEQ_HEAD
     ach = decode_bytes / (dkernel_ms * 1e-3) / 1e9
     dec = {"metric": "decode seq/s", "value": DECODE["B"] * world / (ms_decode * 1e-3), "unit": "seq/s",
@@ -319,7 +339,10 @@ def _bench_decode(args, gdn, workloads, dev, stream, barrier, max_over_ranks, ra
                        "25% open a page, 10,000-page pool (step = decode slots + decode)",
            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                         "algorithmic_bytes": decode_bytes},
-           "clocks": dclocks}
+           "clocks": dclocks,
+           "pool_copy_rows": {"rows": DECODE["B"], "bytes_per_call": copy_bytes, "kernel_ms": copy_ms,
+                              "roofline": {"bound": "hbm", "achieved": copy_ach, "peak": hbm, "unit": "GB/s",
+                                           "frac": copy_ach / hbm}}}
     # The same batch on a bf16 state pool (the fp32 pool's values cut to bf16):
     # half the state bytes, fp32 arithmetic on the chip.
     bpool = (dpool.view(torch.int32) >> 16).to(torch.int16).view(torch.bfloat16)
@@ -339,8 +362,8 @@ def _bench_decode(args, gdn, workloads, dev, stream, barrier, max_over_ranks, ra
                      "warmup": max(args.warmup, 3), "ms_per_step": ms_decode, "higher_is_better": True,
                      "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
                      "config": {"workload": dec["workload"]}, "roofline": dec["roofline"], "clocks": dec["clocks"],
-                     "bf16_state_pool": dec["bf16_state_pool"]})
-    return 4 * dsteps  # slots + decode, fp32 and bf16 pools
+                     "bf16_state_pool": dec["bf16_state_pool"], "pool_copy_rows": dec["pool_copy_rows"]})
+    return 4 * dsteps  # slots + decode, fp32 and bf16 pools (the row-copy timing is a side measurement)
 
 
 # ---------------------------------------------------------------------------

@@ -23,6 +23,8 @@ __all__ = [
     "gdn_chunk_gated_delta_rule",
     "gdn_chunk_gated_delta_rule_paged",
     "gdn_gated_delta_rule_decode_paged",
+    "gdn_pool_copy_rows",
+    "gdn_pool_zero_rows",
     "gdn_prefill_workspace_bytes",
     "gdn_status_string",
     "library",
@@ -80,6 +82,8 @@ def library():
                                                         P, i32, i32, P, P, i32, P, P, P, sz, P, P],
                 "gdn_gated_delta_rule_decode_paged_ex": [P, P, P, P, P, P, i32, i32, i32, i32, f32,
                                                          P, i32, i32, P, P, P, P, P, P],
+                "gdn_pool_copy_rows": [P, i64, i64, P, P, i32, i32, P, P],
+                "gdn_pool_zero_rows": [P, i64, i64, P, i32, i32, P, P],
             }
             for name, args in sig.items():
                 fn = getattr(lib, name)
@@ -303,3 +307,38 @@ def gdn_gated_delta_rule_decode_paged(q, k, v, g, beta, state_pool, page_indices
     else:
         _check("gdn_gated_delta_rule_decode_paged", library().gdn_gated_delta_rule_decode_paged(*head, *rest))
     return o
+
+
+def _pool_rows(pool, name):
+    if not pool.is_cuda or pool.dim() < 2:
+        raise ValueError("%s must be a CUDA tensor [rows, ...]" % name)
+    inner = pool[0]
+    if not inner.is_contiguous():
+        raise ValueError("%s rows must be contiguous" % name)
+    return inner.numel() * pool.element_size(), pool.stride(0) * pool.element_size()
+
+
+def gdn_pool_copy_rows(pool, src_rows, dst_rows, err_word=None):
+    """Bit-exact copies of whole pool rows: row dst_rows[i] <- row src_rows[i]
+    (-1 on either side skips).  Any element type; the pool is updated in place."""
+    i32 = torch.int32
+    _need(src_rows, i32, "src_rows", 1)
+    _need(dst_rows, i32, "dst_rows", 1)
+    if src_rows.numel() != dst_rows.numel():
+        raise ValueError("src_rows and dst_rows must have the same length")
+    row_bytes, stride_bytes = _pool_rows(pool, "pool")
+    _check("gdn_pool_copy_rows", library().gdn_pool_copy_rows(
+        _ptr(pool), row_bytes, stride_bytes, _ptr(src_rows), _ptr(dst_rows), dst_rows.numel(), pool.shape[0],
+        _ptr(_opt(err_word, i32, "err_word")), _stream(pool)))
+    return pool
+
+
+def gdn_pool_zero_rows(pool, rows, err_word=None):
+    """Whole pool rows set to zero bits (-1 skips); the pool is updated in place."""
+    i32 = torch.int32
+    _need(rows, i32, "rows", 1)
+    row_bytes, stride_bytes = _pool_rows(pool, "pool")
+    _check("gdn_pool_zero_rows", library().gdn_pool_zero_rows(
+        _ptr(pool), row_bytes, stride_bytes, _ptr(rows), rows.numel(), pool.shape[0],
+        _ptr(_opt(err_word, i32, "err_word")), _stream(pool)))
+    return pool

@@ -256,6 +256,33 @@ int gdn_gated_delta_rule_decode_paged_ex(const gdn_bf16 *q, const gdn_bf16 *k, c
                                          const gdn_decode_slots *slots, int32_t *err_word,
                                          void *stream);
 
+/* gdn_pool_copy_rows -- "gdn-prefix-cache", §The fix: a cached block's state
+ * is kept in that block's page and moved as bit-exact row copies (the
+ * request's row into the block after a step that ends on a block boundary,
+ * the block back into the request's row before a step that starts from a
+ * hit); on this library's pool the same move forks a shared page before a
+ * sequence writes it (copy-on-write).  For i < n, row dst_rows[i] of pool
+ * receives the row_bytes bytes of row src_rows[i], bit for bit (any element
+ * type: fp32 or bf16 states, NaN payloads kept); a -1 on either side skips the
+ * pair.  pool rows are pool_row_stride_bytes apart; row_bytes (a full row is
+ * H * V * K * element size) and the stride are multiples of 16, pool is
+ * 16-byte aligned, src_rows / dst_rows are int32 [n] on the device.  Rows
+ * outside [0, num_rows) are skipped and, with err_word, reported as
+ * GDN_DEVERR_PAGE_ID with the pair index.  Preconditions (unchecked): no row
+ * is the destination of two pairs, and no destination row is the source of
+ * another pair.  n <= 65535. */
+int gdn_pool_copy_rows(void *pool, int64_t row_bytes, int64_t pool_row_stride_bytes,
+                       const int32_t *src_rows, const int32_t *dst_rows, int32_t n, int32_t num_rows,
+                       int32_t *err_word, void *stream);
+
+/* gdn_pool_zero_rows -- "gdn-prefix-cache", §The fix: new blocks and rows are
+ * zeroed, so that no non-finite value outlives the step that produced it.
+ * For i < n, the row_bytes bytes of row rows[i] become zero bits (+0.0 in fp32
+ * and bf16: the zero state); -1 skips.  Same layout, checks and limits as
+ * gdn_pool_copy_rows. */
+int gdn_pool_zero_rows(void *pool, int64_t row_bytes, int64_t pool_row_stride_bytes, const int32_t *rows,
+                       int32_t n, int32_t num_rows, int32_t *err_word, void *stream);
+
 /* Bytes of device workspace a prefill call over num_seqs sequences,
  * total_tokens new tokens and H heads needs (0 for invalid arguments).  The
  * prefill runs in two phases: a chunk-local phase computes, for every 64-token

@@ -223,3 +223,24 @@ def gated_delta_rule_decode_paged(q, k, v, g, beta, state_pool, page_indices, pa
     s = decode_slots(page_indptr, page_indices, last_page_len, page_size)
     return gated_delta_rule_decode(q, k, v, g, beta, state_pool, s["initial_state_indices"],
                                    s["output_state_indices"], scale, chains=chains)
+
+
+def pool_copy_rows(pool, src_rows, dst_rows):
+    """Row copies by their definition ("gdn-prefix-cache", §The fix: states
+    moved between rows as bit-exact copies): for each pair in order, row dst
+    takes the bytes of row src; -1 on either side, or a row outside the pool,
+    skips the pair.  pool: any numpy array [rows, ...], updated in place."""
+    n = pool.shape[0]
+    for s_, d in zip(np.asarray(src_rows).tolist(), np.asarray(dst_rows).tolist()):
+        if 0 <= s_ < n and 0 <= d < n:
+            pool[d] = pool[s_]
+    return pool
+
+
+def pool_zero_rows(pool, rows):
+    """Rows set to zero bits (the zero state); -1 or out-of-range rows skip."""
+    n = pool.shape[0]
+    for r in np.asarray(rows).tolist():
+        if 0 <= r < n:
+            pool[r] = 0
+    return pool

@@ -116,3 +116,19 @@ def test_binding_has_no_fallback_without_gpu():
     t = torch.zeros(4, dtype=torch.int32)
     with pytest.raises((ValueError, RuntimeError)):
         gdn.gdn_paged_decode_slots(t, t, t)
+
+
+def test_pool_row_calls_reject_bad_arguments():
+    """Host-side checks of the row utilities (no device work is queued)."""
+    lib = gdn.library()
+    fake = ctypes.c_void_p(16)  # never dereferenced: every case below fails a host check first
+    rows = ctypes.c_void_p(32)
+    row = 32 * 128 * 128 * 4
+    assert lib.gdn_pool_copy_rows(fake, row + 8, row + 16, rows, rows, 1, 4, None, None) == -1  # row bytes % 16
+    assert lib.gdn_pool_copy_rows(fake, row, row - 16, rows, rows, 1, 4, None, None) == -1      # stride < row
+    assert lib.gdn_pool_copy_rows(fake, row, row, None, rows, 1, 4, None, None) == -1           # no sources
+    assert lib.gdn_pool_copy_rows(None, row, row, rows, rows, 1, 4, None, None) == -1           # no pool
+    assert lib.gdn_pool_copy_rows(ctypes.c_void_p(24), row, row, rows, rows, 1, 4, None, None) == -1  # misaligned
+    assert lib.gdn_pool_zero_rows(fake, row, row, rows, -1, 4, None, None) == -1                 # n < 0
+    assert lib.gdn_pool_zero_rows(fake, row, row, rows, 1, 0, None, None) == -1                  # no rows in pool
+    assert lib.gdn_pool_zero_rows(fake, row, row, rows, 0, 4, None, None) == 0                   # nothing to do

@@ -560,3 +560,19 @@ def test_bf16_pool_stores_the_nearest_value():
                                       output_state_indices=[0])
         assert (bf_pool[0, 0, :, 5] == want).all()
         assert (np.delete(bf_pool[0, 0], 5, axis=1) == 0).all()
+
+
+def test_row_copies_keep_every_bit():
+    """The row utilities' reference is their definition: rows move whole and bit
+    for bit (NaN payloads, -0.0 and bf16 bit patterns included), -1 skips, a row
+    outside the pool skips, and pairs run in order."""
+    pool = np.arange(6 * 8, dtype=np.uint32).reshape(6, 8) | np.uint32(0x7FC00000)
+    pool[1, 0] = np.float32(-0.0).view(np.uint32)
+    before = pool.copy()
+    oracle.pool_copy_rows(pool, [1, -1, 2, 9], [4, 3, 5, 0])
+    assert (pool[4] == before[1]).all() and (pool[5] == before[2]).all()
+    assert (pool[[0, 1, 2, 3]] == before[[0, 1, 2, 3]]).all()
+    bf = np.arange(4 * 4, dtype=np.uint16).reshape(4, 4) | np.uint16(0x7F80)
+    bref = bf.copy()
+    oracle.pool_zero_rows(bf, [2, -1, 7])
+    assert (bf[2] == 0).all() and (bf[[0, 1, 3]] == bref[[0, 1, 3]]).all()
