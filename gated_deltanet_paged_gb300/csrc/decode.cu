@@ -5,12 +5,13 @@
 // pool: carried in fp32 and rounded to the nearest bf16 on the way out) is read
 // once from its read row, updated and written once to its write row:
 //     S' = e S + beta (v - e S k) k^T,   o = scale S' q = scale (e S q + d (k.q))
-// with e = exp(g) and d = beta (v - e S k) per state row.  The kernel is a
-// streaming read-update-write bound by HBM bandwidth: each warp owns 16 rows,
-// each lane one float4 of every row (16-byte coalesced, evict-first loads and
-// streaming stores, all 16 loads in flight before any arithmetic); the 32 dot
-// products a warp needs (S k and S q of its 16 rows) are reduced together by
-// a transpose reduction (31 shuffles instead of 160).
+// with e = exp(g) and d = beta (v - e S k) per state row.  Both kernels are a
+// streaming read-update-write bound by HBM bandwidth: 16-byte coalesced,
+// evict-first loads and streaming stores, all 16 loads of a thread in flight
+// before any arithmetic.  In the fp32 kernel each warp owns 16 rows, each
+// lane one float4 of every row; the 32 dot products a warp needs (S k and S q
+// of its 16 rows) are reduced together by a transpose reduction (31 shuffles
+// instead of 160).  The bf16 kernel is laid out below.
 #include <math.h>
 
 #include "common.cuh"
@@ -28,7 +29,7 @@ struct DecodeArgs {
   const float* g;
   const float* beta;
   __nv_bfloat16* o;
-  void* pool;  // float or __nv_bfloat16 elements (the kernel's template argument)
+  void* pool;  // float (decode_f32_kernel) or __nv_bfloat16 (decode_bf16_kernel) elements
   int64_t row_stride;
   int32_t H;
   int32_t num_pages;
@@ -66,25 +67,9 @@ __device__ __forceinline__ void bf16x4(const __nv_bfloat16* p, float (&f)[4]) {
   f[3] = b.y;
 }
 
-// Four consecutive state values of one row: 16 bytes of fp32 or 8 of bf16.
-__device__ __forceinline__ float4 load4(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
-__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
-  const uint2 u = __ldcs(reinterpret_cast<const uint2*>(p));
-  const float2 a = gdn::unpack_bf162(u.x), b = gdn::unpack_bf162(u.y);
-  return make_float4(a.x, a.y, b.x, b.y);
-}
-__device__ __forceinline__ void store4(float* p, float4 x) { __stcs(reinterpret_cast<float4*>(p), x); }
-__device__ __forceinline__ void store4(__nv_bfloat16* p, float4 x) {
-  __stcs(reinterpret_cast<uint2*>(p), make_uint2(gdn::pack_bf162(x.x, x.y), gdn::pack_bf162(x.z, x.w)));
-}
-
-template <typename St>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a) {
-  const int bh = blockIdx.x;
-  const int b = bh / a.H, h = bh % a.H;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  int in_row, out_row;
+// The rows a (sequence b) reads and writes, from the explicit slots or the
+// page table: false when the CTA has nothing to do (a bad entry, recorded).
+__device__ __forceinline__ bool resolve_rows(const DecodeArgs& a, int b, int& in_row, int& out_row) {
   bool bad = false;
   int kind = 0;
   if (a.in_rows) {
@@ -95,7 +80,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
     const int32_t lpl = a.last_len[b];
     if (i1 - i0 < 1) {
       if (threadIdx.x == 0) gdn::record_error(a.err_word, GDN_DEVERR_PAGE_TABLE, b);
-      return;
+      return false;
     }
     out_row = a.pages[i1 - 1];
     in_row = (lpl == 1) ? (i1 - i0 >= 2 ? a.pages[i1 - 2] : -1) : out_row;
@@ -108,18 +93,28 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
     bad = true, kind = GDN_DEVERR_PAGE_ID;
   if (bad) {
     if (threadIdx.x == 0) gdn::record_error(a.err_word, kind, b);
-    return;
+    return false;
   }
+  return true;
+}
+
+// fp32 pool: 8 warps x 16 rows, each lane one float4 of every row.
+__global__ void __launch_bounds__(kThreads, 2) decode_f32_kernel(const DecodeArgs a) {
+  const int bh = blockIdx.x;
+  const int b = bh / a.H, h = bh % a.H;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int in_row, out_row;
+  if (!resolve_rows(a, b, in_row, out_row)) return;
 
   const int r0 = warp * kRowsPerWarp;
   const int64_t head_off = static_cast<int64_t>(h) * gdn::kDimV * gdn::kDimK;
 
-  St* const pool = static_cast<St*>(a.pool);
+  float* const pool = static_cast<float*>(a.pool);
   float4 s[kRowsPerWarp];
   if (in_row >= 0) {
-    const St* src = pool + in_row * a.row_stride + head_off + r0 * gdn::kDimK + 4 * lane;
+    const float* src = pool + in_row * a.row_stride + head_off + r0 * gdn::kDimK + 4 * lane;
 #pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) s[i] = load4(src + i * gdn::kDimK);
+    for (int i = 0; i < kRowsPerWarp; ++i) s[i] = __ldcs(reinterpret_cast<const float4*>(src + i * gdn::kDimK));
   } else {
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -150,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
         __float2bfloat16_rn(a.scale * (e * red + d_row * kq));
 
   if (out_row >= 0) {
-    St* dst = pool + out_row * a.row_stride + head_off + r0 * gdn::kDimK + 4 * lane;
+    float* dst = pool + out_row * a.row_stride + head_off + r0 * gdn::kDimK + 4 * lane;
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
       const float di = __shfl_sync(0xffffffffu, d, 2 * i);
@@ -159,7 +154,121 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeArgs a)
       n.y = e * s[i].y + di * kk[1];
       n.z = e * s[i].z + di * kk[2];
       n.w = e * s[i].w + di * kk[3];
-      store4(dst + i * gdn::kDimK, n);
+      __stcs(reinterpret_cast<float4*>(dst + i * gdn::kDimK), n);
+    }
+  }
+}
+
+// bf16 pool.  A 256-byte bf16 row is half a warp of 16-byte loads, so a warp
+// takes two rows per load: lane l (p = l & 15, half c = l >> 4) holds
+// elements 8p..8p+7 of rows 2i+c, i < 16, 32 rows per warp and four warps per
+// state.  16 loads of 16 bytes in flight per thread (three CTAs per SM); the
+// values stay packed in registers and are widened to fp32 where they are used.
+// A thread has twice the fp32 arithmetic of the fp32 kernel's for the same
+// bytes, enough to show against HBM, so the products and sums run as paired
+// fp32 operations (fma.rn.f32x2, each half rounded like a scalar fma).
+constexpr int kBf16Threads = 128;
+constexpr int kBf16RowsPerWarp = 32;
+static_assert(kBf16Threads / 32 * kBf16RowsPerWarp == gdn::kDimV, "one CTA covers one 128-row state");
+
+__device__ __forceinline__ void widen8(const uint4& u, float2 (&f)[4]) {
+  f[0] = gdn::unpack_bf162(u.x), f[1] = gdn::unpack_bf162(u.y);
+  f[2] = gdn::unpack_bf162(u.z), f[3] = gdn::unpack_bf162(u.w);
+}
+
+__device__ __forceinline__ float dot8(const float2 (&x)[4], const float2 (&w)[4]) {
+  float2 r = __fmul2_rn(x[0], w[0]);
+#pragma unroll
+  for (int j = 1; j < 4; ++j) r = __ffma2_rn(x[j], w[j], r);
+  return r.x + r.y;
+}
+
+__global__ void __launch_bounds__(kBf16Threads, 3) decode_bf16_kernel(const DecodeArgs a) {
+  const int bh = blockIdx.x;
+  const int b = bh / a.H, h = bh % a.H;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int p = lane & 15, c = lane >> 4;
+  int in_row, out_row;
+  if (!resolve_rows(a, b, in_row, out_row)) return;
+
+  const int r0 = warp * kBf16RowsPerWarp;
+  // this lane's piece of row r0 + 2i + c is at lane_off + i * 2 rows
+  const int64_t lane_off = static_cast<int64_t>(h) * gdn::kDimV * gdn::kDimK + (r0 + c) * gdn::kDimK + 8 * p;
+
+  __nv_bfloat16* const pool = static_cast<__nv_bfloat16*>(a.pool);
+  uint4 s[16];
+  if (in_row >= 0) {
+    const __nv_bfloat16* src = pool + in_row * a.row_stride + lane_off;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s[i] = __ldcs(reinterpret_cast<const uint4*>(src + i * 2 * gdn::kDimK));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+
+  float2 kk[4], qq[4];
+  widen8(*reinterpret_cast<const uint4*>(a.k + static_cast<int64_t>(bh) * gdn::kDimK + 8 * p), kk);
+  widen8(*reinterpret_cast<const uint4*>(a.q + static_cast<int64_t>(bh) * gdn::kDimK + 8 * p), qq);
+  float kq = dot8(kk, qq);
+#pragma unroll
+  for (int m = 8; m >= 1; m >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, m);  // both halves hold all of k, q
+  const int row = r0 + 2 * p + c;  // the row this lane finishes
+  const float e = expf(a.g[bh]);
+  const float be = a.beta[bh];
+  const float myv = __bfloat162float(a.v[static_cast<int64_t>(bh) * gdn::kDimV + row]);
+
+  // 32 partial dot products per lane, value 2i = (S k) and 2i+1 = (S q) of
+  // load i, summed over the 16 lanes of each half by a transpose reduction
+  // (lane bit 3 pairs value bit 4, ..., lane bit 0 pairs value bit 1).  The
+  // first step is taken as the values are formed, so that 16 are live at once.
+  float x[16];
+  {
+    const bool upper = (lane & 8) != 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // loads j and 8 + j: values 2j, 2j + 1 and 2j + 16, 2j + 17
+      float2 lo[4], hi[4];
+      widen8(s[j], lo);
+      widen8(s[8 + j], hi);
+      const float k0 = dot8(lo, kk), k1 = dot8(hi, kk), q0 = dot8(lo, qq), q1 = dot8(hi, qq);
+      x[2 * j] = (upper ? k1 : k0) + __shfl_xor_sync(0xffffffffu, upper ? k0 : k1, 8);
+      x[2 * j + 1] = (upper ? q1 : q0) + __shfl_xor_sync(0xffffffffu, upper ? q0 : q1, 8);
+    }
+  }
+#pragma unroll
+  for (int m = 4; m >= 1; m >>= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 2 * m; ++i) {
+      const float send = upper ? x[i] : x[i + 2 * m];
+      const float keep = upper ? x[i + 2 * m] : x[i];
+      x[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+  // x[0] = (S k), x[1] = (S q) of load p in this half, i.e. of row r0 + 2p + c
+  const float d = be * (myv - e * x[0]);
+  a.o[static_cast<int64_t>(bh) * gdn::kDimV + row] = __float2bfloat16_rn(a.scale * (e * x[1] + d * kq));
+
+  if (out_row >= 0) {
+    // An empty asm on the packed values makes the compiler widen them again
+    // here instead of keeping all 128 widened values live from the dot products.
+#pragma unroll
+    for (int i = 0; i < 16; ++i) asm("" : "+r"(s[i].x), "+r"(s[i].y), "+r"(s[i].z), "+r"(s[i].w));
+    __nv_bfloat16* dst = pool + out_row * a.row_stride + lane_off;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float di = __shfl_sync(0xffffffffu, d, (lane & 16) | i);
+      float2 f[4];
+      widen8(s[i], f);
+      const float2 e2 = make_float2(e, e), d2 = make_float2(di, di);
+      float2 n[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) n[j] = __ffma2_rn(e2, f[j], __fmul2_rn(d2, kk[j]));
+      uint4 u;
+      u.x = gdn::pack_bf162(n[0].x, n[0].y);  // nearest bf16, ties to even
+      u.y = gdn::pack_bf162(n[1].x, n[1].y);
+      u.z = gdn::pack_bf162(n[2].x, n[2].y);
+      u.w = gdn::pack_bf162(n[3].x, n[3].y);
+      __stcs(reinterpret_cast<uint4*>(dst + i * 2 * gdn::kDimK), u);
     }
   }
 }
@@ -212,9 +321,9 @@ extern "C" int gdn_gated_delta_rule_decode_paged_ex(const gdn_bf16* q, const gdn
   a.err_word = err_word;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (state_dtype == GDN_STATE_BF16)
-    decode_kernel<__nv_bfloat16><<<batch * H, kThreads, 0, st>>>(a);
+    decode_bf16_kernel<<<batch * H, kBf16Threads, 0, st>>>(a);
   else
-    decode_kernel<float><<<batch * H, kThreads, 0, st>>>(a);
+    decode_f32_kernel<<<batch * H, kThreads, 0, st>>>(a);
   return gdn_host::launch_status();
 }
 
