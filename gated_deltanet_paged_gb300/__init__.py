@@ -77,7 +77,7 @@ def library():
                 "gdn_gated_delta_rule_decode_paged": [P, P, P, P, P, P, i32, i32, i32, i32, f32,
                                                       P, i32, P, P, P, P, P, P],
                 "gdn_chunk_gated_delta_rule_ex": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32,
-                                                  P, P, P, P, P, P, P, P, i32, i64, i32, P, sz, P, P],
+                                                  P, P, P, P, P, P, P, P, i32, i64, i32, i32, P, sz, P, P],
                 "gdn_chunk_gated_delta_rule_paged_ex": [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32,
                                                         P, i32, i32, P, P, i32, P, P, P, sz, P, P],
                 "gdn_gated_delta_rule_decode_paged_ex": [P, P, P, P, P, P, i32, i32, i32, i32, f32,
@@ -141,6 +141,35 @@ def _state_dtype(pools, names):
     if kind not in _STATE_DTYPES:
         raise TypeError("state pools must be float32 or bfloat16, got %s" % kind)
     return _STATE_DTYPES[kind]
+
+
+# Slot-array element types (GDN_INDEX_I32 / GDN_INDEX_I64 of the C header).
+_INDEX_DTYPES = {torch.int32: 0, torch.int64: 1}
+
+
+def _index_dtype(arrays, names):
+    """The slot arrays' common element type code; int32 or int64, all alike."""
+    kinds = {t.dtype for t in arrays if t is not None}
+    if len(kinds) > 1:
+        raise TypeError("%s must share one dtype" % ", ".join(names))
+    kind = kinds.pop() if kinds else torch.int32
+    if kind not in _INDEX_DTYPES:
+        raise TypeError("slot arrays must be int32 or int64, got %s" % kind)
+    return _INDEX_DTYPES[kind]
+
+
+def _pool_arg(t, dtype, name):
+    """A state pool [rows, H, V, K] whose rows are dense; the row stride
+    (stride(0)) may be padded."""
+    if t is None:
+        return None
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dim() != 4 or not t[0].is_contiguous() or t.stride(0) < t[0].numel():
+        raise ValueError("%s must be [rows, H, V, K] with dense rows" % name)
+    return t
 
 
 def gdn_status_string(status: int) -> str:
@@ -217,33 +246,37 @@ def gdn_chunk_gated_delta_rule(q, k, v, g, beta, cu_seqlens, *, scale=0.0, initi
                                checkpoint_cu_starts=None, prefix_lens=None, checkpoint_every_n_tokens=0,
                                o=None, err_word=None, workspace=None):
     """Chunked prefill with slot arguments (explicit read / final / checkpoint
-    rows).  Returns o (bf16 [T, H, V]); pools are updated in place.
+    rows).  Returns o (bf16 [T, H, V]); pools are updated in place.  The slot
+    arrays are int32 or int64 (all alike); the pools fp32 or bf16 (all alike)
+    [rows, H, V, K] with dense rows and one row stride, which may be padded.
     ``workspace``: optional uint8 device tensor of at least
     gdn_prefill_workspace_bytes(num_seqs, T, H) bytes."""
     T, H, K, V = _tokens(q, k, v, g, beta)
     _need(cu_seqlens, torch.int32, "cu_seqlens")
-    i32 = torch.int32
     pool_names = ("initial_state", "output_state", "state_checkpoints")
     sd = _state_dtype((initial_state, output_state, state_checkpoints), pool_names)
     pdt = torch.bfloat16 if sd else torch.float32
-    pools = [_opt(p, pdt, n) for p, n in zip((initial_state, output_state, state_checkpoints), pool_names)]
-    stride = 0
-    for p in pools:
-        if p is not None:
-            stride = p.stride(0)
+    pools = [_pool_arg(p, pdt, n) for p, n in zip((initial_state, output_state, state_checkpoints), pool_names)]
+    strides = {p.stride(0) for p in pools if p is not None}
+    if len(strides) > 1:
+        raise ValueError("%s must share one row stride" % ", ".join(pool_names))
+    stride = strides.pop() if strides else 0
+    idx_names = ("state_indices", "output_state_indices", "checkpoint_state_indices", "checkpoint_cu_starts",
+                 "prefix_lens")
+    idx = (state_indices, output_state_indices, checkpoint_state_indices, checkpoint_cu_starts, prefix_lens)
+    xd = _index_dtype(idx, idx_names)
+    idt = torch.int64 if xd else torch.int32
+    idx = [_opt(t, idt, n) for t, n in zip(idx, idx_names)]
     if o is None:
         o = torch.empty(T, H, V, dtype=torch.bfloat16, device=q.device)
     _need(o, torch.bfloat16, "o", 3)
     ws = _workspace(workspace, cu_seqlens.numel() - 1, T, H, q.device)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(o), _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, H,
-            K, V, float(scale), _ptr(pools[0]), _ptr(_opt(state_indices, i32, "state_indices")), _ptr(pools[1]),
-            _ptr(_opt(output_state_indices, i32, "output_state_indices")), _ptr(pools[2]),
-            _ptr(_opt(checkpoint_state_indices, i32, "checkpoint_state_indices")),
-            _ptr(_opt(checkpoint_cu_starts, i32, "checkpoint_cu_starts")), _ptr(_opt(prefix_lens, i32, "prefix_lens")),
-            int(checkpoint_every_n_tokens), stride)
-    tail = (_ptr(ws), ws.numel(), _ptr(_opt(err_word, i32, "err_word")), _stream(q))
-    if sd:
-        _check("gdn_chunk_gated_delta_rule_ex", library().gdn_chunk_gated_delta_rule_ex(*args, sd, *tail))
+            K, V, float(scale), _ptr(pools[0]), _ptr(idx[0]), _ptr(pools[1]), _ptr(idx[1]), _ptr(pools[2]),
+            _ptr(idx[2]), _ptr(idx[3]), _ptr(idx[4]), int(checkpoint_every_n_tokens), stride)
+    tail = (_ptr(ws), ws.numel(), _ptr(_opt(err_word, torch.int32, "err_word")), _stream(q))
+    if sd or xd:
+        _check("gdn_chunk_gated_delta_rule_ex", library().gdn_chunk_gated_delta_rule_ex(*args, sd, xd, *tail))
     else:
         _check("gdn_chunk_gated_delta_rule", library().gdn_chunk_gated_delta_rule(*args, *tail))
     return o

@@ -170,7 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- rows of this sequence ----
   int P, in_row, out_row;
-  const int32_t* ck_rows = nullptr;  // j-th checkpoint row = ck_rows[j]
+  const void* ck_rows = nullptr;  // j-th checkpoint row = index_at(ck_rows, ck_off + j, ck_wide)
+  int64_t ck_off = 0;
+  int32_t ck_wide = 0;
   int N = a.N;
   if (a.indptr) {
     const int i0 = a.indptr[b], i1 = a.indptr[b + 1];
@@ -184,7 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     P = static_cast<int>(tot - L);
     in_row = P > 0 ? a.pages[i0 + (P - 1) / a.page_size] : -1;
     out_row = a.pages[i1 - 1];
-    ck_rows = a.pages + i0 + P / a.page_size;
+    ck_rows = a.pages;
+    ck_off = i0 + P / a.page_size;
     N = a.page_size;
     if (a.err_word) {
       if (tid == 0) {
@@ -200,14 +203,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (sh.flag) return;
     }
   } else {
-    P = a.prefix_lens ? a.prefix_lens[b] : 0;
-    in_row = a.state_indices ? a.state_indices[b] : -1;
-    out_row = a.output_state_indices ? a.output_state_indices[b] : -1;
-    if (a.state_checkpoints) ck_rows = a.checkpoint_state_indices + a.checkpoint_cu_starts[b];
-    if (P < 0 || static_cast<long long>(P) + L > 0x3FFFFFFFLL) {
+    const int64_t p64 = a.prefix_lens ? index_at(a.prefix_lens, b, a.index64) : 0;
+    const int64_t in64 = a.state_indices ? index_at(a.state_indices, b, a.index64) : -1;
+    const int64_t out64 = a.output_state_indices ? index_at(a.output_state_indices, b, a.index64) : -1;
+    if (a.state_checkpoints) {
+      ck_rows = a.checkpoint_state_indices;
+      ck_off = index_at(a.checkpoint_cu_starts, b, a.index64);
+      ck_wide = a.index64;
+    }
+    if (p64 < 0 || p64 + L > 0x3FFFFFFFLL) {
       if (tid == 0) record_error(a.err_word, GDN_DEVERR_PAGE_TABLE, b);
       return;
     }
+    P = static_cast<int>(p64);
+    if (a.index64) {
+      // int64 slot entries: every row this sequence uses, and its first
+      // checkpoint entry, must lie in the int32 range (rows >= -1).
+      if (tid == 0) {
+        constexpr int64_t kMax = 0x7FFFFFFFLL;
+        int bad = in64 < -1 || in64 > kMax || out64 < -1 || out64 > kMax;
+        if (ck_rows && a.N > 0) {
+          const int64_t nck = (p64 + L) / a.N - p64 / a.N;
+          bad |= ck_off < 0 || ck_off > kMax;
+          for (int64_t j = 0; j < nck && !bad; ++j) {
+            const int64_t r = index_at(ck_rows, ck_off + j, 1);
+            bad |= r < -1 || r > kMax;
+          }
+        }
+        sh.flag = bad;
+        if (bad) record_error(a.err_word, GDN_DEVERR_INDEX_RANGE, b);
+      }
+      __syncthreads();
+      if (sh.flag) return;
+    }
+    in_row = static_cast<int>(in64);
+    out_row = static_cast<int>(out64);
   }
   if (static_cast<long long>(cu_b) + L > a.T || cu_b < 0) {
     if (tid == 0) record_error(a.err_word, GDN_DEVERR_PAGE_TABLE, b);
@@ -715,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid == 0 && c + 2 < nch) tma_k(c + 2);  // U^T K~ of chunk c has read its K slot
       const int a_end = chunk_a0(c) + kChunk;
       if (ck_rows && ck_pool && a_end % N == 0 && a_end <= end_pos) {
-        const int row = ck_rows[a_end / N - 1 - first_ck];
+        const int row = static_cast<int>(index_at(ck_rows, ck_off + a_end / N - 1 - first_ck, ck_wide));
         if (row >= 0) store_state(ck_pool, row);
       }
       // Outputs of chunk c (columns of O^T).  In a full chunk each warp reads its
@@ -867,16 +897,21 @@ extern "C" int gdn_chunk_gated_delta_rule_ex(const gdn_bf16* q, const gdn_bf16* 
                                              const float* g, const float* beta, gdn_bf16* o,
                                              const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens,
                                              int32_t H, int32_t K, int32_t V, float scale, const void* initial_state,
-                                             const int32_t* state_indices, void* output_state,
-                                             const int32_t* output_state_indices, void* state_checkpoints,
-                                             const int32_t* checkpoint_state_indices,
-                                             const int32_t* checkpoint_cu_starts, const int32_t* prefix_lens,
-                                             int32_t checkpoint_every_n_tokens, int64_t pool_row_stride,
-                                             int32_t state_dtype, void* workspace, size_t workspace_bytes,
-                                             int32_t* err_word, void* stream) {
+                                             const void* state_indices, void* output_state,
+                                             const void* output_state_indices, void* state_checkpoints,
+                                             const void* checkpoint_state_indices, const void* checkpoint_cu_starts,
+                                             const void* prefix_lens, int32_t checkpoint_every_n_tokens,
+                                             int64_t pool_row_stride, int32_t state_dtype, int32_t index_dtype,
+                                             void* workspace, size_t workspace_bytes, int32_t* err_word,
+                                             void* stream) {
   int rc = check_common(q, k, v, g, beta, o, cu_seqlens, num_seqs, total_tokens, H, K, V);
   if (rc != GDN_OK) return rc;
   if (state_dtype != GDN_STATE_F32 && state_dtype != GDN_STATE_BF16) return GDN_ERR_INVALID_ARGUMENT;
+  if (index_dtype != GDN_INDEX_I32 && index_dtype != GDN_INDEX_I64) return GDN_ERR_INVALID_ARGUMENT;
+  const uintptr_t index_align = index_dtype == GDN_INDEX_I64 ? 8 : 4;
+  for (const void* p : {state_indices, output_state_indices, checkpoint_state_indices, checkpoint_cu_starts,
+                        prefix_lens})
+    if (reinterpret_cast<uintptr_t>(p) % index_align != 0) return GDN_ERR_INVALID_ARGUMENT;
   if ((state_indices != nullptr) != (initial_state != nullptr)) return GDN_ERR_INVALID_ARGUMENT;
   if ((output_state_indices != nullptr) != (output_state != nullptr)) return GDN_ERR_INVALID_ARGUMENT;
   const int nck = (state_checkpoints != nullptr) + (checkpoint_state_indices != nullptr) +
@@ -905,6 +940,7 @@ extern "C" int gdn_chunk_gated_delta_rule_ex(const gdn_bf16* q, const gdn_bf16* 
   a.checkpoint_state_indices = checkpoint_state_indices;
   a.checkpoint_cu_starts = checkpoint_cu_starts;
   a.prefix_lens = prefix_lens;
+  a.index64 = index_dtype == GDN_INDEX_I64;
   a.N = nck ? checkpoint_every_n_tokens : 0;
   a.row_stride = any_pool ? pool_row_stride : 0;
   a.state_bf16 = state_dtype == GDN_STATE_BF16;
@@ -924,7 +960,8 @@ extern "C" int gdn_chunk_gated_delta_rule(const gdn_bf16* q, const gdn_bf16* k, 
   return gdn_chunk_gated_delta_rule_ex(q, k, v, g, beta, o, cu_seqlens, num_seqs, total_tokens, H, K, V, scale,
                                        initial_state, state_indices, output_state, output_state_indices,
                                        state_checkpoints, checkpoint_state_indices, checkpoint_cu_starts, prefix_lens,
-                                       checkpoint_every_n_tokens, pool_row_stride, GDN_STATE_F32, workspace,
+                                       checkpoint_every_n_tokens, pool_row_stride, GDN_STATE_F32, GDN_INDEX_I32,
+                                       workspace,
                                        workspace_bytes, err_word, stream);
 }
 

@@ -22,13 +22,15 @@ struct PrefillArgs {
   int32_t H;
   float scale;
   const float* initial_state;
-  const int32_t* state_indices;
+  // The slot arrays: int32, or int64 when index64 is set (index_at reads both).
+  const void* state_indices;
   float* output_state;
-  const int32_t* output_state_indices;
+  const void* output_state_indices;
   float* state_checkpoints;
-  const int32_t* checkpoint_state_indices;
-  const int32_t* checkpoint_cu_starts;
-  const int32_t* prefix_lens;
+  const void* checkpoint_state_indices;
+  const void* checkpoint_cu_starts;
+  const void* prefix_lens;
+  int32_t index64;
   int32_t N;
   int64_t row_stride;  // elements of the pools' type
   int32_t state_bf16;  // pools of bf16 (states widened on load, rounded to nearest on store), else fp32
@@ -69,6 +71,11 @@ __host__ __device__ inline size_t workspace_bytes(int64_t T, int64_t num_seqs, i
   return workspace_map_bytes(ns) + static_cast<size_t>(ns) * H * (kTinvBytes + kWBytes);
 }
 
+// Entry i of a slot array of int32 (wide == 0) or int64 elements.
+__device__ inline int64_t index_at(const void* p, int64_t i, int32_t wide) {
+  return wide ? static_cast<const int64_t*>(p)[i] : static_cast<int64_t>(static_cast<const int32_t*>(p)[i]);
+}
+
 // Prefix length P, start cu_b and new length L of sequence b.  Returns false
 // for a zero-length sequence or arguments no kernel may act on (the chain
 // kernel reports those in err_word).
@@ -83,8 +90,9 @@ __device__ inline bool seq_extent(const PrefillArgs& a, int b, int& cu_b, int& L
     if (n < 1 || lpl < 1 || lpl > a.page_size || tot < L || tot > 0x3FFFFFFFLL) return false;
     P = static_cast<int>(tot - L);
   } else {
-    P = a.prefix_lens ? a.prefix_lens[b] : 0;
-    if (P < 0 || static_cast<long long>(P) + L > 0x3FFFFFFFLL) return false;
+    const int64_t p64 = a.prefix_lens ? index_at(a.prefix_lens, b, a.index64) : 0;
+    if (p64 < 0 || p64 + L > 0x3FFFFFFFLL) return false;
+    P = static_cast<int>(p64);
   }
   return true;
 }

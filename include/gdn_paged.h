@@ -70,9 +70,16 @@ typedef uint16_t gdn_bf16; /* raw bfloat16 bit pattern */
 #define GDN_STATE_F32 0
 #define GDN_STATE_BF16 1
 
+/* Element type of the slot arrays of gdn_chunk_gated_delta_rule_ex
+ * ("Slot arguments of chunk_gated_delta_rule": each is an int32 or int64
+ * tensor). */
+#define GDN_INDEX_I32 0
+#define GDN_INDEX_I64 1
+
 #define GDN_DEVERR_PAGE_ID 1       /* a page id outside [0, num_pages) */
 #define GDN_DEVERR_PAGE_TABLE 2    /* no page, last_page_len outside 1..page_size, more new tokens than tokens, or tokens past total_tokens */
 #define GDN_DEVERR_NO_PREV_TOKEN 3 /* decode: the decoded token is the sequence's first */
+#define GDN_DEVERR_INDEX_RANGE 4   /* an int64 slot entry outside the int32 range (rows below -1) */
 #define GDN_DEVERR_TIMEOUT 15      /* an internal wait ran past its iteration limit */
 
 /* Per-sequence pool rows of a paged prefill batch, each int32 [num_seqs] on
@@ -225,18 +232,26 @@ int gdn_gated_delta_rule_decode_paged(const gdn_bf16 *q, const gdn_bf16 *k, cons
  * GDN_ERR_INVALID_ARGUMENT).  Pools are passed untyped; every pool of one call
  * has that element type.  For bf16 pools pool_row_stride (elements) must be a
  * multiple of 8, so rows stay 16-byte aligned.  The fp32 calls above are these
- * with GDN_STATE_F32. */
+ * with GDN_STATE_F32.
+ * The general call also takes the element type of its five slot arrays
+ * (state_indices, output_state_indices, checkpoint_state_indices,
+ * checkpoint_cu_starts, prefix_lens: all GDN_INDEX_I32 or all GDN_INDEX_I64,
+ * each aligned to its element size; cu_seqlens stays int32).  With int64
+ * entries a sequence whose read, final or checkpoint row lies outside
+ * [-1, 2^31 - 1], or whose checkpoint start lies outside [0, 2^31 - 1], is
+ * skipped (reads and writes nothing) and recorded as GDN_DEVERR_INDEX_RANGE
+ * in err_word; the values are otherwise those of the int32 call. */
 int gdn_chunk_gated_delta_rule_ex(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
                                   const float *g, const float *beta, gdn_bf16 *o,
                                   const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens,
                                   int32_t H, int32_t K, int32_t V, float scale,
-                                  const void *initial_state, const int32_t *state_indices,
-                                  void *output_state, const int32_t *output_state_indices,
-                                  void *state_checkpoints, const int32_t *checkpoint_state_indices,
-                                  const int32_t *checkpoint_cu_starts, const int32_t *prefix_lens,
+                                  const void *initial_state, const void *state_indices,
+                                  void *output_state, const void *output_state_indices,
+                                  void *state_checkpoints, const void *checkpoint_state_indices,
+                                  const void *checkpoint_cu_starts, const void *prefix_lens,
                                   int32_t checkpoint_every_n_tokens, int64_t pool_row_stride,
-                                  int32_t state_dtype, void *workspace, size_t workspace_bytes,
-                                  int32_t *err_word, void *stream);
+                                  int32_t state_dtype, int32_t index_dtype, void *workspace,
+                                  size_t workspace_bytes, int32_t *err_word, void *stream);
 int gdn_chunk_gated_delta_rule_paged_ex(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
                                         const float *g, const float *beta, gdn_bf16 *o,
                                         const int32_t *cu_seqlens, int32_t num_seqs,

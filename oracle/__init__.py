@@ -120,7 +120,10 @@ def _row_stride(pool, H, K, V):
         return H * V * K
     if pool.dtype not in (np.float32, np.uint16) or not pool.flags.c_contiguous:
         raise TypeError("pools must be C-contiguous float32, or uint16 holding bf16 bits")
-    return int(np.prod(pool.shape[1:]))
+    stride = int(np.prod(pool.shape[1:]))  # a row may be padded past its H*V*K state elements
+    if stride < H * V * K:
+        raise ValueError("a pool row holds fewer than H*V*K elements")
+    return stride
 
 
 def _state_bf16(pools):

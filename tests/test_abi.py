@@ -91,6 +91,25 @@ def test_prefill_rejects_bad_arguments():
     assert _chunk(lib, ws=FAKE + 8, wsb=need) == -1            # not 16-byte aligned
 
 
+def test_general_call_index_and_state_types_are_checked():
+    lib = gdn.library()
+
+    def ex(sd=0, xd=0, **kw):
+        a = dict(init=FAKE, si=FAKE, out=None, osi=None, stride=2 * 128 * 128)
+        a.update(kw)
+        return lib.gdn_chunk_gated_delta_rule_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 0, 2, 128, 128, 0.0,
+                                                 a["init"], a["si"], a["out"], a["osi"], None, None, None, None, 0,
+                                                 a["stride"], sd, xd, FAKE, 1 << 40, None, None)
+    assert ex() == 0 and ex(xd=1) == 0 and ex(sd=1) == 0  # T = 0: checks pass, nothing to do
+    assert ex(xd=2) == -1 and ex(xd=-1) == -1                # unknown index type
+    assert ex(sd=2) == -1                                    # unknown state type
+    assert ex(xd=1, si=FAKE + 4) == -1                       # int64 slots must be 8-byte aligned
+    assert ex(xd=0, si=FAKE + 4) == 0                        # int32 slots: 4 bytes
+    assert ex(xd=0, si=FAKE + 2) == -1
+    assert ex(sd=1, stride=2 * 128 * 128 + 4) == -1          # bf16 rows: stride a multiple of 8
+    assert ex(sd=0, stride=2 * 128 * 128 + 4) == 0           # fp32 rows: a multiple of 4
+
+
 def test_paged_calls_reject_bad_arguments():
     lib = gdn.library()
     p = FAKE

@@ -170,6 +170,34 @@ def test_checkpoint_rows_minus_one_skip():
     assert (ck[2].view(np.uint32) == before[2].view(np.uint32)).all()
 
 
+def test_padded_pool_rows():
+    """Pools whose rows are padded (row stride > H*V*K, slot arguments
+    paragraph: "the row stride may be padded") give the states of a dense pool
+    in the first H*V*K elements of each row and never touch the padding."""
+    H, N, P, L = 2, 64, 30, 170
+    q, k, v, g, b = draw(L, H, 15)
+    rng = np.random.default_rng(3)
+    n, pad = H * 128 * 128, 24
+    dense = sentinel(4, H)
+    dense[1] = rng.standard_normal((H, 128, 128)).astype(np.float32)
+    padded = np.empty((4, n + pad), np.float32)
+    padded[:, :n] = dense.reshape(4, n)
+    padded[:, n:] = (np.arange(4, dtype=np.uint32).reshape(4, 1) | 0x7FA00000).view(np.float32)
+    before = padded.copy()
+    kw = dict(state_indices=[1], output_state_indices=[3], checkpoint_state_indices=[0, 2, 0],
+              checkpoint_cu_starts=[0], prefix_lens=[P], checkpoint_every_n_tokens=N)
+    o1, w1, c1 = oracle.chunk_gated_delta_rule(q, k, v, g, b, [0, L], SCALE, initial_state=dense,
+                                               output_state=dense, state_checkpoints=dense, **kw)
+    o2, w2, c2 = oracle.chunk_gated_delta_rule(q, k, v, g, b, [0, L], SCALE, initial_state=padded,
+                                               output_state=padded, state_checkpoints=padded, **kw)
+    assert (o1 == o2).all() and (w1 == w2).all() and (c1 == c2).all()
+    assert w1.tolist() == [0, 0, 0, 1] and c1.tolist() == [1, 0, 1, 0]
+    assert (padded[:, :n].view(np.uint32) == dense.reshape(4, n).view(np.uint32)).all()
+    assert (padded[:, n:].view(np.uint32) == before[:, n:].view(np.uint32)).all()
+    with pytest.raises(ValueError):  # rows shorter than one state
+        oracle.chunk_gated_delta_rule(q, k, v, g, b, [0, L], SCALE, initial_state=padded[:, : n - 8].copy(), **kw)
+
+
 def _random_table(rng, S, ps, allow_empty=True):
     lens = rng.integers(0 if allow_empty else 1, 3 * ps, S)
     pre = rng.integers(0, 4 * ps, S)
