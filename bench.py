@@ -147,6 +147,8 @@ def run_gpu(args, rank, world, local_rank):
     if args.workload in ("all", "decode"):
         launches += _bench_decode(args, gdn, workloads, dev, stream, barrier, max_over_ranks, rank, world, hbm,
                                   line)
+    if args.workload in ("all", "layers"):
+        launches += _bench_layers(args, gdn, workloads, dev, stream, barrier, max_over_ranks, world, hbm, line)
     line["gpu_launches"] = launches
     if rank == 0 and not args.no_cpu_baseline and args.workload in ("all", "prefill"):
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -366,6 +368,104 @@ def _bench_decode(args, gdn, workloads, dev, stream, barrier, max_over_ranks, ra
     return 4 * dsteps  # slots + decode, fp32 and bf16 pools (the row-copy timing is a side measurement)
 
 
+def _bench_layers(args, gdn, workloads, dev, stream, barrier, max_over_ranks, world, hbm, line):
+    """Multi-layer model steps: one slots call per step shared by L = 32
+    layers, each layer with its own state pool and inputs, run eagerly (one
+    binding call per layer) and as one captured CUDA graph replayed per step.
+    Between two steps every layer's rows pass once, 1 GB or more, so L2 holds
+    nothing of a layer from one step to the next (no flush)."""
+    L = 32
+    steps = max(args.steps, 10)
+    res = {}
+    launches = 0
+    for name, make in (("decode_B256", lambda: workloads.decode_layers(dev, L=L, B=256, seed=1241 + 10 * world)),
+                       ("decode_B8", lambda: workloads.decode_layers(dev, L=L, B=8, seed=1243 + 10 * world)),
+                       ("prefill_4x8192", lambda: workloads.prefill_layers(dev, L=L, seed=1244 + 10 * world))):
+        st = make()
+        c0 = st.calls[0]
+        H = st.H
+        if isinstance(c0, workloads.DecodeCall):
+            B = c0.q.shape[0]
+            slots = gdn.gdn_paged_decode_slots(c0.page_indptr, c0.page_indices, c0.last_page_len)
+            outs = [torch.empty(B, H, V, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+
+            def step():
+                gdn.gdn_paged_decode_slots(c0.page_indptr, c0.page_indices, c0.last_page_len, out=slots)
+                for l, c in enumerate(st.calls):
+                    gdn.gdn_gated_delta_rule_decode_paged(c.q, c.k, c.v, c.g, c.beta, st.pools[l], c.page_indices,
+                                                          c.page_indptr, c.last_page_len, scale=SCALE, slots=slots,
+                                                          o=outs[l])
+            units, unit = B, "seq"
+            layer_bytes = B * H * DECODE_BYTES_PER_SEQ_HEAD
+        else:
+            T = c0.q.shape[0]
+            S = c0.cu_seqlens.numel() - 1
+            slots = gdn.gdn_paged_prefill_slots(c0.cu_seqlens, c0.page_indptr, c0.page_indices, c0.last_page_len,
+                                                c0.page_size)
+            outs = [torch.empty(T, H, V, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+            ws = torch.empty(gdn.gdn_prefill_workspace_bytes(S, T, H), dtype=torch.uint8, device=dev)
+
+            def step():
+                gdn.gdn_paged_prefill_slots(c0.cu_seqlens, c0.page_indptr, c0.page_indices, c0.last_page_len,
+                                            c0.page_size, out=slots)
+                for l, c in enumerate(st.calls):
+                    gdn.gdn_chunk_gated_delta_rule_paged(c.q, c.k, c.v, c.g, c.beta, c.cu_seqlens, st.pools[l],
+                                                         c.page_indices, c.page_indptr, c.page_size,
+                                                         c.last_page_len, scale=SCALE, slots=slots, o=outs[l],
+                                                         workspace=ws)
+            units, unit = T, "tok"
+            stores = S * -(-(T // S) // c0.page_size)
+            layer_bytes = T * H * BYTES_PER_TOKEN_HEAD + stores * H * STATE_BYTES
+        per_step = (1 + L) if unit == "seq" else (1 + 3 * L)  # slots + per layer decode / (slot map, ut, chain)
+
+        def timed(run):
+            for _ in range(max(args.warmup, 3)):
+                run()
+            start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with ClockSampler(dev.index) as clk:
+                barrier()
+                torch.cuda.synchronize(dev)
+                start.record(stream)
+                for _ in range(steps):
+                    run()
+                stop.record(stream)
+                torch.cuda.synchronize(dev)
+                barrier()
+            return max_over_ranks(start.elapsed_time(stop) / steps), clk.summary()
+
+        eager_ms, clk_e = timed(step)
+        # capture one step (slots + all layers) after an eager warm-up on the capture side stream
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph_ms, clk_g = timed(graph.replay)
+        ach = L * layer_bytes / (graph_ms * 1e-3) / 1e9
+        res[name] = {"workload": st.name, "layers": L, "steps": steps,
+                     "eager_ms_per_step": eager_ms, "graph_ms_per_step": graph_ms,
+                     "graph_us_per_layer": 1e3 * graph_ms / L,
+                     "value": units * world / (graph_ms * 1e-3), "unit": "%s/s through all %d layers" % (unit, L),
+                     "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                                  "algorithmic_bytes_per_step": L * layer_bytes},
+                     "launches_per_step": per_step, "clocks": {"eager": clk_e, "graph": clk_g}}
+        launches += 2 * steps * per_step
+        del graph, st, outs, slots, step
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+    line["layer_step"] = res
+    if "metric" not in line:  # layers-only run: the 256-sequence decode step is the line
+        d = res["decode_B256"]
+        line.update({"metric": METRIC, "value": d["value"], "unit": "seq/s", "n_gpus": world, "steps": steps,
+                     "warmup": max(args.warmup, 3), "ms_per_step": d["graph_ms_per_step"], "higher_is_better": True,
+                     "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+                     "config": {"workload": d["workload"]}, "roofline": d["roofline"], "clocks": d["clocks"]["graph"]})
+    return launches
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline / reference arm)
 # ---------------------------------------------------------------------------
@@ -449,7 +549,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--workload", choices=["all", "prefill", "decode"], default="all")
+    ap.add_argument("--workload", choices=["all", "prefill", "decode", "layers"], default="all")
     ap.add_argument("--prefill-tokens", type=int, default=PREFILL["L"],
                     help="new tokens per sequence of the prefill workload (smaller only for profiling)")
     args = ap.parse_args()

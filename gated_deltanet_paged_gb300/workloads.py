@@ -269,4 +269,87 @@ def long_context(device="cuda", S: int = 4, L: int = 65536, H: int = 32, page_si
                     seq_lens=torch.tensor([L] * S), prefix_lens=torch.zeros(S, dtype=torch.int64))
 
 
+@dataclass
+class LayerStep:
+    """One model step through L GDN layers ("flashinfer.gdn_paged", §Page
+    table: the rows depend only on the batch, so one slots call per step serves
+    every layer).  Every layer has its own state pool, pools[l] = fp32
+    [num_pages, H, V, K], and its own inputs, calls[l]; the page table is the
+    same for all layers."""
+    name: str
+    H: int
+    page_size: int
+    pools: torch.Tensor            # fp32 [L, num_pages, H, V, K]
+    calls: List[object]
+
+
+def decode_layers(device="cuda", L: int = 32, B: int = 256, H: int = 32, page_size: int = 1024,
+                  max_ctx: int = 32768, seed: int = 1241, sentinel: bool = False) -> LayerStep:
+    """B sequences decode one token through L layers.  ctx ~ U{2..max_ctx}, a
+    quarter (seeded) forced to ctx = m * page_size + 1 (the token opens a new
+    page), as in decode_batch.  All pages of a sequence but its last two are
+    full prefix pages shared by every sequence (ids 0 .. n_shared - 1; decode
+    never reads or writes them); the last two are its own (n_shared + 2b,
+    n_shared + 2b + 1), so a layer's pool holds n_shared + 2B rows.  Pools:
+    with ``sentinel`` the usual NaN rows with N(0, 1) in the rows a sequence
+    owns; otherwise (timing) layer 0's rows N(0, 1), copied to every layer."""
+    gen = _gen(seed, device)
+    ctx = torch.randint(2, max_ctx + 1, (B,), generator=gen, device=device)
+    forced = torch.randperm(B, generator=gen, device=device)[: B // 4]
+    m = torch.randint(1, max_ctx // page_size, (B // 4,), generator=gen, device=device)
+    ctx[forced] = m * page_size + 1
+    ctx = ctx.cpu().tolist()
+    n_shared = max(0, max(math.ceil(c / page_size) for c in ctx) - 2)
+    indptr, indices, last = [0], [], []
+    for b, c in enumerate(ctx):
+        n = math.ceil(c / page_size)
+        own = [n_shared + 2 * b, n_shared + 2 * b + 1][2 - min(n, 2):]
+        indices += list(range(n - len(own))) + own
+        indptr.append(len(indices))
+        last.append(c - (n - 1) * page_size)
+    as_t = lambda x: torch.tensor(x, dtype=torch.int32, device=device)
+    ip, pi, lpl = as_t(indptr), as_t(indices), as_t(last)
+    num_pages = n_shared + 2 * B
+    calls = []
+    for _ in range(L):
+        q, k, v, g, b_ = draw_tokens(gen, B, H, device)
+        calls.append(DecodeCall(q, k, v, g, b_, ip, pi, lpl, page_size))
+    if sentinel:
+        pools = torch.stack([sentinel_pool(num_pages, H, device) for _ in range(L)])
+        for l in range(L):
+            fill_rows(pools[l], range(n_shared, num_pages), gen)
+    else:
+        pools = torch.empty(L, num_pages, H, V_DIM, K_DIM, device=device)
+        pools[0] = torch.randn(num_pages, H, V_DIM, K_DIM, generator=gen, device=device)
+        pools[1:] = pools[0]
+    return LayerStep("decode step: %d layers, B=%d, H=%d, ps=%d, ctx U{2..%d} (25%% open a page), "
+                     "last two pages per sequence own, the rest shared" % (L, B, H, page_size, max_ctx),
+                     H, page_size, pools, calls)
+
+
+def prefill_layers(device="cuda", L: int = 32, S: int = 4, T_seq: int = 8192, H: int = 32,
+                   page_size: int = 1152, seed: int = 1242, sentinel: bool = False) -> LayerStep:
+    """S sequences of T_seq new tokens from an empty prefix through L layers
+    (state stored at every page end).  Layer 0's tokens are drawn as usual;
+    layer l's are layer 0's rolled by l * 997 tokens (distinct buffers and
+    contents).  Pools: sentinel NaN rows with ``sentinel``, else zeros (an
+    empty prefix reads no row)."""
+    gen = _gen(seed, device)
+    num_pages = S * math.ceil(T_seq / page_size)
+    perm = torch.randperm(num_pages, generator=gen, device=device).cpu()
+    ip, pi, lpl = page_table([T_seq] * S, perm, page_size, device)
+    q0, k0, v0, g0, b0 = draw_tokens(gen, S * T_seq, H, device)
+    cu = _cu([T_seq] * S, device)
+    calls = []
+    for l in range(L):
+        r = lambda t: torch.roll(t, l * 997, dims=0).contiguous()
+        calls.append(PrefillCall(r(q0), r(k0), r(v0), r(g0), r(b0), cu, ip, pi, lpl, page_size))
+    if sentinel:
+        pools = torch.stack([sentinel_pool(num_pages, H, device) for _ in range(L)])
+    else:
+        pools = torch.zeros(L, num_pages, H, V_DIM, K_DIM, device=device)
+    return LayerStep("prefill step: %d layers, %d seqs x %d new tokens, H=%d, ps=%d"
+                     % (L, S, T_seq, H, page_size), H, page_size, pools, calls)
+
+
 WORKLOADS = {0: tiny, 1: worked_example, 2: decode_batch, 3: mixed_prefill, 4: long_context}
