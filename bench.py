@@ -279,7 +279,7 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
 def _bench_decode(args, gdn, workloads, dev, stream, barrier, max_over_ranks, rank, world, hbm, line):
     H = DECODE["H"]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    wd = workloads.decode_batch(dev, seed=1236 + rank)
+    wd = workloads.decode_batch(dev, seed=1236 + rank, max_ctx=args.decode_max_ctx, num_pages=args.decode_pages)
     dc = wd.calls[0]
     dpool = wd.pool
     od = torch.empty(DECODE["B"], H, V, dtype=torch.bfloat16, device=dev)
@@ -552,6 +552,10 @@ def main():
     ap.add_argument("--workload", choices=["all", "prefill", "decode", "layers"], default="all")
     ap.add_argument("--prefill-tokens", type=int, default=PREFILL["L"],
                     help="new tokens per sequence of the prefill workload (smaller only for profiling)")
+    ap.add_argument("--decode-max-ctx", type=int, default=32768,
+                    help="longest context of the decode batch; with --decode-pages, a smaller pool for profiling "
+                         "(the decode kernels touch one or two rows per sequence at any context)")
+    ap.add_argument("--decode-pages", type=int, default=DECODE["num_pages"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "gdn" else args.warmup
     rank = int(os.environ.get("RANK", "0"))
