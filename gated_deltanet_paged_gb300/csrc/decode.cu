@@ -9,18 +9,34 @@
 // streaming read-update-write bound by HBM bandwidth: 16-byte coalesced,
 // evict-first loads and streaming stores, all 16 loads of a thread in flight
 // before any arithmetic.  In the fp32 kernel each warp owns 16 rows, each
-// lane one float4 of every row; the 32 dot products a warp needs (S k and S q
-// of its 16 rows) are reduced together by a transpose reduction (31 shuffles
-// instead of 160).  The bf16 kernel is laid out below.
+// lane one float4 of every row, and two 4-warp CTAs share a state (rows 0-63
+// and 64-127), which spreads a small batch over more SMs; the 32 dot products
+// a warp needs (S k and S q of its 16 rows) are reduced together by a
+// transpose reduction (31 shuffles instead of 160).  The bf16 kernel is laid
+// out below.
+//
+// Both kernels are launched as programmatic dependents of the kernel before
+// them on the stream: a CTA waits (griddepcontrol.wait) until that kernel has
+// finished and its writes are visible before it reads anything, so the order
+// of the stream is kept, while the launch itself overlaps the previous
+// kernel's tail -- a step of many layers' decodes spends less time between
+// kernels.
 #include <math.h>
 
 #include "common.cuh"
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 constexpr int kRowsPerWarp = 16;
-static_assert(kThreads / 32 * kRowsPerWarp == gdn::kDimV, "one CTA covers one 128-row state");
+static_assert(kThreads / 32 * kRowsPerWarp * 2 == gdn::kDimV, "two CTAs cover one 128-row state");
+
+// Programmatic dependent launch: wait for the previous kernel on the stream to
+// complete (its memory visible), then let the next one begin launching.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+}
 
 struct DecodeArgs {
   const __nv_bfloat16* q;
@@ -98,15 +114,17 @@ __device__ __forceinline__ bool resolve_rows(const DecodeArgs& a, int b, int& in
   return true;
 }
 
-// fp32 pool: 8 warps x 16 rows, each lane one float4 of every row.
-__global__ void __launch_bounds__(kThreads, 2) decode_f32_kernel(const DecodeArgs a) {
-  const int bh = blockIdx.x;
+// fp32 pool: two CTAs per state, each 4 warps x 16 rows, each lane one float4
+// of every row.
+__global__ void __launch_bounds__(kThreads, 4) decode_f32_kernel(const DecodeArgs a) {
+  pdl_enter();
+  const int bh = blockIdx.x >> 1;  // blockIdx.x & 1: which 64 rows of the state
   const int b = bh / a.H, h = bh % a.H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int in_row, out_row;
   if (!resolve_rows(a, b, in_row, out_row)) return;
 
-  const int r0 = warp * kRowsPerWarp;
+  const int r0 = (blockIdx.x & 1) * 64 + warp * kRowsPerWarp;
   const int64_t head_off = static_cast<int64_t>(h) * gdn::kDimV * gdn::kDimK;
 
   float* const pool = static_cast<float*>(a.pool);
@@ -184,6 +202,7 @@ __device__ __forceinline__ float dot8(const float2 (&x)[4], const float2 (&w)[4]
 }
 
 __global__ void __launch_bounds__(kBf16Threads, 3) decode_bf16_kernel(const DecodeArgs a) {
+  pdl_enter();
   const int bh = blockIdx.x;
   const int b = bh / a.H, h = bh % a.H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -295,7 +314,7 @@ extern "C" int gdn_gated_delta_rule_decode_paged_ex(const gdn_bf16* q, const gdn
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(state_pool) ||
       !aligned16(g) || !aligned16(beta))
     return GDN_ERR_INVALID_ARGUMENT;
-  if (static_cast<int64_t>(batch) * H > 0x7FFFFFFF) return GDN_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(batch) * H > 0x3FFFFFFF) return GDN_ERR_UNSUPPORTED;  // two fp32 CTAs per state
   if (batch == 0) return GDN_OK;
   int rc = gdn_host::check_device(nullptr);
   if (rc != GDN_OK) return rc;
@@ -320,10 +339,22 @@ extern "C" int gdn_gated_delta_rule_decode_paged_ex(const gdn_bf16* q, const gdn
   a.last_len = last_page_len;
   a.err_word = err_word;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (state_dtype == GDN_STATE_BF16)
-    decode_bf16_kernel<<<batch * H, kBf16Threads, 0, st>>>(a);
-  else
-    decode_f32_kernel<<<batch * H, kThreads, 0, st>>>(a);
+  cudaLaunchConfig_t cfg = {};  // programmatic dependent launch (see the top of this file)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.stream = st;
+  if (state_dtype == GDN_STATE_BF16) {
+    cfg.gridDim = dim3(batch * H);
+    cfg.blockDim = dim3(kBf16Threads);
+    cudaLaunchKernelEx(&cfg, decode_bf16_kernel, a);
+  } else {
+    cfg.gridDim = dim3(2 * batch * H);
+    cfg.blockDim = dim3(kThreads);
+    cudaLaunchKernelEx(&cfg, decode_f32_kernel, a);
+  }
   return gdn_host::launch_status();
 }
 

@@ -218,7 +218,9 @@ int gdn_chunk_gated_delta_rule_paged_static_workspace(
  * [batch, H, K], v and o [batch, H, V], g and beta [batch, H].  slots
  * (nullable): rows from gdn_paged_decode_slots (or any explicit read / write
  * rows, -1 read = zero state, -1 write = skip); when NULL the kernel derives
- * them from the page table. */
+ * them from the page table.  The kernel is launched as a programmatic
+ * dependent of the previous kernel on the stream (it waits for that kernel to
+ * complete before reading anything), so stream order holds as for any launch. */
 int gdn_gated_delta_rule_decode_paged(const gdn_bf16 *q, const gdn_bf16 *k, const gdn_bf16 *v,
                                       const float *g, const float *beta, gdn_bf16 *o,
                                       int32_t batch, int32_t H, int32_t K, int32_t V, float scale,
