@@ -109,6 +109,37 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+class Replicas:
+    """Timing coordination of N independent replicas, one process per GPU
+    (no collective on the data path): a barrier on both sides of every timed
+    region and the maximum of a per-rank time over the ranks.  ``dist`` is
+    torch.distributed with an initialised process group, or None for one
+    process; ``device`` is where the reduction tensor lives (the GPU with NCCL,
+    "cpu" with gloo)."""
+
+    def __init__(self, dist=None, device="cpu"):
+        self.dist = dist
+        self.device = device
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, x):
+        if self.dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+
+def launch_env():
+    """(rank, world size, local rank) from the launcher's environment; one
+    process when absent."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
@@ -123,17 +154,8 @@ def run_gpu(args, rank, world, local_rank):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    replicas = Replicas(dist, dev)
+    barrier, max_over_ranks = replicas.barrier, replicas.max
 
     hbm, bf16, peak_kind = peaks()
     stream = torch.cuda.current_stream(dev)
@@ -558,9 +580,7 @@ def main():
     ap.add_argument("--decode-pages", type=int, default=DECODE["num_pages"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "gdn" else args.warmup
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, world, local_rank = launch_env()
     if args.impl == "reference":
         line = run_reference(args, rank)
     else:
