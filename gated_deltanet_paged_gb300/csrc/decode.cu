@@ -177,14 +177,16 @@ __global__ void __launch_bounds__(kThreads, 4) decode_f32_kernel(const DecodeArg
   }
 }
 
-// bf16 pool.  A 256-byte bf16 row is half a warp of 16-byte loads, so a warp
-// takes two rows per load: lane l (p = l & 15, half c = l >> 4) holds
-// elements 8p..8p+7 of rows 2i+c, i < 16, 32 rows per warp and four warps per
-// state.  16 loads of 16 bytes in flight per thread (three CTAs per SM); the
-// values stay packed in registers and are widened to fp32 where they are used.
-// A thread has twice the fp32 arithmetic of the fp32 kernel's for the same
-// bytes, enough to show against HBM, so the products and sums run as paired
-// fp32 operations (fma.rn.f32x2, each half rounded like a scalar fma).
+// bf16 pool.  The 32 KB state comes into shared memory by one bulk copy, so
+// that the bytes in flight cost no registers (five CTAs per SM, 160 KB of
+// state reads in flight).  A 256-byte bf16 row is half a warp of 16-byte
+// pieces, so a warp takes two rows per step: lane l (p = l & 15, half
+// c = l >> 4) reads elements 8p..8p+7 of rows 2i+c, i < 16, 32 rows per warp
+// and four warps per state, once for the dot products and once for the
+// update, widening to fp32 as it goes.  A thread has twice the fp32 arithmetic
+// of the fp32 kernel's for the same bytes, enough to show against HBM, so the
+// products and sums run as paired fp32 operations (fma.rn.f32x2, each half
+// rounded like a scalar fma).
 constexpr int kBf16Threads = 128;
 constexpr int kBf16RowsPerWarp = 32;
 static_assert(kBf16Threads / 32 * kBf16RowsPerWarp == gdn::kDimV, "one CTA covers one 128-row state");
@@ -201,28 +203,44 @@ __device__ __forceinline__ float dot8(const float2 (&x)[4], const float2 (&w)[4]
   return r.x + r.y;
 }
 
-__global__ void __launch_bounds__(kBf16Threads, 3) decode_bf16_kernel(const DecodeArgs a) {
+constexpr uint32_t kBf16StateBytes = gdn::kDimV * gdn::kDimK * 2;  // 32 KB
+
+// One bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global into shared memory, completing on an mbarrier.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   gdn::smem_u32(smem_dst)),
+               "l"(src), "r"(bytes), "r"(gdn::smem_u32(bar))
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kBf16Threads, 5) decode_bf16_kernel(const DecodeArgs a) {
+  __shared__ alignas(128) uint4 st[kBf16StateBytes / 16];
+  __shared__ uint64_t bar;
   pdl_enter();
   const int bh = blockIdx.x;
   const int b = bh / a.H, h = bh % a.H;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int p = lane & 15, c = lane >> 4;
   int in_row, out_row;
   if (!resolve_rows(a, b, in_row, out_row)) return;
 
-  const int r0 = warp * kBf16RowsPerWarp;
-  // this lane's piece of row r0 + 2i + c is at lane_off + i * 2 rows
-  const int64_t lane_off = static_cast<int64_t>(h) * gdn::kDimV * gdn::kDimK + (r0 + c) * gdn::kDimK + 8 * p;
-
+  const int64_t head_off = static_cast<int64_t>(h) * gdn::kDimV * gdn::kDimK;
   __nv_bfloat16* const pool = static_cast<__nv_bfloat16*>(a.pool);
-  uint4 s[16];
+  // The whole 32 KB state in one bulk copy (a zero state is written in place).
   if (in_row >= 0) {
-    const __nv_bfloat16* src = pool + in_row * a.row_stride + lane_off;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) s[i] = __ldcs(reinterpret_cast<const uint4*>(src + i * 2 * gdn::kDimK));
+    if (tid == 0) {
+      gdn::mbar_init(&bar, 1);
+      gdn::fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      gdn::mbar_arrive_expect_tx(&bar, kBf16StateBytes);
+      bulk_load(st, pool + in_row * a.row_stride + head_off, kBf16StateBytes, &bar);
+    }
   } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) s[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < static_cast<int>(kBf16StateBytes / 16); i += kBf16Threads) st[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
   }
 
   float2 kk[4], qq[4];
@@ -231,23 +249,37 @@ __global__ void __launch_bounds__(kBf16Threads, 3) decode_bf16_kernel(const Deco
   float kq = dot8(kk, qq);
 #pragma unroll
   for (int m = 8; m >= 1; m >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, m);  // both halves hold all of k, q
+  const int r0 = warp * kBf16RowsPerWarp;
   const int row = r0 + 2 * p + c;  // the row this lane finishes
   const float e = expf(a.g[bh]);
   const float be = a.beta[bh];
   const float myv = __bfloat162float(a.v[static_cast<int64_t>(bh) * gdn::kDimV + row]);
 
+  if (in_row >= 0) {
+    // every lane of a warp takes the same decision, so no shuffle below runs
+    // with part of a warp
+    const bool landed = __all_sync(0xffffffffu, gdn::mbar_wait(&bar, 0));
+    if (!landed) {
+      if (lane == 0) gdn::record_error(a.err_word, GDN_DEVERR_TIMEOUT, b);
+      gdn::mbar_wait(&bar, 0);  // the copy writes this CTA's shared memory: let it finish (bounded)
+      return;
+    }
+  }
+  // this lane's piece of row r0 + 2i + c: srow[32 i] (two 256-byte rows per step)
+  const uint4* srow = st + (r0 + c) * 16 + p;
+
   // 32 partial dot products per lane, value 2i = (S k) and 2i+1 = (S q) of
-  // load i, summed over the 16 lanes of each half by a transpose reduction
+  // step i, summed over the 16 lanes of each half by a transpose reduction
   // (lane bit 3 pairs value bit 4, ..., lane bit 0 pairs value bit 1).  The
   // first step is taken as the values are formed, so that 16 are live at once.
   float x[16];
   {
     const bool upper = (lane & 8) != 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {  // loads j and 8 + j: values 2j, 2j + 1 and 2j + 16, 2j + 17
+    for (int j = 0; j < 8; ++j) {  // steps j and 8 + j: values 2j, 2j + 1 and 2j + 16, 2j + 17
       float2 lo[4], hi[4];
-      widen8(s[j], lo);
-      widen8(s[8 + j], hi);
+      widen8(srow[32 * j], lo);
+      widen8(srow[32 * (8 + j)], hi);
       const float k0 = dot8(lo, kk), k1 = dot8(hi, kk), q0 = dot8(lo, qq), q1 = dot8(hi, qq);
       x[2 * j] = (upper ? k1 : k0) + __shfl_xor_sync(0xffffffffu, upper ? k0 : k1, 8);
       x[2 * j + 1] = (upper ? q1 : q0) + __shfl_xor_sync(0xffffffffu, upper ? q0 : q1, 8);
@@ -263,21 +295,17 @@ __global__ void __launch_bounds__(kBf16Threads, 3) decode_bf16_kernel(const Deco
       x[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
     }
   }
-  // x[0] = (S k), x[1] = (S q) of load p in this half, i.e. of row r0 + 2p + c
+  // x[0] = (S k), x[1] = (S q) of step p in this half, i.e. of row r0 + 2p + c
   const float d = be * (myv - e * x[0]);
   a.o[static_cast<int64_t>(bh) * gdn::kDimV + row] = __float2bfloat16_rn(a.scale * (e * x[1] + d * kq));
 
   if (out_row >= 0) {
-    // An empty asm on the packed values makes the compiler widen them again
-    // here instead of keeping all 128 widened values live from the dot products.
-#pragma unroll
-    for (int i = 0; i < 16; ++i) asm("" : "+r"(s[i].x), "+r"(s[i].y), "+r"(s[i].z), "+r"(s[i].w));
-    __nv_bfloat16* dst = pool + out_row * a.row_stride + lane_off;
+    __nv_bfloat16* dst = pool + out_row * a.row_stride + head_off + (r0 + c) * gdn::kDimK + 8 * p;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const float di = __shfl_sync(0xffffffffu, d, (lane & 16) | i);
       float2 f[4];
-      widen8(s[i], f);
+      widen8(srow[32 * i], f);
       const float2 e2 = make_float2(e, e), d2 = make_float2(di, di);
       float2 n[4];
 #pragma unroll
@@ -347,6 +375,12 @@ extern "C" int gdn_gated_delta_rule_decode_paged_ex(const gdn_bf16* q, const gdn
   cfg.numAttrs = 1;
   cfg.stream = st;
   if (state_dtype == GDN_STATE_BF16) {
+    // five 32 KB states per SM: ask for the largest shared-memory carveout
+    if (cudaFuncSetAttribute(decode_bf16_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
+      cudaGetLastError();
+      return GDN_ERR_CUDA;
+    }
     cfg.gridDim = dim3(batch * H);
     cfg.blockDim = dim3(kBf16Threads);
     cudaLaunchKernelEx(&cfg, decode_bf16_kernel, a);
