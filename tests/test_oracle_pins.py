@@ -471,6 +471,32 @@ def test_heads_are_independent():
     assert (out2 == out1[:, perm]).all()
 
 
+def test_value_rows_are_independent():
+    """Row v of S and component v of every output depend on v only through
+    v_t[v] and row v of the initial state (the recurrence is applied row by
+    row): changing the values and initial state of row 5 changes row 5 of the
+    state and component 5 of the outputs, bit for bit nothing else.  A
+    transposed state or a q / k swap breaks this."""
+    T, H = 70, 2
+    q, k, v, g, b = draw(T, H, 93)
+    rng = np.random.default_rng(19)
+    init = rng.standard_normal((1, H, 128, 128)).astype(np.float32)
+    init2 = init.copy()
+    init2[:, :, 5, :] = rng.standard_normal((H, 128)).astype(np.float32)
+    v2 = v.copy()
+    v2[:, :, 5] = bf16_bits(torch.randn(T, H, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16))
+    outs = []
+    for vv, ii in ((v, init), (v2, init2)):
+        out = np.zeros_like(init)
+        o, _, _ = oracle.chunk_gated_delta_rule(q, k, vv, g, b, [0, T], SCALE, initial_state=ii, state_indices=[0],
+                                                output_state=out, output_state_indices=[0])
+        outs.append((o, out))
+    (o1, s1), (o2, s2) = outs
+    others = [i for i in range(128) if i != 5]
+    assert (o1[:, :, others] == o2[:, :, others]).all() and (s1[:, :, others] == s2[:, :, others]).all()
+    assert (o1[:, :, 5] != o2[:, :, 5]).any() and (s1[:, :, 5] != s2[:, :, 5]).any()
+
+
 def test_rows_outside_write_set_keep_their_bits():
     """NaN-poisoned pool after a mixed batch: exactly the rows the oracle
     reports as written changed; every other row is bit-identical."""
