@@ -534,13 +534,10 @@ int launch_chunk_inverse(const PrefillArgs& a, const void* k, cudaStream_t strea
   }
   // Persistent CTAs: three per SM (the shared-memory and register budget), each
   // taking work items in strides of the grid.
-  static int num_sms = 0;
-  if (num_sms == 0) {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return GDN_ERR_CUDA;
-    num_sms = n;
-  }
+  int dev = 0, num_sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return GDN_ERR_CUDA;
   const long long items = static_cast<long long>((a.num_slots + 1) / 2) * a.H;
   const unsigned grid = static_cast<unsigned>(items < 3LL * num_sms ? items : 3LL * num_sms);
   ut_kernel<<<grid, kUtThreads, UT_SMEM, stream>>>(mk, mt, mw, a);
