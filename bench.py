@@ -109,6 +109,17 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def prefill_config(tokens_per_seq, world):
+    """The `config` of the prefill line, the same for both arms."""
+    full = tokens_per_seq == PREFILL["L"]
+    return {"workload": "long-context paged prefill: 4 seqs x %d new tokens, H=32, K=V=128, page_size=1152, "
+                        "state stored at every page end (step = slots + prefill)%s"
+                        % (tokens_per_seq, "" if full else " [reduced size: not a headline run]"),
+            "tokens_per_step": PREFILL["S"] * tokens_per_seq,
+            "l2": "inputs larger than L2 (streamed q/k/v/o per step), no flush",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 class Replicas:
     """Timing coordination of N independent replicas, one process per GPU
     (no collective on the data path): a barrier on both sides of every timed
@@ -263,7 +274,6 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
 
     value = T * world / (ms_prefill * 1e-3)
     achieved = prefill_bytes / (kernel_ms * 1e-3) / 1e9
-    full = args.prefill_tokens == PREFILL["L"]
     line.update({
         "metric": METRIC,
         "value": value,
@@ -278,11 +288,7 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
         "dtype": "bf16",
         "precision": "bf16 q/k/v/o, fp32 g/beta/state, fp16 tensor-core operands with fp32 accumulation",
         "data": "synthetic (seeded; q,k L2-normalised bf16, v bf16, g=-softplus(N), beta=sigmoid(N))",
-        "config": {"workload": "long-context paged prefill: 4 seqs x %d new tokens, H=32, K=V=128, "
-                               "page_size=1152, state stored at every page end (step = slots + prefill)%s"
-                               % (args.prefill_tokens, "" if full else " [reduced size: not a headline run]"),
-                   "tokens_per_step": T, "l2": "inputs larger than L2 (streamed q/k/v/o per step), no flush",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": prefill_config(args.prefill_tokens, world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": PREFILL_TRAFFIC_PER_TOKEN * T, "traffic_source": TRAFFIC_SOURCE,
                      "kernel": "paged prefill call (slot map + chunk-local kernel + state chain)",
@@ -537,7 +543,7 @@ def cpu_baseline(target_s=15.0):
                       % (n_tok, dt)}
 
 
-def run_reference(args, rank):
+def run_reference(args, rank, world):
     """Reference arm: the fp64 oracle timed on the host cores, each step a
     bounded sample of the prefill workload; rank 0 only."""
     if rank != 0:
@@ -555,8 +561,7 @@ def run_reference(args, rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)", "impl": "reference",
-        "config": {"workload": "long-context paged prefill: 4 seqs x 65,536 new tokens, H=32, K=V=128, "
-                               "page_size=1152 (bounded sample per step)"},
+        "config": prefill_config(PREFILL["L"], world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -582,7 +587,7 @@ def main():
     args.warmup = max(args.warmup, 3) if args.impl == "gdn" else args.warmup
     rank, world, local_rank = launch_env()
     if args.impl == "reference":
-        line = run_reference(args, rank)
+        line = run_reference(args, rank, world)
     else:
         line = run_gpu(args, rank, world, local_rank)
     if rank == 0 and line is not None:
