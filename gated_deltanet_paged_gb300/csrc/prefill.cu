@@ -24,12 +24,14 @@
 //   - warps 0-7, "chain": the fp32 state in registers (thread = state row v,
 //     64 columns), U^T packed in place in TMEM, the state update and its fp16
 //     copy, the outputs and the page-boundary / final state stores; Q~ and K~
-//     of the next chunk, and the slot refills they are first to learn about;
+//     of the next chunk, and the -W and K refills they are first to learn
+//     about;
 //   - warps 8-13, "prep": gates, V -> fp16 and P (decayed, masked Q K^T) of the
 //     next chunk while the chain works on the current one;
-//   - warp 14 issues the preparation's MMAs, warp 15 the chain's.  A thread's
-//     MMA issue runs almost in step with the tensor core, so one issuer would
-//     let a preparation MMA hold up a chain MMA for its whole duration.
+//   - warp 14 issues the preparation's MMAs, warp 15 the chain's (and the V,
+//     T'' and Q refills, off the chain threads' path).  A thread's MMA issue
+//     runs almost in step with the tensor core, so one issuer would let a
+//     preparation MMA hold up a chain MMA for its whole duration.
 // Per chunk (M = 128 = state rows v, fp32 accumulators in TMEM; the U half of
 // D_X is its columns 0-63 for even chunks, 64-127 for odd ones):
 //   prep : D_P  = [Q; .] K^T                  (bf16 from TMA; P from rows 0-63)
@@ -314,8 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_arrive_expect_tx(&sh.bar_q[ch & 1], 16384);
     tma_rows(&tm_q, qslot(ch), &sh.bar_q[ch & 1], ch);
   };
-  // Slot refills, each issued by the thread that learns first that the slot is
-  // free: -W after X, K after U^T K~, V and T'' after U~, Q after Q~ and Q K^T.
+  // Slot refills, each issued by a thread that learns early that the slot is
+  // free: -W after X, K after U^T K~ (chain thread 0); V and T'' after U~, Q
+  // after Q~ and Q K^T (the chain issuer, after X).
   auto tma_k = [&](int ch) {
     mbar_arrive_expect_tx(&sh.bar_k[ch & 1], 16384);
     tma_rows(&tm_k, kslot(ch), &sh.bar_k[ch & 1], ch);
@@ -372,6 +375,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c + 2 < nch) {  // U~ of chunk c has read its V and T'' slots
           tma_v(c + 2);
           tma_t(c + 2);
+          // Q of chunk c+2 into the slot of chunk c: Q~ of chunk c (waited for
+          // above) and Q K^T of chunk c have read it
+          if (!w(&sh.bar_p[e], ph)) {
+            *abort_flag = 1;
+            break;
+          }
+          tma_q(c + 2);
         }
         if (!w(&sh.u_ready, e) || !w(&sh.kt_ready[e], ph)) {
           *abort_flag = 1;
@@ -407,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto w = [&](uint64_t* bar, uint32_t parity) { return mbar_wait_or_abort(bar, parity, abort_flag); };
       for (int p = 0; p < nch; ++p) {
         const uint32_t e = p & 1, ph = (p >> 1) & 1;
-        if (!w(&sh.mp_ready, e)) {
+        if (!w(&sh.mp_ready, e) || !w(&sh.bar_q[e], ph) || !w(&sh.bar_k[e], ph)) {
           *abort_flag = 1;
           break;
         }
@@ -522,7 +532,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           prefetch_g(p + 1);
         }
         __syncwarp();
-        if (lane == 0 && go && pwait(&sh.bar_q[e], (p >> 1) & 1) && pwait(&sh.bar_k[e], (p >> 1) & 1)) {
+        // (Q and K of chunk p are waited for by the threads that read them: the
+        // prep issuer before Q K^T, the chain threads before Q~)
+        if (lane == 0 && go) {
           mbar_arrive(&sh.mp_ready);
           mbar_arrive(&sh.gates_ready[e]);
         }
@@ -674,16 +686,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto kt_part = [&](int q) -> bool {
       const uint32_t eq = q & 1;
       const int lo = chunk_lo(q), hi = chunk_hi(q);
-      if (!cwait(&sh.bar_p[eq], (q >> 1) & 1) || !cwait(&sh.gates_ready[eq], (q >> 1) & 1)) return false;
-      // Q of chunk q+2 into the slot of chunk q once its Q~ and Q K^T are done
-      if (ci == 0 && q + 2 < nch) {
-        if (!mbar_wait_or_abort(&sh.xa_full, eq, abort_flag)) {
-          *abort_flag = 1;
-          ok = false;
-          return false;
-        }
-        tma_q(q + 2);
-      }
+      // (the gates of chunk q were waited for by qt_part(q), earlier on this thread)
+      if (!cwait(&sh.bar_p[eq], (q >> 1) & 1)) return false;
       const float* ksc = sh.gates.ksc[eq];
       uint8_t* kt = sm + kslot(q);
 #pragma unroll
