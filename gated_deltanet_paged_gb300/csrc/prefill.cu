@@ -643,8 +643,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) w[i] = pack_half2(S[32 * hh + 2 * i], S[32 * hh + 2 * i + 1]);
-        tmem_st16(lane_addr + COL_SA + 32 * hc + 16 * hh, w);
+        tmem_st16_nw(lane_addr + COL_SA + 32 * hc + 16 * hh, w);
       }
+      tmem_wait_st();
       tc_fence_before();
     };
     // 32 zero columns of this thread's TMEM lane: the O half of D_X, into which X
@@ -653,8 +654,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t z[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) z[i] = 0u;
-      tmem_st16(taddr, z);
-      tmem_st16(taddr + 16, z);
+      tmem_st16_nw(taddr, z);
+      tmem_st16_nw(taddr + 16, z);
+      tmem_wait_st();
     };
     zero32(lane_addr + COL_DX + 64 + 32 * hc);   // O half of even chunks
     zero32(lane_addr + COL_DX + 128 + 32 * hc);  // O half of odd chunks
@@ -764,8 +766,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lo = chunk_lo(c), hi = chunk_hi(c), tf = chunk_tf(c);
         if (lo == 0 && hi == kChunk) {
           uint32_t f[2][16];
-          tmem_ld16x256_x4(oh + 32 * hc, f[0]);               // lanes 32 wq + 0..15
-          tmem_ld16x256_x4(oh + 32 * hc + (16u << 16), f[1]);  // lanes 32 wq + 16..31
+          tmem_ld16x256_x4_nw(oh + 32 * hc, f[0]);               // lanes 32 wq + 0..15
+          tmem_ld16x256_x4_nw(oh + 32 * hc + (16u << 16), f[1]);  // lanes 32 wq + 16..31
+          tmem_wait_ld2(f[0], f[1]);
           zero32(oh + 32 * hc);
           tc_fence_before();
           mbar_arrive(&sh.o_read[e]);
