@@ -246,13 +246,21 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = host_o.numel() * host_o.element_size()
 
-        def e2e_step():
+        def e2e_step(ev=None):
+            if ev is not None:
+                ev[0].record(stream)
             for n, t in host.items():
                 dbuf[n].copy_(t, non_blocking=True)
+            if ev is not None:
+                ev[1].record(stream)
             gdn.gdn_chunk_gated_delta_rule_paged(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"],
                                                  pre.cu_seqlens, pool, pre.page_indices, pre.page_indptr,
                                                  pre.page_size, pre.last_page_len, scale=SCALE, o=o, workspace=ws)
+            if ev is not None:
+                ev[2].record(stream)
             host_o.copy_(o, non_blocking=True)
+            if ev is not None:
+                ev[3].record(stream)
 
         for _ in range(max(3, args.warmup)):  # first touches of the pinned buffers are slow
             e2e_step()
@@ -260,15 +268,18 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
         e2e_steps = max(1, min(args.steps, 5))
         barrier()
         torch.cuda.synchronize(dev)
+        eev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(e2e_steps)]
         start.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
+        for i in range(e2e_steps):
+            e2e_step(eev[i])
         stop.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
         ms_e2e = max_over_ranks(start.elapsed_time(stop) / e2e_steps)
+        part = lambda j: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in eev)
         e2e = {"value": T * world / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+               "parts_ms": {"h2d": part(0), "call": part(1), "d2h": part(2)}}
         launches += 3 * e2e_steps  # timed steps: slot map, chunk-local kernel, state chain
         del host, host_o, dbuf
 
