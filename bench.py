@@ -48,6 +48,7 @@ PREFILL_TRAFFIC_PER_TOKEN = 2.138e9 / 32768
 TRAFFIC_SOURCE = "ncu dram__bytes_read+write of 4x8192-token call, scaled by tokens"
 PREFILL = dict(S=4, L=65536, H=32, page_size=1152, num_pages=256)
 DECODE = dict(B=256, H=32, page_size=1024, num_pages=10000)
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (the roofline's peak is the measured copy rate)
 
 
 def peaks():
@@ -301,6 +302,7 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
         "data": "synthetic (seeded; q,k L2-normalised bf16, v bf16, g=-softplus(N), beta=sigmoid(N))",
         "config": prefill_config(args.prefill_tokens, world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "frac_of_nominal_8000": achieved / NOMINAL_HBM_GBS,
                      "traffic": PREFILL_TRAFFIC_PER_TOKEN * T, "traffic_source": TRAFFIC_SOURCE,
                      "kernel": "paged prefill call (slot map + chunk-local kernel + state chain)",
                      "kernel_ms": kernel_ms,
@@ -379,6 +381,7 @@ def _bench_decode(args, gdn, workloads, dev, stream, barrier, max_over_ranks, ra
            "workload": "paged decode batch: B=256, H=32, page_size=1024, ctx U{2..32768}, "
                        "25% open a page, 10,000-page pool (step = decode slots + decode)",
            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                        "frac_of_nominal_8000": ach / NOMINAL_HBM_GBS,
                         "algorithmic_bytes": decode_bytes},
            "clocks": dclocks,
            "pool_copy_rows": {"rows": DECODE["B"], "bytes_per_call": copy_bytes, "kernel_ms": copy_ms,
@@ -489,6 +492,7 @@ def _bench_layers(args, gdn, workloads, dev, stream, barrier, max_over_ranks, wo
                      "graph_us_per_layer": 1e3 * graph_ms / L,
                      "value": units * world / (graph_ms * 1e-3), "unit": "%s/s through all %d layers" % (unit, L),
                      "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                        "frac_of_nominal_8000": ach / NOMINAL_HBM_GBS,
                                   "algorithmic_bytes_per_step": L * layer_bytes},
                      "launches_per_step": per_step, "clocks": {"eager": clk_e, "graph": clk_g}}
         launches += 2 * steps * per_step
