@@ -119,11 +119,12 @@ def test_long_ragged_sequences():
     print("long ragged sequences: %r" % errs)
 
 
-@pytest.mark.parametrize("H", [1, 3, 5])
+@pytest.mark.parametrize("H", [1, 3, 5, 64])
 def test_head_counts_that_are_not_powers_of_two(H):
     """The chunk-local kernel's work items (chunk pair x head) and the chain's
     grid (sequence x head) both map through H; odd head counts (and one head)
-    run the ragged prefixes / lengths of the page_size 128 case."""
+    run the ragged prefixes / lengths of the page_size 128 case; 64 heads make
+    the token rows 16 KB wide."""
     ps, lens, prefixes = RAGGED[2]
     call, pool = _ragged_case(200 + H, ps, lens, prefixes, H=H)
     errs = Errors()
