@@ -105,8 +105,8 @@ static int32_t walk_pages(int64_t upto, int32_t page_size, int64_t *pages_closed
  *                           after the prefix (page_indptr[b] + number of pages
  *                           that are full at or before the prefix end)
  *   prefix_lens[b]          tokens before the new ones
- * Returns 0, or -1 if a sequence owns no page or has more new tokens than
- * tokens. */
+ * Returns 0, or -1 if a sequence owns no page, has a last page holding no
+ * token or more than page_size tokens, or has more new tokens than tokens. */
 int oracle_prefill_slots(int32_t num_seqs, const int32_t *cu_seqlens,
                          const int32_t *page_indptr, const int32_t *page_indices,
                          const int32_t *last_page_len, int32_t page_size,
@@ -116,6 +116,8 @@ int oracle_prefill_slots(int32_t num_seqs, const int32_t *cu_seqlens,
     for (int32_t b = 0; b < num_seqs; ++b) {
         int64_t npages = (int64_t)page_indptr[b + 1] - page_indptr[b];
         if (npages < 1) return -1;
+        /* a last page holds at least one token and at most a page of them */
+        if (last_page_len[b] < 1 || last_page_len[b] > page_size) return -1;
         int64_t new_tokens = (int64_t)cu_seqlens[b + 1] - cu_seqlens[b];
         int64_t total = (npages - 1) * page_size + last_page_len[b];
         int64_t prefix = total - new_tokens;
@@ -154,6 +156,7 @@ int oracle_decode_slots(int32_t batch, const int32_t *page_indptr,
     for (int32_t b = 0; b < batch; ++b) {
         int64_t npages = (int64_t)page_indptr[b + 1] - page_indptr[b];
         if (npages < 1) return -1;
+        if (last_page_len[b] < 1 || last_page_len[b] > page_size) return -1;
         int64_t total = (npages - 1) * page_size + last_page_len[b];
         const int32_t *pages = page_indices + page_indptr[b];
         initial_state_indices[b] = total >= 2 ? pages[walk_pages(total - 1, page_size, NULL)] : -1;

@@ -249,6 +249,25 @@ def test_decode_slots_rule():
     assert (p["output_state_indices"] == s["output_state_indices"]).all()
 
 
+@pytest.mark.parametrize("lpl", [0, -3, 65, 1000])
+def test_last_page_len_outside_a_page_is_rejected(lpl):
+    """Page table section: the last page of a sequence holds between one token
+    and a full page, so a last_page_len outside 1..page_size names no token
+    position and both slot derivations refuse the table (rather than walk past
+    the sequence's page list)."""
+    indptr = np.array([0, 2], np.int32)
+    indices = np.array([4, 7], np.int32)
+    last = np.array([lpl], np.int32)
+    with pytest.raises(ValueError):
+        oracle.prefill_slots(np.array([0, 1], np.int32), indptr, indices, last, 64)
+    with pytest.raises(ValueError):
+        oracle.decode_slots(indptr, indices, last, 64)
+    # the bounds themselves are valid
+    for ok in (1, 64):
+        s = oracle.prefill_slots(np.array([0, 1], np.int32), indptr, indices, np.array([ok], np.int32), 64)
+        assert s["output_state_indices"].tolist() == [7]
+
+
 def test_zero_length_sequences_leave_pool_unchanged():
     """A zero-length sequence (and a padded one: no new tokens, one scratch
     page) writes nothing; its neighbours are unaffected."""
