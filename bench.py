@@ -183,9 +183,12 @@ def run_gpu(args, rank, world, local_rank):
                                   line)
     if args.workload in ("all", "layers"):
         launches += _bench_layers(args, gdn, workloads, dev, stream, barrier, max_over_ranks, world, hbm, line)
+    if args.workload in ("all", "configs"):
+        launches += _bench_configs(args, gdn, workloads, dev, stream, hbm, bf16, line)
     line["gpu_launches"] = launches
     if rank == 0 and not args.no_cpu_baseline and args.workload in ("all", "prefill"):
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    line["summary"] = summary(line)
     if dist is not None:
         dist.destroy_process_group()
     return line
@@ -193,7 +196,7 @@ def run_gpu(args, rank, world, local_rank):
 
 def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, rank, world, hbm, bf16, peak_kind,
                    line):
-    wp = workloads.long_context(dev, L=args.prefill_tokens, decode_steps=0, seed=1238 + rank)
+    wp = workloads.long_context(dev, L=args.prefill_tokens, decode_steps=128, seed=1238 + rank)
     pre = wp.calls[0]
     pool = wp.pool
     T, H = pre.q.shape[0], pre.q.shape[1]
@@ -314,6 +317,171 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
     if e2e is not None:
         line["e2e"] = e2e
     del o
+
+    # ---- the workload's decode phase: 128 steps at B = 4 on the prefilled pool ----
+    decs = wp.calls[1:]
+    dslots = gdn.gdn_paged_decode_slots(decs[0].page_indptr, decs[0].page_indices, decs[0].last_page_len)
+    od = torch.empty(PREFILL["S"], H, V, dtype=torch.bfloat16, device=dev)
+
+    def decode_phase():
+        for c in decs:
+            gdn.gdn_paged_decode_slots(c.page_indptr, c.page_indices, c.last_page_len, out=dslots)
+            gdn.gdn_gated_delta_rule_decode_paged(c.q, c.k, c.v, c.g, c.beta, pool, c.page_indices, c.page_indptr,
+                                                  c.last_page_len, scale=SCALE, slots=dslots, o=od)
+
+    decode_phase()  # warm-up (in place: repeats rewrite the same rows)
+    reps = 5
+    pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize(dev)
+    for a_, b_ in pev:
+        a_.record(stream)
+        decode_phase()
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    phase_ms = statistics.median(a_.elapsed_time(b_) for a_, b_ in pev)
+    step_bytes = PREFILL["S"] * H * DECODE_BYTES_PER_SEQ_HEAD
+    us_step = 1e3 * phase_ms / len(decs)
+    line["long_context_decode"] = {
+        "workload": "the long-context workload's decode phase: 128 decode steps at B=4, H=32, on the prefilled "
+                    "pool (step = decode slots + decode; last_page_len 1025..1152, in place)",
+        "us_per_step": us_step, "value": PREFILL["S"] / (us_step * 1e-6), "unit": "seq/s",
+        "roofline": {"bound": "latency", "achieved": step_bytes / (us_step * 1e-6) / 1e9, "peak": hbm,
+                     "unit": "GB/s", "frac": step_bytes / (us_step * 1e-6) / 1e9 / hbm,
+                     "algorithmic_bytes_per_step": step_bytes},
+        "reps": reps}
+    launches += 2 * len(decs) * reps
+    return launches
+
+
+def _event_median_ms(stream, fn, reps):
+    """Median CUDA-event time of fn() on the stream over reps calls (each call
+    bracketed by its own pair of events)."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda.synchronize()
+    for a_, b_ in ev:
+        a_.record(stream)
+        fn()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a_.elapsed_time(b_) for a_, b_ in ev)
+
+
+def _checkpoint_layout(prefix, lens, N):
+    """Checkpoints per sequence, (prefix + len) // N - prefix // N ("Slot
+    arguments of chunk_gated_delta_rule"), laid out densely: (cu_starts, total)."""
+    counts = (prefix + lens) // N - prefix // N
+    starts = np.concatenate([[0], np.cumsum(counts)[:-1]]).astype(np.int32)
+    return starts, int(counts.sum())
+
+
+def _bench_configs(args, gdn, workloads, dev, stream, hbm, bf16, line):
+    """The other workloads of the method's pages: the tiny two-sequence case
+    and the worked 2500-token example (latency of one call), and the mixed
+    chunked-prefill batch through the general slot API (tok/s with both
+    roofline fractions, computed from its seeded draw)."""
+    out = {}
+    launches = 0
+    todev = lambda t: t.to(dev)
+    reps = 50
+
+    # tiny: the prefix call untimed, then the main prefill call and the decode step
+    w = workloads.tiny("cpu")
+    pool = todev(w.pool)
+    c0, c1, cd = w.calls
+    ws = torch.empty(gdn.gdn_prefill_workspace_bytes(2, 137, w.H), dtype=torch.uint8, device=dev)
+
+    def pf(c):
+        return lambda: gdn.gdn_chunk_gated_delta_rule_paged(
+            todev_c[c].q, todev_c[c].k, todev_c[c].v, todev_c[c].g, todev_c[c].beta, todev_c[c].cu_seqlens, pool,
+            todev_c[c].page_indices, todev_c[c].page_indptr, todev_c[c].page_size, todev_c[c].last_page_len,
+            scale=SCALE, workspace=ws, o=outs[c])
+
+    class _C:
+        pass
+
+    def move(c):
+        m = _C()
+        for n in ("q", "k", "v", "g", "beta", "page_indptr", "page_indices", "last_page_len"):
+            setattr(m, n, todev(getattr(c, n)))
+        if hasattr(c, "cu_seqlens"):
+            m.cu_seqlens = todev(c.cu_seqlens)
+        m.page_size = c.page_size
+        return m
+
+    todev_c = {i: move(c) for i, c in enumerate(w.calls)}
+    outs = {0: torch.empty(64, w.H, V, dtype=torch.bfloat16, device=dev),
+            1: torch.empty(137, w.H, V, dtype=torch.bfloat16, device=dev)}
+    pf(0)()
+    ms_pre = _event_median_ms(stream, pf(1), reps)
+    dc = todev_c[2]
+    od = torch.empty(2, w.H, V, dtype=torch.bfloat16, device=dev)
+    ms_dec = _event_median_ms(stream, lambda: gdn.gdn_gated_delta_rule_decode_paged(
+        dc.q, dc.k, dc.v, dc.g, dc.beta, pool, dc.page_indices, dc.page_indptr, dc.last_page_len, scale=SCALE,
+        o=od), reps)
+    out["tiny"] = {"workload": w.name, "prefill_call_us": 1e3 * ms_pre, "decode_call_us": 1e3 * ms_dec,
+                   "unit": "us per call (median of %d, CUDA events)" % reps}
+    launches += reps * 4  # prefill: slot map, chunk-local, chain; decode: one kernel
+
+    # worked example: the 2048-token prefix call untimed, then the 452-token call
+    w = workloads.worked_example("cpu")
+    pool = todev(w.pool)
+    todev_c = {i: move(c) for i, c in enumerate(w.calls)}
+    outs = {0: torch.empty(2048, w.H, V, dtype=torch.bfloat16, device=dev),
+            1: torch.empty(452, w.H, V, dtype=torch.bfloat16, device=dev)}
+    ws = torch.empty(gdn.gdn_prefill_workspace_bytes(1, 2048, w.H), dtype=torch.uint8, device=dev)
+    pf(0)()
+    ms_w = _event_median_ms(stream, pf(1), reps)
+    out["worked_example"] = {"workload": w.name, "prefill_call_us": 1e3 * ms_w,
+                             "value": 452 / (ms_w * 1e-3), "unit": "tok/s (452 new tokens per call)"}
+    launches += reps * 3
+
+    # mixed chunked prefill through the general slot API, checkpoints into a separate buffer
+    w = workloads.mixed_prefill("cpu")
+    c = move(w.calls[0])
+    P, L = w.prefix_lens.numpy(), w.seq_lens.numpy()
+    N = w.checkpoint_every
+    ccs, total = _checkpoint_layout(P, L, N)
+    pool = todev(w.pool)
+    ck = torch.zeros(total, w.H, V, K, dtype=torch.float32, device=dev)
+    cki = torch.arange(total, dtype=torch.int32, device=dev)
+    ccs_d = torch.as_tensor(ccs, device=dev)
+    T, H = c.q.shape[0], w.H
+    S = len(L)
+    ws = torch.empty(gdn.gdn_prefill_workspace_bytes(S, T, H), dtype=torch.uint8, device=dev)
+    om = torch.empty(T, H, V, dtype=torch.bfloat16, device=dev)
+    slots = gdn.gdn_paged_prefill_slots(c.cu_seqlens, c.page_indptr, c.page_indices, c.last_page_len, w.page_size)
+
+    def mixed_step(ev=None):
+        gdn.gdn_paged_prefill_slots(c.cu_seqlens, c.page_indptr, c.page_indices, c.last_page_len, w.page_size,
+                                    out=slots)
+        gdn.gdn_chunk_gated_delta_rule(
+            c.q, c.k, c.v, c.g, c.beta, c.cu_seqlens, scale=SCALE, initial_state=pool,
+            state_indices=slots["state_indices"], output_state=pool,
+            output_state_indices=slots["output_state_indices"], state_checkpoints=ck,
+            checkpoint_state_indices=cki, checkpoint_cu_starts=ccs_d, prefix_lens=slots["prefix_lens"],
+            checkpoint_every_n_tokens=N, o=om, workspace=ws)
+
+    for _ in range(3):
+        mixed_step()
+    with ClockSampler(dev.index) as clk:
+        ms_m = _event_median_ms(stream, mixed_step, 20)
+    reads = int(((P > 0) & (L > 0)).sum())
+    writes = int((L > 0).sum()) + total
+    mbytes = int(L.sum()) * H * BYTES_PER_TOKEN_HEAD + (reads + writes) * H * STATE_BYTES
+    mflops = int(L.sum()) * H * FLOP_PER_TOKEN_HEAD
+    ach = mbytes / (ms_m * 1e-3) / 1e9
+    tf = mflops / (ms_m * 1e-3) / 1e12
+    out["mixed_prefill"] = {
+        "workload": w.name + " (general slot API, checkpoints every 896 tokens into a separate buffer; "
+                             "step = slots + prefill)",
+        "new_tokens": int(L.sum()), "longest": int(L.max()), "state_reads": reads, "state_writes": writes,
+        "ms_per_step": ms_m, "value": int(L.sum()) / (ms_m * 1e-3), "unit": "tok/s",
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                     "algorithmic_bytes": mbytes},
+        "tensor": {"achieved_tflops": tf, "peak_tflops": bf16, "frac": tf / bf16, "flops_per_step": mflops},
+        "clocks": clk.summary()}
+    launches += 20 * 4
+    line["configs"] = out
     return launches
 
 
@@ -509,6 +677,38 @@ def _bench_layers(args, gdn, workloads, dev, stream, barrier, max_over_ranks, wo
     return launches
 
 
+def summary(line):
+    """The headline figures of every measured workload in one short object,
+    printed last so that a reader of the line's tail sees them all."""
+    def get(d, *path):
+        for p_ in path:
+            if not isinstance(d, dict) or p_ not in d:
+                return None
+            d = d[p_]
+        return round(d, 4) if isinstance(d, float) else d
+
+    return {
+        "prefill_long_context_tok_s": get(line, "value") if "tensor" in line else None,
+        "prefill_ms": get(line, "roofline", "kernel_ms"),
+        "prefill_tensor_frac": get(line, "tensor", "frac"),
+        "prefill_hbm_frac": get(line, "roofline", "frac") if "tensor" in line else None,
+        "decode_seq_s": get(line, "decode", "value"),
+        "decode_hbm_frac": get(line, "decode", "roofline", "frac"),
+        "decode_bf16_pool_seq_s": get(line, "decode", "bf16_state_pool", "value"),
+        "decode_bf16_pool_hbm_frac": get(line, "decode", "bf16_state_pool", "roofline", "frac"),
+        "long_context_decode_us_per_step": get(line, "long_context_decode", "us_per_step"),
+        "mixed_prefill_tok_s": get(line, "configs", "mixed_prefill", "value"),
+        "mixed_prefill_hbm_frac": get(line, "configs", "mixed_prefill", "roofline", "frac"),
+        "mixed_prefill_tensor_frac": get(line, "configs", "mixed_prefill", "tensor", "frac"),
+        "worked_example_us": get(line, "configs", "worked_example", "prefill_call_us"),
+        "tiny_prefill_us": get(line, "configs", "tiny", "prefill_call_us"),
+        "tiny_decode_us": get(line, "configs", "tiny", "decode_call_us"),
+        "layer_step_decode_B256_us_per_layer": get(line, "layer_step", "decode_B256", "graph_us_per_layer"),
+        "cpu_oracle_tok_s": get(line, "cpu_baseline", "value"),
+        "cpu_cores": get(line, "cpu_baseline", "cores"),
+    }
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline / reference arm)
 # ---------------------------------------------------------------------------
@@ -591,7 +791,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--workload", choices=["all", "prefill", "decode", "layers"], default="all")
+    ap.add_argument("--workload", choices=["all", "prefill", "decode", "layers", "configs"], default="all")
     ap.add_argument("--prefill-tokens", type=int, default=PREFILL["L"],
                     help="new tokens per sequence of the prefill workload (smaller only for profiling)")
     ap.add_argument("--decode-max-ctx", type=int, default=32768,

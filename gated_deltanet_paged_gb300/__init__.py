@@ -93,8 +93,19 @@ def library():
             lib.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
             lib.gdn_status_string.argtypes = [ctypes.c_int]
             lib.gdn_status_string.restype = ctypes.c_char_p
+            lib.gdn_debug_set_wait_stall.argtypes = [i32]
+            lib.gdn_debug_set_wait_stall.restype = None
             _lib = lib
     return _lib
+
+
+def gdn_debug_set_wait_stall(enable: bool) -> None:
+    """Fault injection for tests of the bounded waits: while enabled, the
+    state-chain kernel of each later prefill call makes its first wait on a
+    barrier that nothing completes; the wait gives up after about 1 ms, before
+    any copy or tensor-core operation is issued, and the call records
+    GDN_DEVERR_TIMEOUT in err_word and writes nothing."""
+    library().gdn_debug_set_wait_stall(1 if enable else 0)
 
 
 def _ptr(t):

@@ -96,14 +96,14 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of an mbarrier, giving up after ~2 s.  Returns
-// false on time-out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for phase `parity` of an mbarrier, giving up after limit_ns (~2 s by
+// default).  Returns false on time-out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait_suspend(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > 2000000000ull) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -46,6 +46,7 @@
 // would not) except Q K^T, which uses the bf16 tiles as loaded.
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "prefill_common.cuh"
@@ -94,6 +95,7 @@ struct Small {
   // hand-offs between warp groups
   uint64_t xa_full, mp_ready, m2_ready, u_ready, s16_ready, gates_ready[2], kt_ready[2], o_read[2];
   uint64_t p_ready[2];          // P of a chunk written (the prep's TMEM readers), by parity
+  uint64_t stall;               // the test hook's barrier, never completed
   uint32_t tmem_base;
   int seq;
   int flag;
@@ -114,12 +116,22 @@ __device__ __forceinline__ uint4 pack8h(const float* x) {
   return u;
 }
 
-// bf16 x 8 -> fp16 x 8 times sc (zeros unless keep); src may equal dst.
-__device__ __forceinline__ void cvt8(uint8_t* dst, const uint8_t* src, float sc, bool keep) {
+// Largest magnitude an fp16 tensor-core operand holds.
+constexpr float kF16Max = 65504.f;
+
+// bf16 x 8 -> fp16 x 8 times sc (zeros unless keep); src may equal dst.  With
+// check, an input element of magnitude above the fp16 range sets bad.
+__device__ __forceinline__ void cvt8(uint8_t* dst, const uint8_t* src, float sc, bool keep, bool check,
+                                     bool& bad) {
   uint4 out = make_uint4(0u, 0u, 0u, 0u);
   if (keep) {
     const uint4 in = *reinterpret_cast<const uint4*>(src);
     const float2 f0 = unpack_bf162(in.x), f1 = unpack_bf162(in.y), f2 = unpack_bf162(in.z), f3 = unpack_bf162(in.w);
+    if (check) {
+      const float m = fmaxf(fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y))),
+                            fmaxf(fmaxf(fabsf(f2.x), fabsf(f2.y)), fmaxf(fabsf(f3.x), fabsf(f3.y))));
+      bad |= !(m <= kF16Max);  // NaN inputs too
+    }
     out.x = pack_half2(f0.x * sc, f0.y * sc);
     out.y = pack_half2(f1.x * sc, f1.y * sc);
     out.z = pack_half2(f2.x * sc, f2.y * sc);
@@ -251,6 +263,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!init_pool) in_row = -1;
   if (!out_pool) out_row = -1;
 
+  if (a.debug_stall) {
+    // Test hook: one wait that runs out (about 1 ms), taken before any copy,
+    // MMA or TMEM allocation, so that nothing is in flight when the CTA leaves.
+    if (tid == 0) {
+      mbar_init(&sh.stall, 1);
+      fence_mbar_init();
+      sh.flag = mbar_wait(&sh.stall, 0, 1000000ull) ? 0 : 1;
+    }
+    __syncthreads();
+    if (sh.flag) {
+      if (tid == 0) record_error(a.err_word, GDN_DEVERR_TIMEOUT, b);
+      return;
+    }
+  }
+
   const int end_pos = P + L;
   const int first_pos = (P / kChunk) * kChunk;
   const int nch = chunk_count(P, L);
@@ -340,6 +367,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_load_2d(sm + dst, &tm_w, bar, 0, row);
     tma_load_2d(sm + dst + 32768, &tm_w, bar, 64, row);
   };
+
+  // With err_word: q, k and v elements beyond the fp16 range (the tensor-core
+  // operands are fp16) and non-finite stored states are reported.
+  const bool check_range = a.err_word != nullptr;
+  bool range_bad = false;
 
   // Two issuing warps, so that an MMA of the preparation never holds up one of
   // the chain (a thread's issue runs almost in step with the tensor core).  Each
@@ -545,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = pt; i < 1024; i += kPrepThreads) {
           const int row = (i & 511) >> 3;
           uint8_t* ptr = sm + vslot(p) + (i >> 9) * kTile + (i & 511) * 16;
-          cvt8(ptr, ptr, 1.f, row >= lo && row < hi);
+          cvt8(ptr, ptr, 1.f, row >= lo && row < hi, check_range, range_bad);
         }
         fence_proxy_async();
         mbar_arrive(&sh.m2_ready);
@@ -582,6 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       if (!pclose()) break;
     }
+    if (range_bad) record_error(a.err_word, GDN_DEVERR_RANGE, b);
   } else {
     // ================================================================= chain
     // Thread (v, hc): state row v (TMEM lane v) and state columns 64 hc .. 64 hc
@@ -679,7 +712,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < 4; ++k) {
         const int i = ci + 256 * k;
         const int kb = i >> 9, rc = i & 511, row = rc >> 3;
-        cvt8(sm + OFF_XA + kb * 32768 + 8192 + 8192 * eq + rc * 16, src + i * 16, gam[row], row >= lo && row < hi);
+        cvt8(sm + OFF_XA + kb * 32768 + 8192 + 8192 * eq + rc * 16, src + i * 16, gam[row], row >= lo && row < hi,
+             check_range, range_bad);
       }
       fence_proxy_async();
       mbar_arrive(&sh.xa_full);
@@ -696,13 +730,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < 4; ++k) {
         const int i = ci + 256 * k;
         const int row = (i & 511) >> 3;
-        cvt8(kt + i * 16, kt + i * 16, ksc[row], row >= lo && row < hi);
+        cvt8(kt + i * 16, kt + i * 16, ksc[row], row >= lo && row < hi, check_range, range_bad);
       }
       fence_proxy_async();
       mbar_arrive(&sh.kt_ready[eq]);
       return true;
     };
     auto store_state = [&](float* pool, int row) {
+      if (check_range) {  // an fp16 operand that overflowed leaves a non-finite state
+        bool fin = true;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) fin &= isfinite(S[i]);
+        range_bad |= !fin;
+      }
       if (a.state_bf16) {  // nearest bf16, ties to even
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pool) + state_off(row));
 #pragma unroll
@@ -819,6 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) bulk_wait_all();
     if (ok && out_row >= 0) store_state(out_pool, out_row);
+    if (range_bad) record_error(a.err_word, GDN_DEVERR_RANGE, b);
   }
 
   tc_fence_before();
@@ -830,8 +871,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+std::atomic<int32_t> g_debug_stall{0};
+
 int launch(PrefillArgs& a, const void* q, const void* k, const void* v, void* workspace, size_t workspace_bytes,
            cudaStream_t stream) {
+  a.debug_stall = g_debug_stall.load(std::memory_order_relaxed);
   const int64_t ns = num_chunk_slots(a.T, a.num_seqs);
   if (!workspace || workspace_bytes < gdn::workspace_bytes(a.T, a.num_seqs, a.H) || !gdn_host::aligned16(workspace))
     return GDN_ERR_INVALID_ARGUMENT;
@@ -894,6 +938,8 @@ void fill_common(PrefillArgs& a, const float* g, const float* beta, gdn_bf16* o,
 }
 
 }  // namespace
+
+extern "C" void gdn_debug_set_wait_stall(int32_t enable) { g_debug_stall.store(enable != 0 ? 1 : 0); }
 
 extern "C" size_t gdn_prefill_workspace_bytes(int32_t num_seqs, int32_t total_tokens, int32_t H) {
   if (num_seqs < 0 || total_tokens < 0 || H < 1) return 0;

@@ -50,6 +50,9 @@ struct PrefillArgs {
   __half* tinv;
   __half* wneg;
   int32_t num_slots;
+  // Test hook (gdn_debug_set_wait_stall): the state chain's first wait is on a
+  // barrier that nothing completes, so that its time-out path runs.
+  int32_t debug_stall;
 };
 
 // Workspace chunk slots.  Chunk c of sequence b lives in slot

@@ -21,9 +21,14 @@ __global__ void prefill_slots_kernel(const int32_t* __restrict__ cu_seqlens, con
   const int32_t i0 = indptr[b], i1 = indptr[b + 1];
   const int64_t n = static_cast<int64_t>(i1) - i0;
   const int64_t len = static_cast<int64_t>(cu_seqlens[b + 1]) - cu_seqlens[b];
-  const int64_t total = (n - 1) * page_size + last_len[b];
+  const int32_t lpl = last_len[b];
+  const int64_t total = (n - 1) * page_size + lpl;
   const int64_t prefix = total - len;
-  if (n < 1 || prefix < 0 || len < 0) {  // not a valid sequence: nothing to read or write
+  // Not a valid sequence (no page, a last page holding no token or more than a
+  // page, more new tokens than tokens, or more tokens than the prefill kernels
+  // address): nothing to read or write, the same sequences the prefill kernels
+  // skip when they derive the rows themselves.
+  if (n < 1 || lpl < 1 || lpl > page_size || prefix < 0 || len < 0 || total > 0x3FFFFFFF) {
     state_indices[b] = -1;
     output_state_indices[b] = -1;
     checkpoint_cu_starts[b] = i0;

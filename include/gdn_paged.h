@@ -41,8 +41,14 @@
  *   - Preconditions (unchecked): page ids are real ids (-1 is not a padding
  *     value); rows written by one sequence are not read or written by another
  *     sequence of the same call; a decoded sequence holds at least one token
- *     before the decoded one; prefill input values stay within the fp16 range
- *     (|x| < 65504), since the tensor-core products run on fp16 operands.
+ *     before the decoded one.
+ *   - fp16 range of the prefill: its tensor-core products run on fp16
+ *     operands, so q, k and v elements must lie within +-65504 and the states
+ *     and intermediate values they produce must stay within the fp16 range.
+ *     Larger values turn into infinities, and the sequence's outputs and
+ *     states then hold non-finite values.  With err_word the prefill kernels
+ *     check every q, k and v element they convert and every state they store,
+ *     and report a violation as GDN_DEVERR_RANGE (the sequence still runs).
  */
 #ifndef GDN_PAGED_H
 #define GDN_PAGED_H
@@ -80,6 +86,7 @@ typedef uint16_t gdn_bf16; /* raw bfloat16 bit pattern */
 #define GDN_DEVERR_PAGE_TABLE 2    /* no page, last_page_len outside 1..page_size, more new tokens than tokens, or tokens past total_tokens */
 #define GDN_DEVERR_NO_PREV_TOKEN 3 /* decode: the decoded token is the sequence's first */
 #define GDN_DEVERR_INDEX_RANGE 4   /* an int64 slot entry outside the int32 range (rows below -1) */
+#define GDN_DEVERR_RANGE 5         /* prefill: a q, k or v element beyond the fp16 range (|x| > 65504, or NaN), or a stored state that is not finite */
 #define GDN_DEVERR_TIMEOUT 15      /* an internal wait ran past its iteration limit */
 
 /* Per-sequence pool rows of a paged prefill batch, each int32 [num_seqs] on
@@ -106,7 +113,9 @@ typedef struct {
  *   output_state_indices[b] = L_b > 0 ? page_indices[page_indptr[b+1] - 1] : -1
  *   checkpoint_cu_starts[b] = page_indptr[b] + P_b / page_size
  *   prefix_lens[b]          = P_b
- * A sequence with no page or with P_b < 0 gets -1 rows, prefix 0.
+ * A sequence with no page, a last_page_len outside 1..page_size, P_b < 0, or
+ * more than 2^30 - 1 tokens gets -1 rows, prefix 0 (the rows the prefill
+ * kernels would skip).
  * Inputs: cu_seqlens [num_seqs+1], page_indptr [num_seqs+1], page_indices,
  * last_page_len [num_seqs]; outputs four int32 [num_seqs] arrays.
  * page_size must be a positive multiple of 64. */
@@ -311,6 +320,16 @@ int gdn_pool_zero_rows(void *pool, int64_t row_bytes, int64_t pool_row_stride_by
  * head), with
  * total_tokens / 64 + 2 num_seqs + 2 chunk slots. */
 size_t gdn_prefill_workspace_bytes(int32_t num_seqs, int32_t total_tokens, int32_t H);
+
+/* gdn_debug_set_wait_stall -- fault injection for tests of the bounded waits
+ * (no counterpart in the method's API).  While enabled (enable != 0), the
+ * state-chain kernel of every prefill call launched afterwards from this
+ * process first waits on a barrier that nothing completes; the wait gives up
+ * after about 1 ms, before the kernel has issued any copy or tensor-core
+ * operation, and the kernel records GDN_DEVERR_TIMEOUT in err_word and
+ * returns: the call writes no output and no pool row.  Disabled by default;
+ * enable 0 disables it again.  Not for production use. */
+void gdn_debug_set_wait_stall(int32_t enable);
 
 /* Static text for a status code. */
 const char *gdn_status_string(int status);

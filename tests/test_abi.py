@@ -14,7 +14,7 @@ HEADER = os.path.join(ROOT, "include", "gdn_paged.h")
 
 def declared():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char \*)\s*(gdn_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|void|const char \*)\s*(gdn_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_boundary():

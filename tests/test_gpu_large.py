@@ -1,9 +1,8 @@
 """GPU parity at the full workload sizes: the 256-sequence decode batch, the
 64-sequence mixed prefill through the general slot API, and the 4 x 65,536
 token long-context prefill followed by 128 decode steps.  The oracle runs on
-every chain where that is cheap (decode, mixed prefill) and on sampled
-(sequence, head) chains of the long-context run; properties that hold at any
-size (finite outputs, untouched rows bit-exact) are checked everywhere."""
+every (sequence, head) chain of each; rows outside the write sets must keep
+their bits."""
 import numpy as np
 import pytest
 import torch
@@ -109,72 +108,60 @@ def test_mixed_prefill_general_api_full_size():
     print("mixed prefill S=64 H=16 (T=%d, %d checkpoints): %r" % (call.q.shape[0], total, errs))
 
 
-SAMPLED_CHAINS = [(0, 0), (1, 13), (2, 22), (3, 31)]
-
-
 def test_long_context_prefill_then_decode():
+    """The long-context workload in full: the 4 x 65,536-token prefill with
+    H = 32 (128 (sequence, head) chains, 57 state stores each), then 128 decode
+    steps on the same pool, every chain against the oracle.  Outputs are
+    compared element by element, every written state row by row, and every
+    other pool row bit for bit.  The oracle runs one sequence (32 chains) at a
+    time so that its fp64 outputs stay a few GB."""
     w = workloads.long_context("cuda")
     pre, decs = w.calls[0], w.calls[1:]
     pool = w.pool
     before = pool.clone()
+    pool_ora = pool.cpu().numpy().copy()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     o = gdn.gdn_chunk_gated_delta_rule_paged(pre.q, pre.k, pre.v, pre.g, pre.beta, pre.cu_seqlens, pool,
                                              pre.page_indices, pre.page_indptr, pre.page_size, pre.last_page_len,
                                              scale=SCALE, err_word=err)
     torch.cuda.synchronize()
     assert err.item() == 0
-    assert torch.isfinite(o.float()).all()
-    owned = pre.page_indices.long()
-    assert torch.isfinite(pool[owned]).all()
-    free = torch.ones(pool.shape[0], dtype=torch.bool, device="cuda")
-    free[owned] = False
-    assert bits_equal(pool[free], before[free])
 
     cu = pre.cu_seqlens.cpu().numpy()
     ip = pre.page_indptr.cpu().numpy()
     pages = pre.page_indices.cpu().numpy()
+    lpl = i32(pre.last_page_len)
     errs = Errors()
-    locals_ = {}
-    for b, h in SAMPLED_CHAINS:
-        t0, t1 = int(cu[b]), int(cu[b + 1])
+    written = np.zeros(pool.shape[0], bool)
+    for b in range(len(cu) - 1):
+        sl = slice(int(cu[b]), int(cu[b + 1]))
         ids = pages[ip[b]:ip[b + 1]]
-        n = len(ids)
-        local = workloads.sentinel_pool(n, 1, "cpu").numpy().copy()
-        sl = slice(t0, t1)
-        o_ref, written = oracle.chunk_gated_delta_rule_paged(
-            bf16_bits(pre.q[sl, h:h + 1]), bf16_bits(pre.k[sl, h:h + 1]), bf16_bits(pre.v[sl, h:h + 1]),
-            f32(pre.g[sl, h:h + 1]), f32(pre.beta[sl, h:h + 1]), [0, t1 - t0], local, np.arange(n, dtype=np.int32),
-            [0, n], pre.page_size, i32(pre.last_page_len[b:b + 1]), SCALE)
-        assert written.all()
-        check_o(o[sl, h:h + 1], o_ref, errs)
-        got = pool[torch.as_tensor(ids, device="cuda").long(), h:h + 1].cpu().numpy()
-        e = rel_fro_rows(got, local)
-        errs.state = max(errs.state, float(e.max()))
-        assert e.max() <= S_TOL, "chain %s: state rel-fro %.4g" % ((b, h), e.max())
-        locals_[(b, h)] = (local, ids)
+        o_ref, w_b = oracle.chunk_gated_delta_rule_paged(
+            bf16_bits(pre.q[sl]), bf16_bits(pre.k[sl]), bf16_bits(pre.v[sl]), f32(pre.g[sl]), f32(pre.beta[sl]),
+            [0, sl.stop - sl.start], pool_ora, ids, [0, len(ids)], pre.page_size, lpl[b:b + 1], SCALE)
+        assert w_b[ids].all() and w_b.sum() == len(ids)  # 57 pages, each written once
+        check_o(o[sl], o_ref, errs)
+        del o_ref
+        written |= w_b.astype(bool)
+    check_pool(pool, before, pool_ora, written, errs, "prefill")
 
-    # 128 decode steps on the same pool (in place; last_page_len 1025 .. 1152)
+    # 128 decode steps on the same pool (in place; last_page_len 1025 .. 1152),
+    # each side continuing from its own fp32 pool
+    before = pool.clone()
+    written = np.zeros(pool.shape[0], bool)
     for step, call in enumerate(decs):
         o_d = gdn.gdn_gated_delta_rule_decode_paged(call.q, call.k, call.v, call.g, call.beta, pool,
                                                     call.page_indices, call.page_indptr, call.last_page_len,
                                                     scale=SCALE, err_word=err)
-        for b, h in SAMPLED_CHAINS:
-            local, ids = locals_[(b, h)]
-            n = len(ids)
-            o_ref, _ = oracle.gated_delta_rule_decode(
-                bf16_bits(call.q[b:b + 1, h:h + 1]), bf16_bits(call.k[b:b + 1, h:h + 1]),
-                bf16_bits(call.v[b:b + 1, h:h + 1]), f32(call.g[b:b + 1, h:h + 1]),
-                f32(call.beta[b:b + 1, h:h + 1]), local, [n - 1], [n - 1], SCALE)
-            check_o(o_d[b:b + 1, h:h + 1], o_ref, errs)
+        o_ref, w_d = oracle.gated_delta_rule_decode_paged(
+            bf16_bits(call.q), bf16_bits(call.k), bf16_bits(call.v), f32(call.g), f32(call.beta), pool_ora,
+            i32(call.page_indices), i32(call.page_indptr), i32(call.last_page_len), call.page_size, SCALE)
+        check_o(o_d, o_ref, errs)
+        written |= w_d.astype(bool)
     torch.cuda.synchronize()
     assert err.item() == 0
-    for b, h in SAMPLED_CHAINS:
-        local, ids = locals_[(b, h)]
-        got = pool[int(ids[-1]), h:h + 1].cpu().numpy()[None]
-        e = rel_fro_rows(got, local[-1:])
-        errs.state = max(errs.state, float(e.max()))
-        assert e.max() <= S_TOL
-    print("long context 4 x 65536, H=32, then 128 decode steps: %r" % errs)
+    check_pool(pool, before, pool_ora, written, errs, "decode")
+    print("long context 4 x 65536, H=32, then 128 decode steps, all chains: %r" % errs)
 
 
 def test_prefill_and_decode_are_deterministic():

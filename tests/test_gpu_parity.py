@@ -240,6 +240,94 @@ def test_device_validation_skips_bad_sequences():
     check_o(o[100:], o_ref[100:], errs)
 
 
+@pytest.mark.parametrize("value", [1.0e6, 300.0])
+@pytest.mark.parametrize("tensor", ["q", "k", "v"])
+def test_value_beyond_fp16_range_is_reported(tensor, value):
+    """The prefill's tensor-core operands are fp16: with err_word, a q, k or v
+    element beyond +-65504 (here about 1e6, planted in sequence 1) is reported
+    as GDN_DEVERR_RANGE for its sequence, while a large value inside the range
+    whose products stay finite (300) is not.  (A k element near the limit,
+    such as 60,000, makes k.k and the factors built from it overflow fp16; the
+    stored states then turn non-finite, which is reported too.)  The other
+    sequence still matches the oracle."""
+    call, pool = _ragged_case(7, 64, [100, 80], [10, 0])
+    t = getattr(call, tensor).clone()
+    t[120, 1, 5] = value  # token 20 of sequence 1, head 1
+    args = {n: getattr(call, n) for n in ("q", "k", "v")}
+    args[tensor] = t
+    call = workloads.PrefillCall(args["q"], args["k"], args["v"], call.g, call.beta, call.cu_seqlens,
+                                 call.page_indptr, call.page_indices, call.last_page_len, call.page_size)
+    pool_g = pool.cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dev = lambda x: x.cuda()
+    o = gdn.gdn_chunk_gated_delta_rule_paged(dev(call.q), dev(call.k), dev(call.v), dev(call.g), dev(call.beta),
+                                             dev(call.cu_seqlens), pool_g, dev(call.page_indices),
+                                             dev(call.page_indptr), 64, dev(call.last_page_len), scale=SCALE,
+                                             err_word=err)
+    torch.cuda.synchronize()
+    if value > 65504:
+        assert int(err.item()) == (5 << 24) | 1
+    else:
+        assert int(err.item()) == 0
+        assert torch.isfinite(o.float()).all()
+    pool_o = pool.numpy().copy()
+    o_ref, written = oracle.chunk_gated_delta_rule_paged(
+        bf16_bits(call.q), bf16_bits(call.k), bf16_bits(call.v), f32(call.g), f32(call.beta), i32(call.cu_seqlens),
+        pool_o, i32(call.page_indices), i32(call.page_indptr), 64, i32(call.last_page_len), SCALE,
+        chains=np.array([[1, 1], [0, 0]], bool))
+    errs = Errors()
+    check_o(o[:100], o_ref[:100], errs)
+    n0 = int(call.page_indptr[1])
+    rows = call.page_indices[:n0].long()
+    got = pool_g[rows.cuda()].cpu().numpy()
+    from gpu_util import rel_fro_rows, S_TOL
+    assert rel_fro_rows(got, pool_o[rows.numpy()]).max() <= S_TOL
+
+
+def test_wait_that_runs_out_is_reported():
+    """A bounded wait that runs out: with the test hook enabled, the state
+    chain's first wait is on a barrier that nothing completes.  It gives up
+    after about 1 ms, before any copy or tensor-core operation is in flight,
+    records GDN_DEVERR_TIMEOUT and returns; the call then has written no output
+    and no pool row, and the next call (hook disabled) runs normally on the
+    same context and matches the oracle."""
+    w = workloads.tiny("cpu")
+    call = w.calls[0]
+    dev = lambda t: t.cuda()
+    pool_g = w.pool.cuda()
+    before = pool_g.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = torch.full((call.q.shape[0], w.H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_debug_set_wait_stall(True)
+    try:
+        gdn.gdn_chunk_gated_delta_rule_paged(dev(call.q), dev(call.k), dev(call.v), dev(call.g), dev(call.beta),
+                                             dev(call.cu_seqlens), pool_g, dev(call.page_indices),
+                                             dev(call.page_indptr), call.page_size, dev(call.last_page_len),
+                                             scale=SCALE, o=o, err_word=err)
+        torch.cuda.synchronize()
+    finally:
+        gdn.gdn_debug_set_wait_stall(False)
+    assert int(err.item()) >> 24 == 15
+    assert bits_equal(pool_g, before)
+    assert torch.isnan(o.float()).all()
+    errs = Errors()
+    prefill_paged_both(call, pool_g, w.pool.numpy().copy(), errs)
+
+
+def test_prefill_slots_refuse_a_last_page_len_outside_a_page():
+    """The slot kernel skips (rows -1, prefix 0) the sequences the prefill
+    kernels skip: a last page holding no token or more than page_size tokens;
+    a valid neighbour keeps its rows (prefix 125 at page_size 64: read its
+    page 1, write its page 1, first checkpoint entry 4 + 1)."""
+    t = lambda x: torch.tensor(x, dtype=torch.int32, device="cuda")
+    slots = gdn.gdn_paged_prefill_slots(t([0, 3, 5, 8]), t([0, 2, 4, 6]), t([5, 6, 7, 8, 9, 10]), t([0, 65, 64]),
+                                        64)
+    assert slots["state_indices"].tolist() == [-1, -1, 10]
+    assert slots["output_state_indices"].tolist() == [-1, -1, 10]
+    assert slots["prefix_lens"].tolist() == [0, 0, 125]
+    assert slots["checkpoint_cu_starts"].tolist() == [0, 2, 5]
+
+
 def test_empty_and_all_zero_length_batches():
     H = 2
     pool = workloads.sentinel_pool(4, H, "cuda")
