@@ -140,6 +140,9 @@ __device__ __forceinline__ void cvt8(uint8_t* dst, const uint8_t* src, float sc,
   *reinterpret_cast<uint4*>(dst) = out;
 }
 
+// kCheck: compiled with the fp16-range and finite-state checks (err_word
+// given); without them the hot loops carry no code for the checks.
+template <bool kCheck>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
@@ -370,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // With err_word: q, k and v elements beyond the fp16 range (the tensor-core
   // operands are fp16) and non-finite stored states are reported.
-  const bool check_range = a.err_word != nullptr;
+  constexpr bool check_range = kCheck;
   bool range_bad = false;
 
   // Two issuing warps, so that an MMA of the preparation never holds up one of
@@ -895,13 +898,13 @@ int launch(PrefillArgs& a, const void* q, const void* k, const void* v, void* wo
       gdn_host::encode_tiles_map_f16(&mt, a.tinv, ns * a.H * 64, 64) != GDN_OK ||
       gdn_host::encode_tiles_map_f16(&mw, a.wneg, ns * a.H * 64, 128) != GDN_OK)
     return GDN_ERR_CUDA;
-  if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-      cudaSuccess) {
+  auto kernel = a.err_word ? prefill_kernel<true> : prefill_kernel<false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess) {
     cudaGetLastError();
     return GDN_ERR_CUDA;
   }
   const long long grid = static_cast<long long>(a.num_seqs) * a.H;
-  prefill_kernel<<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, stream>>>(mq, mk, mv, mt, mo, mw, a);
+  kernel<<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, stream>>>(mq, mk, mv, mt, mo, mw, a);
   return gdn_host::launch_status();
 }
 
