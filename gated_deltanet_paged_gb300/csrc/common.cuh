@@ -110,15 +110,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
 // As mbar_wait, but also gives up as soon as *abort becomes non-zero (another
 // thread of the CTA timed out).
 // The thread sleeps in the wait instruction (no issue slots taken from the
-// warps that work) until the phase completes or ~1 ms passes.
-__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, const volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+// warps that work) until the phase completes or ~1 ms passes.  The loop is a
+// function of its own, so that the many call sites in a kernel's hot loop each
+// carry only the first test.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const volatile int* abort) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait_suspend(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > 2000000000ull) return false;
   }
+}
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort);
 }
 
 // Proxy fence: makes this thread's generic-proxy shared-memory writes visible

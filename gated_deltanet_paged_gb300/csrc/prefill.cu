@@ -141,8 +141,10 @@ __device__ __forceinline__ void cvt8(uint8_t* dst, const uint8_t* src, float sc,
 }
 
 // kCheck: compiled with the fp16-range and finite-state checks (err_word
-// given); without them the hot loops carry no code for the checks.
-template <bool kCheck>
+// given); without them the hot loops carry no code for the checks.  kBf16:
+// pools of bf16 states (else fp32).  The hot loops carry only the code of
+// their own variant.
+template <bool kCheck, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_t,
@@ -644,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Element offset of this thread's 64 state values (row v, columns 64 hc ..)
     // in pool row `row`; pools hold fp32 or (state_bf16) bf16 elements.
     auto state_off = [&](int row) { return row * a.row_stride + head_off + v * kDimK + 64 * hc; };
-    if (in_row >= 0 && a.state_bf16) {
+    if (in_row >= 0 && kBf16) {
       const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(init_pool) +
                                                         state_off(in_row));
 #pragma unroll
@@ -746,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 64; ++i) fin &= isfinite(S[i]);
         range_bad |= !fin;
       }
-      if (a.state_bf16) {  // nearest bf16, ties to even
+      if (kBf16) {  // nearest bf16, ties to even
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pool) + state_off(row));
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -898,7 +900,8 @@ int launch(PrefillArgs& a, const void* q, const void* k, const void* v, void* wo
       gdn_host::encode_tiles_map_f16(&mt, a.tinv, ns * a.H * 64, 64) != GDN_OK ||
       gdn_host::encode_tiles_map_f16(&mw, a.wneg, ns * a.H * 64, 128) != GDN_OK)
     return GDN_ERR_CUDA;
-  auto kernel = a.err_word ? prefill_kernel<true> : prefill_kernel<false>;
+  auto kernel = a.err_word ? (a.state_bf16 ? prefill_kernel<true, true> : prefill_kernel<true, false>)
+                           : (a.state_bf16 ? prefill_kernel<false, true> : prefill_kernel<false, false>);
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess) {
     cudaGetLastError();
     return GDN_ERR_CUDA;
