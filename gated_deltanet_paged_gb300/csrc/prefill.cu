@@ -741,6 +741,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sh.kt_ready[eq]);
       return true;
     };
+    // A state store goes through this warp's 2 KB output staging block, a few
+    // rows at a time, so that every global store instruction writes whole
+    // 256-byte (fp32) or 128-byte (bf16) row halves: lanes write their rows into
+    // the block (16-byte pieces swizzled by row, free of bank conflicts), then
+    // the warp reads the block back in row order and stores it.
     auto store_state = [&](float* pool, int row) {
       if (check_range) {  // an fp16 operand that overflowed leaves a non-finite state
         bool fin = true;
@@ -748,17 +753,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 64; ++i) fin &= isfinite(S[i]);
         range_bad |= !fin;
       }
-      if (kBf16) {  // nearest bf16, ties to even
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(pool) + state_off(row));
+      uint8_t* stg = sm + OFF_OST + warp * 2048;
+      if (lane == 0) bulk_wait_read();  // this warp's last output store has read the block
+      __syncwarp();
+      const int v0 = 32 * wq;
+      if (kBf16) {  // nearest bf16, ties to even; 2 rounds of 16 rows x 128 B
+        __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(pool);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          dst[i] = make_uint4(pack_bf162(S[8 * i], S[8 * i + 1]), pack_bf162(S[8 * i + 2], S[8 * i + 3]),
-                              pack_bf162(S[8 * i + 4], S[8 * i + 5]), pack_bf162(S[8 * i + 6], S[8 * i + 7]));
+        for (int r = 0; r < 2; ++r) {
+          if ((lane >> 4) == r) {
+            const int rr = lane & 15;
+#pragma unroll
+            for (int f = 0; f < 8; ++f)
+              *reinterpret_cast<uint4*>(stg + rr * 128 + ((f ^ (rr & 7)) << 4)) =
+                  make_uint4(pack_bf162(S[8 * f], S[8 * f + 1]), pack_bf162(S[8 * f + 2], S[8 * f + 3]),
+                             pack_bf162(S[8 * f + 4], S[8 * f + 5]), pack_bf162(S[8 * f + 6], S[8 * f + 7]));
+          }
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int pc = 32 * j + lane, rr = pc >> 3, f = pc & 7;
+            const uint4 x = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((f ^ (rr & 7)) << 4));
+            *reinterpret_cast<uint4*>(pb + row * a.row_stride + head_off + (v0 + 16 * r + rr) * kDimK + 64 * hc + 8 * f) = x;
+          }
+          __syncwarp();
+        }
         return;
       }
-      float4* dst = reinterpret_cast<float4*>(pool + state_off(row));
 #pragma unroll
-      for (int i = 0; i < 16; ++i) dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
+      for (int r = 0; r < 4; ++r) {  // 4 rounds of 8 rows x 256 B
+        if ((lane >> 3) == r) {
+          const int rr = lane & 7;
+#pragma unroll
+          for (int f = 0; f < 16; ++f)
+            *reinterpret_cast<float4*>(stg + rr * 256 + ((f ^ rr) << 4)) =
+                make_float4(S[4 * f], S[4 * f + 1], S[4 * f + 2], S[4 * f + 3]);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int pc = 32 * j + lane, rr = pc >> 4, f = pc & 15;
+          const float4 x = *reinterpret_cast<const float4*>(stg + rr * 256 + ((f ^ rr) << 4));
+          *reinterpret_cast<float4*>(pool + row * a.row_stride + head_off + (v0 + 8 * r + rr) * kDimK + 64 * hc + 4 * f) = x;
+        }
+        __syncwarp();
+      }
     };
     if (!qt_part(0) || !kt_part(0)) ok = false;
     for (int c = 0; c < nch && ok; ++c) {
@@ -862,8 +901,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (c + 1 < nch && !kt_part(c + 1)) break;
     }
-    if (lane == 0) bulk_wait_all();
     if (ok && out_row >= 0) store_state(out_pool, out_row);
+    if (lane == 0) bulk_wait_all();
     if (range_bad) record_error(a.err_word, GDN_DEVERR_RANGE, b);
   }
 
