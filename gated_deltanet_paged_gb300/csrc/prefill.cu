@@ -140,6 +140,24 @@ __device__ __forceinline__ void cvt8(uint8_t* dst, const uint8_t* src, float sc,
   *reinterpret_cast<uint4*>(dst) = out;
 }
 
+// The same on a loaded piece, returning the converted one.
+__device__ __forceinline__ uint4 cvt8v(const uint4 in, float sc, bool keep, bool check, bool& bad) {
+  uint4 out = make_uint4(0u, 0u, 0u, 0u);
+  if (keep) {
+    const float2 f0 = unpack_bf162(in.x), f1 = unpack_bf162(in.y), f2 = unpack_bf162(in.z), f3 = unpack_bf162(in.w);
+    if (check) {
+      const float m = fmaxf(fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y))),
+                            fmaxf(fmaxf(fabsf(f2.x), fabsf(f2.y)), fmaxf(fabsf(f3.x), fabsf(f3.y))));
+      bad |= !(m <= kF16Max);  // NaN inputs too
+    }
+    out.x = pack_half2(f0.x * sc, f0.y * sc);
+    out.y = pack_half2(f1.x * sc, f1.y * sc);
+    out.z = pack_half2(f2.x * sc, f2.y * sc);
+    out.w = pack_half2(f3.x * sc, f3.y * sc);
+  }
+  return out;
+}
+
 // kCheck: compiled with the fp16-range and finite-state checks (err_word
 // given); without them the hot loops carry no code for the checks.  kBf16:
 // pools of bf16 states (else fp32).  The hot loops carry only the code of
@@ -713,12 +731,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!cwait(&sh.bar_q[eq], (q >> 1) & 1) || !cwait(&sh.gates_ready[eq], (q >> 1) & 1)) return false;
       const float* gam = sh.gates.gam[eq];
       const uint8_t* src = sm + qslot(q);
+      uint4 in[4];
+      float sc[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {  // every load before any store
+        const int i = ci + 256 * k;
+        in[k] = *reinterpret_cast<const uint4*>(src + i * 16);
+        sc[k] = gam[(i & 511) >> 3];
+      }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int i = ci + 256 * k;
         const int kb = i >> 9, rc = i & 511, row = rc >> 3;
-        cvt8(sm + OFF_XA + kb * 32768 + 8192 + 8192 * eq + rc * 16, src + i * 16, gam[row], row >= lo && row < hi,
-             check_range, range_bad);
+        *reinterpret_cast<uint4*>(sm + OFF_XA + kb * 32768 + 8192 + 8192 * eq + rc * 16) =
+            cvt8v(in[k], sc[k], row >= lo && row < hi, check_range, range_bad);
       }
       fence_proxy_async();
       mbar_arrive(&sh.xa_full);
@@ -731,11 +757,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!cwait(&sh.bar_p[eq], (q >> 1) & 1)) return false;
       const float* ksc = sh.gates.ksc[eq];
       uint8_t* kt = sm + kslot(q);
+      uint4 in[4];
+      float sc[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {  // every load before any store
+        const int i = ci + 256 * k;
+        in[k] = *reinterpret_cast<const uint4*>(kt + i * 16);
+        sc[k] = ksc[(i & 511) >> 3];
+      }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int i = ci + 256 * k;
         const int row = (i & 511) >> 3;
-        cvt8(kt + i * 16, kt + i * 16, ksc[row], row >= lo && row < hi, check_range, range_bad);
+        *reinterpret_cast<uint4*>(kt + i * 16) = cvt8v(in[k], sc[k], row >= lo && row < hi, check_range, range_bad);
       }
       fence_proxy_async();
       mbar_arrive(&sh.kt_ready[eq]);
