@@ -34,7 +34,7 @@
 //     preparation MMA hold up a chain MMA for its whole duration.
 // Per chunk (M = 128 = state rows v, fp32 accumulators in TMEM; the U half of
 // D_X is its columns 0-63 for even chunks, 64-127 for odd ones):
-//   prep : D_P  = [Q; .] K^T                  (bf16 from TMA; P from rows 0-63)
+//   prep : D_P  = Q K^T                        (M = 64, bf16 from TMA)
 //          D_X(U half) = V^T T''^T                   (U~^T; the chain threads zero
 //                                                      the O half after reading it)
 //   chain: D_X += S0 [-W; Q~]^T or S0 [Q~; -W]^T      (U half: U^T; O half:
@@ -74,7 +74,7 @@ constexpr uint32_t OFF_SMALL = 221184;
 // TMEM columns (lane = state row v).
 constexpr uint32_t COL_DX = 0;     // two 128-column accumulators S0 [XA rows]^T, by chunk parity
 constexpr uint32_t COL_DSU = 256;  // U^T K~
-constexpr uint32_t COL_DP = 384;   // Q K^T of the chunk being prepared (lanes t 0-63, 64 columns)
+constexpr uint32_t COL_DP = 384;   // Q K^T of the chunk being prepared (M = 64: row t in lane 32 (t / 16) + t % 16)
 constexpr uint32_t COL_SA = 448;   // S0 in fp16 pairs: the A operand of S0 [XA rows]^T
 constexpr uint32_t TMEM_COLS = 512;
 
@@ -460,10 +460,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kPrepIssuerWarp) {
     // =========================================================== prep issuer
-    //   D_P  = [Q; .] K^T                      (bf16 from TMA; rows 0-63)
+    //   D_P  = Q K^T                           (M = 64, bf16 from TMA)
     //   D_X(U half) = V^T T''^T                (U~^T)
     const uint32_t id_m2 = idesc_f16(128, 64, false, false, true, true);
-    const uint32_t id_qk = idesc_f16(128, 64, true, true, false, false);
+    const uint32_t id_qk = idesc_f16(64, 64, true, true, false, false);
     // Q K^T is committed only once the chunk's V conversion is in (m2_ready):
     // the preparation threads learn of it (bar_p) before they can arrive on
     // m2_ready or mp_ready for the next chunk, so neither barrier can run a
@@ -499,8 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 8) {
     // ================================================================== prep
     const int pt = tid - 256, pw = warp - 8;
-    const int wq = warp & 3, ph = pw >> 2;
-    const bool tm_reader = wq < 2;                      // warps 8, 9, 12, 13: TMEM lanes 0-63
+    const int wq = warp & 3;
+    const bool tm_reader = warp < 12;  // warps 8-11: one per TMEM lane quarter (rows 16 wq .. 16 wq + 15 of D_P)
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * wq) << 16);
     // Every thread waits for what it needs itself; a thread whose wait fails
     // skips its work, and the group agrees on stopping once per chunk, at the
@@ -605,14 +605,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async();
         mbar_arrive(&sh.m2_ready);
       }
-      // 3. P = decayed, masked Q K^T (TMEM lanes 0-63) once U^T P^T of chunk p-2
+      // 3. P = decayed, masked Q K^T (warps 8-11, a thread per row and half) once U^T P^T of chunk p-2
       //    has read this P tile; warps other than 8 read its gate tables
       if (tm_reader && pwait(&sh.bar_p[e], (p >> 1) & 1) &&
           (p < 2 || pwait(&sh.bar_o[e], ((p - 2) >> 1) & 1)) &&
           (pw == 0 || pwait(&sh.gates_ready[e], (p >> 1) & 1))) {
-        const int t = 32 * wq + lane;
+        const int t = 16 * wq + (lane & 15), ph = lane >> 4;  // row t, columns 32 ph ..
         float x[32];
-        tmem_ld32(lane_addr + COL_DP + 32 * ph, x);
+        tmem_ld16x32bx2_32(lane_addr + COL_DP, x);
         float out[32];
         const int j0 = 32 * ph;
         const int jmax = min(j0 + 31, t);
@@ -791,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) bulk_wait_read();  // this warp's last output store has read the block
       __syncwarp();
       const int v0 = 32 * wq;
-      if (kBf16) {  // nearest bf16, ties to even; 2 rounds of 16 rows x 128 B
+      if constexpr (kBf16) {  // nearest bf16, ties to even; 2 rounds of 16 rows x 128 B
         __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(pool);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
@@ -812,25 +812,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
         }
-        return;
-      }
+      } else {
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {  // 4 rounds of 8 rows x 256 B
-        if ((lane >> 3) == r) {
-          const int rr = lane & 7;
+        for (int r = 0; r < 4; ++r) {  // 4 rounds of 8 rows x 256 B
+          if ((lane >> 3) == r) {
+            const int rr = lane & 7;
 #pragma unroll
-          for (int f = 0; f < 16; ++f)
-            *reinterpret_cast<float4*>(stg + rr * 256 + ((f ^ rr) << 4)) =
-                make_float4(S[4 * f], S[4 * f + 1], S[4 * f + 2], S[4 * f + 3]);
+            for (int f = 0; f < 16; ++f)
+              *reinterpret_cast<float4*>(stg + rr * 256 + ((f ^ rr) << 4)) =
+                  make_float4(S[4 * f], S[4 * f + 1], S[4 * f + 2], S[4 * f + 3]);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int pc = 32 * j + lane, rr = pc >> 4, f = pc & 15;
+            const float4 x = *reinterpret_cast<const float4*>(stg + rr * 256 + ((f ^ rr) << 4));
+            *reinterpret_cast<float4*>(pool + row * a.row_stride + head_off + (v0 + 8 * r + rr) * kDimK + 64 * hc + 4 * f) = x;
+          }
+          __syncwarp();
         }
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int pc = 32 * j + lane, rr = pc >> 4, f = pc & 15;
-          const float4 x = *reinterpret_cast<const float4*>(stg + rr * 256 + ((f ^ rr) << 4));
-          *reinterpret_cast<float4*>(pool + row * a.row_stride + head_off + (v0 + 8 * r + rr) * kDimK + 64 * hc + 4 * f) = x;
-        }
-        __syncwarp();
       }
     };
     if (!qt_part(0) || !kt_part(0)) ok = false;
