@@ -664,62 +664,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Element offset of this thread's 64 state values (row v, columns 64 hc ..)
     // in pool row `row`; pools hold fp32 or (state_bf16) bf16 elements.
     auto state_off = [&](int row) { return row * a.row_stride + head_off + v * kDimK + 64 * hc; };
-    // The initial state comes in through this warp's 2 KB output staging block,
-    // a few rows at a time: the warp loads whole row halves (256 bytes fp32, 128
-    // bytes bf16) per instruction, and each lane then takes its own row.
-    if (in_row >= 0) {
-      uint8_t* stg = sm + OFF_OST + warp * 2048;
-      const int v0 = 32 * wq;
-      if constexpr (kBf16) {
-        const __nv_bfloat16* pb = reinterpret_cast<const __nv_bfloat16*>(init_pool);
+    if (in_row >= 0 && kBf16) {
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(init_pool) +
+                                                        state_off(in_row));
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {  // 2 rounds of 16 rows x 128 B
+      for (int i = 0; i < 8; ++i) {
+        const uint4 x = src[i];
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int pc = 32 * j + lane, rr = pc >> 3, f = pc & 7;
-            *reinterpret_cast<uint4*>(stg + rr * 128 + ((f ^ (rr & 7)) << 4)) = *reinterpret_cast<const uint4*>(
-                pb + in_row * a.row_stride + head_off + (v0 + 16 * r + rr) * kDimK + 64 * hc + 8 * f);
-          }
-          __syncwarp();
-          if ((lane >> 4) == r) {
-            const int rr = lane & 15;
-#pragma unroll
-            for (int f = 0; f < 8; ++f) {
-              const uint4 x = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((f ^ (rr & 7)) << 4));
-              const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float2 v2 = unpack_bf162(w[q]);
-                S[8 * f + 2 * q] = v2.x;
-                S[8 * f + 2 * q + 1] = v2.y;
-              }
-            }
-          }
-          __syncwarp();
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = unpack_bf162(w[j]);
+          S[8 * i + 2 * j] = f.x;
+          S[8 * i + 2 * j + 1] = f.y;
         }
-      } else {
+      }
+    } else if (in_row >= 0) {
+      const float4* src = reinterpret_cast<const float4*>(init_pool + state_off(in_row));
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {  // 4 rounds of 8 rows x 256 B
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int pc = 32 * j + lane, rr = pc >> 4, f = pc & 15;
-            *reinterpret_cast<float4*>(stg + rr * 256 + ((f ^ rr) << 4)) = *reinterpret_cast<const float4*>(
-                init_pool + in_row * a.row_stride + head_off + (v0 + 8 * r + rr) * kDimK + 64 * hc + 4 * f);
-          }
-          __syncwarp();
-          if ((lane >> 3) == r) {
-            const int rr = lane & 7;
-#pragma unroll
-            for (int f = 0; f < 16; ++f) {
-              const float4 x = *reinterpret_cast<const float4*>(stg + rr * 256 + ((f ^ rr) << 4));
-              S[4 * f] = x.x;
-              S[4 * f + 1] = x.y;
-              S[4 * f + 2] = x.z;
-              S[4 * f + 3] = x.w;
-            }
-          }
-          __syncwarp();
-        }
+      for (int i = 0; i < 16; ++i) {
+        const float4 x = src[i];
+        S[4 * i] = x.x;
+        S[4 * i + 1] = x.y;
+        S[4 * i + 2] = x.z;
+        S[4 * i + 3] = x.w;
       }
     } else {
 #pragma unroll
