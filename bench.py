@@ -242,50 +242,88 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
     launches = 4 * args.steps  # slots, slot map, chunk-local kernel, state chain
 
     # ---- e2e: host buffers, copies inside the timed region ----
+    # Every step copies its own inputs from pinned host memory and reads its
+    # output back, as a serving loop would: the steps are pipelined over three
+    # kinds of streams (input copies split over three copy streams, the call on
+    # the main stream, the read-back on its own), with the device-side inputs
+    # and outputs double-buffered, so step i+1's inputs travel while step i
+    # computes and step i-1's output comes back.
     e2e = None
     if not args.no_e2e:
-        host = {n: getattr(pre, n).cpu().pin_memory() for n in ("q", "k", "v", "g", "beta")}
+        names = ("q", "k", "v", "g", "beta")
+        # one pinned copy of the inputs (read-only on the host) and one output
+        # buffer (the read-backs run in order on one stream)
+        host = {n: getattr(pre, n).cpu().pin_memory() for n in names}
         host_o = torch.empty(T, H, V, dtype=torch.bfloat16).pin_memory()
-        dbuf = {n: torch.empty_like(getattr(pre, n)) for n in host}
+        dbuf = [{n: torch.empty_like(getattr(pre, n)) for n in names} for _ in range(2)]
+        dev_o = [torch.empty(T, H, V, dtype=torch.bfloat16, device=dev) for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = host_o.numel() * host_o.element_size()
+        s_in = [torch.cuda.Stream(dev) for _ in range(3)]
+        s_out = torch.cuda.Stream(dev)
 
-        def e2e_step(ev=None):
-            if ev is not None:
-                ev[0].record(stream)
-            for n, t in host.items():
-                dbuf[n].copy_(t, non_blocking=True)
-            if ev is not None:
-                ev[1].record(stream)
-            gdn.gdn_chunk_gated_delta_rule_paged(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"],
-                                                 pre.cu_seqlens, pool, pre.page_indices, pre.page_indptr,
-                                                 pre.page_size, pre.last_page_len, scale=SCALE, o=o, workspace=ws)
-            if ev is not None:
-                ev[2].record(stream)
-            host_o.copy_(o, non_blocking=True)
-            if ev is not None:
-                ev[3].record(stream)
+        def e2e_run(nsteps, marks=None):
+            """nsteps pipelined steps; marks (optional) collects per-step events."""
+            ev = lambda: torch.cuda.Event(enable_timing=marks is not None)
+            done_call, done_out = [None] * nsteps, [None] * nsteps
+            for i in range(nsteps):
+                b = i & 1
+                ins = []
+                for j, n in enumerate(("q", "k", "v")):  # the large tensors, one copy stream each
+                    st = s_in[j]
+                    with torch.cuda.stream(st):
+                        if i >= 2:
+                            st.wait_event(done_call[i - 2])  # buffer b free: call i-2 has read it
+                        if marks is not None and j == 0:
+                            e0 = ev(); e0.record(st)
+                        dbuf[b][n].copy_(host[n], non_blocking=True)
+                        if n == "v":
+                            dbuf[b]["g"].copy_(host["g"], non_blocking=True)
+                            dbuf[b]["beta"].copy_(host["beta"], non_blocking=True)
+                        e = ev(); e.record(st); ins.append(e)
+                for e in ins:
+                    stream.wait_event(e)
+                if i >= 2:
+                    stream.wait_event(done_out[i - 2])  # output buffer b read back
+                if marks is not None:
+                    c0 = ev(); c0.record(stream)
+                gdn.gdn_chunk_gated_delta_rule_paged(
+                    dbuf[b]["q"], dbuf[b]["k"], dbuf[b]["v"], dbuf[b]["g"], dbuf[b]["beta"], pre.cu_seqlens, pool,
+                    pre.page_indices, pre.page_indptr, pre.page_size, pre.last_page_len, scale=SCALE, o=dev_o[b],
+                    workspace=ws)
+                done_call[i] = ev(); done_call[i].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(done_call[i])
+                    host_o.copy_(dev_o[b], non_blocking=True)
+                    done_out[i] = ev(); done_out[i].record(s_out)
+                if marks is not None:
+                    marks.append((e0, ins, c0, done_call[i], done_out[i]))
+            for st in s_in + [s_out]:
+                stream.wait_stream(st)
 
-        for _ in range(max(3, args.warmup)):  # first touches of the pinned buffers are slow
-            e2e_step()
+        e2e_run(max(3, args.warmup))  # first touches of the pinned buffers are slow
         torch.cuda.synchronize(dev)
-        e2e_steps = max(1, min(args.steps, 5))
+        e2e_steps = max(2, min(args.steps, 6))
         barrier()
         torch.cuda.synchronize(dev)
-        eev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(e2e_steps)]
+        marks = []
         start.record(stream)
-        for i in range(e2e_steps):
-            e2e_step(eev[i])
+        for st in s_in + [s_out]:
+            st.wait_stream(stream)
+        e2e_run(e2e_steps, marks)
         stop.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
         ms_e2e = max_over_ranks(start.elapsed_time(stop) / e2e_steps)
-        part = lambda j: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in eev)
+        mean = lambda xs: statistics.mean(xs)
         e2e = {"value": T * world / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
-               "parts_ms": {"h2d": part(0), "call": part(1), "d2h": part(2)}}
+               "pipelined": "device inputs and outputs double-buffered; input copies on 3 streams, read-back on its own",
+               "parts_ms": {"h2d": mean(max(m[0].elapsed_time(e) for e in m[1]) for m in marks),
+                            "call": mean(m[2].elapsed_time(m[3]) for m in marks),
+                            "d2h": mean(m[3].elapsed_time(m[4]) for m in marks)}}
         launches += 3 * e2e_steps  # timed steps: slot map, chunk-local kernel, state chain
-        del host, host_o, dbuf
+        del host, host_o, dbuf, dev_o
 
     value = T * world / (ms_prefill * 1e-3)
     achieved = prefill_bytes / (kernel_ms * 1e-3) / 1e9
