@@ -394,6 +394,23 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
     graph.replay()
     graph_ms = time_phase(graph.replay)
     del graph
+
+    # the same steps with the decode call deriving its rows from the page table
+    # (no slots argument): one launch per step
+    def decode_phase_fused():
+        for c in decs:
+            gdn.gdn_gated_delta_rule_decode_paged(c.q, c.k, c.v, c.g, c.beta, pool, c.page_indices, c.page_indptr,
+                                                  c.last_page_len, scale=SCALE, o=od)
+
+    with torch.cuda.stream(side):
+        decode_phase_fused()
+    stream.wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        decode_phase_fused()
+    graph.replay()
+    fused_ms = time_phase(graph.replay)
+    del graph
     step_bytes = PREFILL["S"] * H * DECODE_BYTES_PER_SEQ_HEAD
     us_step = 1e3 * graph_ms / len(decs)
     line["long_context_decode"] = {
@@ -401,12 +418,13 @@ def _bench_prefill(args, gdn, workloads, dev, stream, barrier, max_over_ranks, r
                     "pool (step = decode slots + decode; last_page_len 1025..1152, in place), replayed as one "
                     "captured CUDA graph",
         "us_per_step": us_step, "eager_us_per_step": 1e3 * eager_ms / len(decs),
+        "rows_from_page_table_us_per_step": 1e3 * fused_ms / len(decs),
         "value": PREFILL["S"] / (us_step * 1e-6), "unit": "seq/s",
         "roofline": {"bound": "latency", "achieved": step_bytes / (us_step * 1e-6) / 1e9, "peak": hbm,
                      "unit": "GB/s", "frac": step_bytes / (us_step * 1e-6) / 1e9 / hbm,
                      "algorithmic_bytes_per_step": step_bytes},
         "reps": reps}
-    launches += 2 * len(decs) * 2 * reps  # eager and graph phases
+    launches += 2 * len(decs) * 2 * reps + len(decs) * reps  # eager and graph phases, one-launch graph
     return launches
 
 
@@ -754,6 +772,8 @@ def summary(line):
         "decode_bf16_pool_seq_s": get(line, "decode", "bf16_state_pool", "value"),
         "decode_bf16_pool_hbm_frac": get(line, "decode", "bf16_state_pool", "roofline", "frac"),
         "long_context_decode_us_per_step": get(line, "long_context_decode", "us_per_step"),
+        "long_context_decode_one_launch_us_per_step": get(line, "long_context_decode",
+                                                          "rows_from_page_table_us_per_step"),
         "mixed_prefill_tok_s": get(line, "configs", "mixed_prefill", "value"),
         "mixed_prefill_hbm_frac": get(line, "configs", "mixed_prefill", "roofline", "frac"),
         "mixed_prefill_tensor_frac": get(line, "configs", "mixed_prefill", "tensor", "frac"),
