@@ -514,6 +514,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       return ok;
     };
+    // The same without the tcgen05 fence, for waits followed by shared-memory
+    // work only (the next TMEM access or MMA comes after a fenced wait).
+    auto pwait_nf = [&](uint64_t* bar, uint32_t parity) -> bool {
+      if (ok && !mbar_wait_or_abort(bar, parity, abort_flag)) {
+        ok = false;
+        *abort_flag = 1;
+      }
+      return ok;
+    };
     auto pclose = [&]() -> bool {
       uint32_t any;
       asm volatile(
@@ -565,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       //    are in (it has its own TMEM columns)
       if (pw == 0) {
         // warp-uniform, so that the shuffles below see every lane
-        const bool go = __all_sync(0xffffffffu, p < 2 || pwait(&sh.kt_ready[e], ((p - 2) >> 1) & 1));
+        const bool go = __all_sync(0xffffffffu, p < 2 || pwait_nf(&sh.kt_ready[e], ((p - 2) >> 1) & 1));
         float s = go ? pg0 + pg1 : 0.f;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -596,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // 2. V -> fp16 in place; U~ = T'' V follows (its issuer waits for T'' and
       //    for the chunk's D_X half)
-      if (pwait(&sh.bar_v[e], (p >> 1) & 1)) {
+      if (pwait_nf(&sh.bar_v[e], (p >> 1) & 1)) {
         for (int i = pt; i < 1024; i += kPrepThreads) {
           const int row = (i & 511) >> 3;
           uint8_t* ptr = sm + vslot(p) + (i >> 9) * kTile + (i & 511) * 16;
@@ -658,6 +667,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 1;
       }
       tc_fence_after();
+      return ok;
+    };
+    // Without the tcgen05 fence: for the waits before the Q~ and K~ conversions,
+    // which touch shared memory only.
+    auto cwait_nf = [&](uint64_t* bar, uint32_t parity) {
+      if (ok && !mbar_wait_or_abort(bar, parity, abort_flag)) {
+        ok = false;
+        *abort_flag = 1;
+      }
       return ok;
     };
     float S[64];
@@ -728,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto qt_part = [&](int q) -> bool {
       const uint32_t eq = q & 1;
       const int lo = chunk_lo(q), hi = chunk_hi(q);
-      if (!cwait(&sh.bar_q[eq], (q >> 1) & 1) || !cwait(&sh.gates_ready[eq], (q >> 1) & 1)) return false;
+      if (!cwait_nf(&sh.bar_q[eq], (q >> 1) & 1) || !cwait_nf(&sh.gates_ready[eq], (q >> 1) & 1)) return false;
       const float* gam = sh.gates.gam[eq];
       const uint8_t* src = sm + qslot(q);
       uint4 in[4];
@@ -754,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t eq = q & 1;
       const int lo = chunk_lo(q), hi = chunk_hi(q);
       // (the gates of chunk q were waited for by qt_part(q), earlier on this thread)
-      if (!cwait(&sh.bar_p[eq], (q >> 1) & 1)) return false;
+      if (!cwait_nf(&sh.bar_p[eq], (q >> 1) & 1)) return false;
       const float* ksc = sh.gates.ksc[eq];
       uint8_t* kt = sm + kslot(q);
       uint4 in[4];
