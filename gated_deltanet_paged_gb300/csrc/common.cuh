@@ -177,6 +177,14 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 // Wait until this thread's bulk stores are complete.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Programmatic dependent launch.  Kernels launched with programmatic stream
+// serialisation (gdn_host::launch_pdl) may start while the kernel before them on
+// the stream finishes; pdl_wait blocks until that kernel has completed and its
+// memory is visible (it returns at once for a plain launch), and
+// pdl_launch_dependents lets the next kernel on the stream begin launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -477,5 +485,23 @@ int encode_tiles_map_f16(CUtensorMap* map, const void* base, int64_t rows, int64
 int encode_tokens_map_32(CUtensorMap* map, const void* base, int64_t T, int64_t H, int64_t D);  // 64B swizzle
 
 inline int launch_status() { return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+// Launch as a programmatic dependent of the previous kernel on the stream (the
+// kernel calls pdl_wait before it reads anything that kernel may write).
+template <typename... Params, typename... Args>
+inline int launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                      Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
 
 }  // namespace gdn_host

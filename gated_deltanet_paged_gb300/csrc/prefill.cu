@@ -177,6 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.H;
   const int rank = blockIdx.x / H, h = blockIdx.x % H;
+  pdl_wait();  // the chunk-local kernel (and everything before it on the stream) is done
+  pdl_launch_dependents();
 
   // ---- pick the sequence: rank-th longest (ties by index) ----
   if (a.num_seqs > 1 && a.num_seqs < 4096) {
@@ -998,8 +1000,8 @@ int launch(PrefillArgs& a, const void* q, const void* k, const void* v, void* wo
     return GDN_ERR_CUDA;
   }
   const long long grid = static_cast<long long>(a.num_seqs) * a.H;
-  kernel<<<static_cast<unsigned>(grid), kThreads, SMEM_BYTES, stream>>>(mq, mk, mv, mt, mo, mw, a);
-  return gdn_host::launch_status();
+  return gdn_host::launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), SMEM_BYTES, stream, mq, mk,
+                              mv, mt, mo, mw, a);
 }
 
 int check_common(const gdn_bf16* q, const gdn_bf16* k, const gdn_bf16* v, const float* g, const float* beta,

@@ -16,6 +16,8 @@ __global__ void prefill_slots_kernel(const int32_t* __restrict__ cu_seqlens, con
                                      int32_t num_seqs, int32_t page_size, int32_t* __restrict__ state_indices,
                                      int32_t* __restrict__ output_state_indices,
                                      int32_t* __restrict__ checkpoint_cu_starts, int32_t* __restrict__ prefix_lens) {
+  gdn::pdl_wait();
+  gdn::pdl_launch_dependents();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= num_seqs) return;
   const int32_t i0 = indptr[b], i1 = indptr[b + 1];
@@ -45,6 +47,8 @@ __global__ void decode_slots_kernel(const int32_t* __restrict__ indptr, const in
                                     const int32_t* __restrict__ last_len, int32_t batch,
                                     int32_t* __restrict__ initial_state_indices,
                                     int32_t* __restrict__ output_state_indices) {
+  gdn::pdl_wait();
+  gdn::pdl_launch_dependents();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= batch) return;
   const int32_t i0 = indptr[b], i1 = indptr[b + 1];
@@ -74,10 +78,10 @@ extern "C" int gdn_paged_prefill_slots(const int32_t* cu_seqlens, const int32_t*
       !output_state_indices || !checkpoint_cu_starts || !prefix_lens)
     return GDN_ERR_INVALID_ARGUMENT;
   const int threads = 128;
-  prefill_slots_kernel<<<(num_seqs + threads - 1) / threads, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-      cu_seqlens, page_indptr, page_indices, last_page_len, num_seqs, page_size, state_indices,
-      output_state_indices, checkpoint_cu_starts, prefix_lens);
-  return gdn_host::launch_status();
+  return gdn_host::launch_pdl(prefill_slots_kernel, dim3((num_seqs + threads - 1) / threads), dim3(threads), 0,
+                              static_cast<cudaStream_t>(stream), cu_seqlens, page_indptr, page_indices,
+                              last_page_len, num_seqs, page_size, state_indices, output_state_indices,
+                              checkpoint_cu_starts, prefix_lens);
 }
 
 extern "C" int gdn_paged_decode_slots(const int32_t* page_indptr, const int32_t* page_indices,
@@ -89,7 +93,7 @@ extern "C" int gdn_paged_decode_slots(const int32_t* page_indptr, const int32_t*
   if (!page_indptr || !page_indices || !last_page_len || !initial_state_indices || !output_state_indices)
     return GDN_ERR_INVALID_ARGUMENT;
   const int threads = 128;
-  decode_slots_kernel<<<(batch + threads - 1) / threads, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-      page_indptr, page_indices, last_page_len, batch, initial_state_indices, output_state_indices);
-  return gdn_host::launch_status();
+  return gdn_host::launch_pdl(decode_slots_kernel, dim3((batch + threads - 1) / threads), dim3(threads), 0,
+                              static_cast<cudaStream_t>(stream), page_indptr, page_indices, last_page_len, batch,
+                              initial_state_indices, output_state_indices);
 }

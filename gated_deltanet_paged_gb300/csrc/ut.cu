@@ -115,6 +115,8 @@ __device__ __forceinline__ void solve32(const uint8_t* blk, int c, float (&x)[32
 // Chunk slot -> {first token of its 64 rows, lo, hi, sequence}; hi <= lo (and
 // sequence -1) when the slot holds no chunk.
 __global__ void slot_map_kernel(const PrefillArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= a.num_slots) return;
   int lo = 0, hi = a.num_seqs - 1;
@@ -186,6 +188,10 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     }
   };
 
+  pdl_wait();  // the slot map (and everything before it on the stream) is done
+  // No early pdl_launch_dependents here: the state chain that follows would
+  // then take SMs one by one as this kernel drains, and that placement made it
+  // 13% slower (measured); it launches when this kernel completes.
   int it = blockIdx.x;
   if (tid == 0) {
     mbar_init(&sh.bar_tma, 1);
@@ -521,7 +527,8 @@ namespace host {
 
 int launch_chunk_inverse(const PrefillArgs& a, const void* k, cudaStream_t stream) {
   if (a.num_seqs == 0 || a.num_slots == 0) return GDN_OK;
-  slot_map_kernel<<<(a.num_slots + 255) / 256, 256, 0, stream>>>(a);
+  int rc = gdn_host::launch_pdl(slot_map_kernel, dim3((a.num_slots + 255) / 256), dim3(256), 0, stream, a);
+  if (rc != GDN_OK) return rc;
   CUtensorMap mk, mt, mw;
   const int64_t rows = static_cast<int64_t>(a.num_slots) * a.H * 64;
   if (gdn_host::encode_tokens_map(&mk, k, a.T, a.H, kDimK) != GDN_OK ||
@@ -540,8 +547,7 @@ int launch_chunk_inverse(const PrefillArgs& a, const void* k, cudaStream_t strea
     return GDN_ERR_CUDA;
   const long long items = static_cast<long long>((a.num_slots + 1) / 2) * a.H;
   const unsigned grid = static_cast<unsigned>(items < 3LL * num_sms ? items : 3LL * num_sms);
-  ut_kernel<<<grid, kUtThreads, UT_SMEM, stream>>>(mk, mt, mw, a);
-  return gdn_host::launch_status();
+  return gdn_host::launch_pdl(ut_kernel, dim3(grid), dim3(kUtThreads), UT_SMEM, stream, mk, mt, mw, a);
 }
 
 }  // namespace host
