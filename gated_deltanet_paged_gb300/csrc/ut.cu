@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     load_gb(nit, b ^ 1);  // in flight during this item
 
     // K -> K^ = diag(gamma) K in fp16, in place (the first MMA has read K), in two
-    // halves done while the two small MMA rounds run.  Each batch loads its four
+    // halves done while the two small MMA products run.  Each batch loads its four
     // 16-byte pieces and their gamma values before any store (a store could alias
     // a later load, so the compiler would otherwise wait for every load in turn).
     auto khat_half = [&](int part) {
@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     __syncthreads();  // every read of the fp32 blocks is done: the space becomes T_d
     // T_d is kept by columns (tile row j = column j of T_d, 64 rows t in 128
     // bytes), so each thread writes its solved column with four 16-byte stores.
-    // Only the diagonal blocks are written: the rounds below read the blocks
+    // Only the diagonal blocks are written: the products below read the blocks
     // off the diagonal only into products that are discarded.
     const int jcol = 32 * bk + lane;
     if (ok) {
@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     if (ok && bk == 1) {  // rows 32-63 of each chunk -> rows 32 h + i of the N21 stack
       float d[32];
       tmem_ld32(lane_addr + r0, d);
-      uint8_t* nt = sm + XB + 16384;  // over A21, which round 1 has read
+      uint8_t* nt = sm + XB + 16384;  // over A21, which the first small product has read
       const int nr = 32 * half + lane;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
