@@ -811,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) bulk_wait_read();  // this warp's last output store has read the block
       __syncwarp();
       const int v0 = 32 * wq;
-      if constexpr (kBf16) {  // nearest bf16, ties to even; 2 rounds of 16 rows x 128 B
+      if constexpr (kBf16) {  // nearest bf16, ties to even; 2 passes of 16 rows x 128 B
         __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(pool);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
@@ -834,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {  // 4 rounds of 8 rows x 256 B
+        for (int r = 0; r < 4; ++r) {  // 4 passes of 8 rows x 256 B
           if ((lane >> 3) == r) {
             const int rr = lane & 7;
 #pragma unroll
