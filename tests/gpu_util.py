@@ -91,7 +91,11 @@ def check_pool(pool_after, pool_before, ref_pool, written, errs, label="pool"):
 
 def prefill_paged_both(call, pool_gpu, pool_ora, errs, use_slots=False, scale=SCALE):
     """One paged prefill call on the GPU and in the oracle; compares
-    everything.  pool_gpu (device) and pool_ora (host) are updated in place."""
+    everything.  pool_gpu (device) and pool_ora (host) are updated in place.
+    The call runs twice: with an error word (the kernels built with the device
+    checks), compared with the oracle, and without one (the kernels built
+    without them, the ones a caller without an error word gets), which must give
+    the same bits."""
     dev = lambda t: t.cuda().contiguous()
     cu, ip, pi, lpl = dev(call.cu_seqlens), dev(call.page_indptr), dev(call.page_indices), dev(call.last_page_len)
     slots = gdn.gdn_paged_prefill_slots(cu, ip, pi, lpl, call.page_size)
@@ -101,11 +105,18 @@ def prefill_paged_both(call, pool_gpu, pool_ora, errs, use_slots=False, scale=SC
         assert (slots[k].cpu().numpy() == v).all(), "slot %s differs" % k
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     before = pool_gpu.clone()
+    pool_fast = pool_gpu.clone()
     o = gdn.gdn_chunk_gated_delta_rule_paged(dev(call.q), dev(call.k), dev(call.v), dev(call.g), dev(call.beta),
                                              cu, pool_gpu, pi, ip, call.page_size, lpl, scale=scale,
                                              slots=slots if use_slots else None, err_word=err)
+    o_fast = gdn.gdn_chunk_gated_delta_rule_paged(dev(call.q), dev(call.k), dev(call.v), dev(call.g), dev(call.beta),
+                                                  cu, pool_fast, pi, ip, call.page_size, lpl, scale=scale,
+                                                  slots=slots if use_slots else None)
     torch.cuda.synchronize()
     assert int(err.item()) == 0, "device error word %#x" % int(err.item())
+    assert torch.equal(o.view(torch.int16), o_fast.view(torch.int16)), "outputs differ without the error word"
+    assert bits_equal(pool_gpu, pool_fast), "pool differs without the error word"
+    del pool_fast
     o_ref, written = oracle.chunk_gated_delta_rule_paged(
         bf16_bits(call.q), bf16_bits(call.k), bf16_bits(call.v), f32(call.g), f32(call.beta), i32(call.cu_seqlens),
         pool_ora, i32(call.page_indices), i32(call.page_indptr), call.page_size, i32(call.last_page_len), scale)
