@@ -421,7 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem + COL_DX + 128 * e;
         const uint32_t ua = d + 64 * e;         // U half
         const uint32_t od = d + 64 * (1 - e);  // O half
-        if (!w(&sh.xa_full, e) || !w(&sh.s16_ready, e) || !w(&sh.bar_w[e], ph) || !w(&sh.bar_m2[e], ph)) {
+        // the state copy (s16_ready) is normally the last of these to complete
+        if (!w(&sh.bar_w[e], ph) || !w(&sh.bar_m2[e], ph) || !w(&sh.xa_full, e) || !w(&sh.s16_ready, e)) {
           *abort_flag = 1;
           break;
         }
@@ -440,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tma_q(c + 2);
         }
-        if (!w(&sh.u_ready, e) || !w(&sh.kt_ready[e], ph)) {
+        if (!w(&sh.kt_ready[e], ph) || !w(&sh.u_ready, e)) {  // U^T (u_ready) is normally last
           *abort_flag = 1;
           break;
         }
