@@ -619,9 +619,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // 3. P = decayed, masked Q K^T (warps 8-11, a thread per row and half) once U^T P^T of chunk p-2
       //    has read this P tile; warps other than 8 read its gate tables
-      if (tm_reader && pwait(&sh.bar_p[e], (p >> 1) & 1) &&
-          (p < 2 || pwait(&sh.bar_o[e], ((p - 2) >> 1) & 1)) &&
-          (pw == 0 || pwait(&sh.gates_ready[e], (p >> 1) & 1))) {
+      if (tm_reader && (p < 2 || pwait_nf(&sh.bar_o[e], ((p - 2) >> 1) & 1)) &&
+          (pw == 0 || pwait_nf(&sh.gates_ready[e], (p >> 1) & 1)) &&
+          pwait(&sh.bar_p[e], (p >> 1) & 1)) {  // one tcgen05 fence, after the last wait, before the TMEM load
         const int t = 16 * wq + (lane & 15), ph = lane >> 4;  // row t, columns 32 ph ..
         float x[32];
         tmem_ld16x32bx2_32(lane_addr + COL_DP, x);
