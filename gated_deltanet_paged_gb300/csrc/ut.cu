@@ -370,14 +370,16 @@ __global__ void __launch_bounds__(kUtThreads, 3)
       // (columns 32-63 of the A21 tile only feed products that are discarded)
     }
     fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
+    // A warp solves the diagonal block whose rows it wrote itself (warp w: chunk
+    // w / 2, rows 32 (w % 2) .. + 31), so a warp barrier is enough here; the
+    // CTA-wide one before the first small product orders the rest.
+    __syncwarp();
 
     // ---- T_d: thread (chunk, block bk, column c) solves column c of block bk ----
     const int bk = warp & 1;
     float x[32];
     if (ok) solve32(sm + XB + half * 8192 + bk * 32 * 128, lane, x);
-    __syncthreads();  // every read of the fp32 blocks is done: the space becomes T_d
+    __syncwarp();  // every lane has read this warp's block: the space becomes its T_d columns
     // T_d is kept by columns (tile row j = column j of T_d, 64 rows t in 128
     // bytes), so each thread writes its solved column with four 16-byte stores.
     // Only the diagonal blocks are written: the products below read the blocks
