@@ -317,12 +317,14 @@ __global__ void __launch_bounds__(kUtThreads, 3)
         sh.flag = 1;
       }
     }
-    __syncthreads();
-    ok = sh.flag == 0;
     if (!(va || vb)) {  // no chunk in either slot: nothing to compute or store
+      __syncthreads();
+      ok = sh.flag == 0;
       if (ok && tid == 0 && nit < nitems) issue_k(nit, b ^ 1, XB);
       continue;
     }
+    // (if thread 0's wait for K ran out, the product was never committed: every
+    // thread's wait below runs out too, and the barrier inside reports it)
     ok = ok && wait_mma();
 
     // ---- row t of A: the diagonal block part in fp32, A21 in fp16 ----
