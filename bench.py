@@ -42,9 +42,9 @@ DECODE_BYTES_PER_SEQ_HEAD = 2 * STATE_BYTES + 2 * (2 * K + 2 * V) + 8   # 132,10
 DECODE_BF16_BYTES_PER_SEQ_HEAD = 2 * (V * K * 2) + 2 * (2 * K + 2 * V) + 8   # 66,568: bf16 state pool
 
 # DRAM bytes (read + write) of one paged prefill call per new token, over all heads:
-# ncu capture of the 4 x 8192-token case (ut_kernel 0.622 GB + prefill_kernel 1.516 GB
+# ncu capture of the 4 x 8192-token case (ut_kernel 0.621 GB + prefill_kernel 1.516 GB
 # for 32,768 tokens); the traffic grows in proportion to the tokens.
-PREFILL_TRAFFIC_PER_TOKEN = 2.138e9 / 32768
+PREFILL_TRAFFIC_PER_TOKEN = 2.137e9 / 32768
 TRAFFIC_SOURCE = "ncu dram__bytes_read+write of 4x8192-token call, scaled by tokens"
 PREFILL = dict(S=4, L=65536, H=32, page_size=1152, num_pages=256)
 DECODE = dict(B=256, H=32, page_size=1024, num_pages=10000)
