@@ -453,10 +453,12 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
 }
+__device__ __forceinline__ uint32_t pack_half2(float2 x) { return pack_half2(x.x, x.y); }
 __device__ __forceinline__ uint32_t pack_bf162(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
 }
+__device__ __forceinline__ uint32_t pack_bf162(float2 x) { return pack_bf162(x.x, x.y); }
 __device__ __forceinline__ float2 unpack_bf162(uint32_t u) {
   __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&u);
   return __bfloat1622float2(h);

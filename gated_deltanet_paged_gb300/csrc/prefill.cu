@@ -140,7 +140,8 @@ __device__ __forceinline__ void cvt8(uint8_t* dst, const uint8_t* src, float sc,
   *reinterpret_cast<uint4*>(dst) = out;
 }
 
-// The same on a loaded piece, returning the converted one.
+// The same on a loaded piece, returning the converted one; the products run as
+// paired fp32 multiplies (each half rounds as a scalar multiply would).
 __device__ __forceinline__ uint4 cvt8v(const uint4 in, float sc, bool keep, bool check, bool& bad) {
   uint4 out = make_uint4(0u, 0u, 0u, 0u);
   if (keep) {
@@ -150,10 +151,11 @@ __device__ __forceinline__ uint4 cvt8v(const uint4 in, float sc, bool keep, bool
                             fmaxf(fmaxf(fabsf(f2.x), fabsf(f2.y)), fmaxf(fabsf(f3.x), fabsf(f3.y))));
       bad |= !(m <= kF16Max);  // NaN inputs too
     }
-    out.x = pack_half2(f0.x * sc, f0.y * sc);
-    out.y = pack_half2(f1.x * sc, f1.y * sc);
-    out.z = pack_half2(f2.x * sc, f2.y * sc);
-    out.w = pack_half2(f3.x * sc, f3.y * sc);
+    const float2 s2 = make_float2(sc, sc);
+    out.x = pack_half2(__fmul2_rn(f0, s2));
+    out.y = pack_half2(__fmul2_rn(f1, s2));
+    out.z = pack_half2(__fmul2_rn(f2, s2));
+    out.w = pack_half2(__fmul2_rn(f3, s2));
   }
   return out;
 }
@@ -882,8 +884,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int hh = 0; hh < 2; ++hh) {
         float su[32];
         tmem_ld32(lane_addr + COL_DSU + 64 * hc + 32 * hh, su);
+        const float2 g2 = make_float2(gamC, gamC);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) S[32 * hh + i] = fmaf(gamC, S[32 * hh + i], su[i]);
+        for (int i = 0; i < 16; ++i) {  // paired fp32 FMAs
+          const float2 r = __ffma2_rn(g2, make_float2(S[32 * hh + 2 * i], S[32 * hh + 2 * i + 1]),
+                                      make_float2(su[2 * i], su[2 * i + 1]));
+          S[32 * hh + 2 * i] = r.x;
+          S[32 * hh + 2 * i + 1] = r.y;
+        }
       }
       stage_state();
       mbar_arrive(&sh.s16_ready);
@@ -914,7 +922,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* stg = sm + OFF_OST + warp * 2048;
           if (lane == 0) bulk_wait_read();  // this warp's previous store has read the block
           __syncwarp();
-          const float sc = a.scale;
+          const float2 sc2 = make_float2(a.scale, a.scale);
           const int mi = lane >> 3, k = lane & 7;  // this thread's row address: matrix mi, row k
 #pragma unroll
           for (int g = 0; g < 2; ++g) {
@@ -924,9 +932,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int q = 0; q < 2; ++q) {
                 const int j = 2 * jj + q;  // tokens 8 j .. 8 j + 7
-                m[2 * q] = pack_bf162(sc * __uint_as_float(f[g][4 * j]), sc * __uint_as_float(f[g][4 * j + 1]));
-                m[2 * q + 1] =
-                    pack_bf162(sc * __uint_as_float(f[g][4 * j + 2]), sc * __uint_as_float(f[g][4 * j + 3]));
+                m[2 * q] = pack_bf162(
+                    __fmul2_rn(sc2, make_float2(__uint_as_float(f[g][4 * j]), __uint_as_float(f[g][4 * j + 1]))));
+                m[2 * q + 1] = pack_bf162(
+                    __fmul2_rn(sc2, make_float2(__uint_as_float(f[g][4 * j + 2]), __uint_as_float(f[g][4 * j + 3]))));
               }
               // matrix mi: tokens 8 (2 jj + mi / 2) .., rows v 16 g + 8 (mi % 2) ..
               const int t = 8 * (2 * jj + (mi >> 1)) + k;

@@ -28,8 +28,8 @@
 //                             both the staging of the T'' stores and the
 //                             (M-major) A operand of W: a thread writes its column
 //                             with 16-byte stores
-//   W = [T''_a; 0] K^_a + [0; T''_b] K^_b,  K^ = diag(gamma) K converted to fp16
-//                             in place once the first MMA has read K
+//   -W = [T''_a; 0] K^_a + [0; T''_b] K^_b,  K^ = -diag(gamma) K converted to
+//                             fp16 in place once the first MMA has read K
 // The per-chunk B operands sit side by side ([X_a | X_b], N = 128) so one MMA
 // serves both chunks (the off-diagonal result blocks are unused).
 #include <math.h>
@@ -82,6 +82,15 @@ __device__ __forceinline__ uint4 pack8h(const float* x) {
   u.w = pack_half2(x[6], x[7]);
   return u;
 }
+// The same of x times s (paired fp32 multiplies).
+__device__ __forceinline__ uint4 pack8h2(const float* x, float2 s) {
+  uint4 u;
+  u.x = pack_half2(__fmul2_rn(make_float2(x[0], x[1]), s));
+  u.y = pack_half2(__fmul2_rn(make_float2(x[2], x[3]), s));
+  u.z = pack_half2(__fmul2_rn(make_float2(x[4], x[5]), s));
+  u.w = pack_half2(__fmul2_rn(make_float2(x[6], x[7]), s));
+  return u;
+}
 
 // Byte offset of floats 4q..4q+3 (q < 8) of row r of a chunk's fp32 diagonal
 // blocks (rows of 128 B; float4 q of row r sits at q ^ (r % 8), so a warp
@@ -92,22 +101,27 @@ __device__ __forceinline__ uint32_t af(int r, int q) { return r * 128 + ((q ^ (r
 // starts at blk (rows 128 B apart, the swizzle of af):
 //   x_t = [t = c] - sum_{j<t} B[t][j] x_j.
 // Every thread reads the same row at the same time (broadcast); four partial
-// sums keep the FMA chains short.
+// sums (j mod 4) keep the FMA chains short, and run as two paired fp32 FMAs
+// where both halves of a pair have a term (each half rounds as a scalar FMA).
 __device__ __forceinline__ void solve32(const uint8_t* blk, int c, float (&x)[32]) {
 #pragma unroll
   for (int t = 0; t < 32; ++t) {
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
       if (4 * m < t) {
         const float4 a4 = *reinterpret_cast<const float4*>(blk + af(t, m));
-        s0 = fmaf(a4.x, x[4 * m], s0);
-        if (4 * m + 1 < t) s1 = fmaf(a4.y, x[4 * m + 1], s1);
-        if (4 * m + 2 < t) s2 = fmaf(a4.z, x[4 * m + 2], s2);
-        if (4 * m + 3 < t) s3 = fmaf(a4.w, x[4 * m + 3], s3);
+        if (4 * m + 1 < t)
+          s01 = __ffma2_rn(make_float2(a4.x, a4.y), make_float2(x[4 * m], x[4 * m + 1]), s01);
+        else
+          s01.x = fmaf(a4.x, x[4 * m], s01.x);
+        if (4 * m + 3 < t)
+          s23 = __ffma2_rn(make_float2(a4.z, a4.w), make_float2(x[4 * m + 2], x[4 * m + 3]), s23);
+        else if (4 * m + 2 < t)
+          s23.x = fmaf(a4.z, x[4 * m + 2], s23.x);
       }
     }
-    const float s = (s0 + s1) + (s2 + s3);
+    const float s = (s01.x + s01.y) + (s23.x + s23.y);
     x[t] = t > c ? -s : (t == c ? 1.f : 0.f);
   }
 }
@@ -267,10 +281,11 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     sh.gam[tid] = __expf(s);
     load_gb(nit, b ^ 1);  // in flight during this item
 
-    // K -> K^ = diag(gamma) K in fp16, in place (the first MMA has read K), in two
-    // halves done while the two small MMA products run.  Each batch loads its four
-    // 16-byte pieces and their gamma values before any store (a store could alias
-    // a later load, so the compiler would otherwise wait for every load in turn).
+    // K -> K^ = -diag(gamma) K in fp16, in place (the first MMA has read K), in two
+    // halves done while the two small MMA products run; its sign makes the W
+    // product come out as -W.  Each batch loads its four 16-byte pieces and their
+    // gamma values before any store (a store could alias a later load, so the
+    // compiler would otherwise wait for every load in turn).
     auto khat_half = [&](int part) {
       const int lo0 = ga.y, hi0 = ga.z, lo1 = gb.y, hi1 = gb.z;
       for (int i0 = tid + 1024 * part; i0 < 1024 * (part + 1); i0 += 4 * kUtThreads) {
@@ -280,7 +295,7 @@ __global__ void __launch_bounds__(kUtThreads, 3)
         for (int k = 0; k < 4; ++k) {
           const int i = i0 + k * kUtThreads;
           in[k] = *reinterpret_cast<const uint4*>(sm + KB + i * 16);
-          gr[k] = sh.gam[((i >> 9) & 1) * 64 + ((i & 511) >> 3)];
+          gr[k] = -sh.gam[((i >> 9) & 1) * 64 + ((i & 511) >> 3)];
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -289,13 +304,11 @@ __global__ void __launch_bounds__(kUtThreads, 3)
           const bool keep = hh ? (row >= lo1 && row < hi1) : (row >= lo0 && row < hi0);
           uint4 out = make_uint4(0u, 0u, 0u, 0u);
           if (keep) {
-            const float g = gr[k];
-            const float2 f0 = unpack_bf162(in[k].x), f1 = unpack_bf162(in[k].y), f2 = unpack_bf162(in[k].z),
-                         f3 = unpack_bf162(in[k].w);
-            out.x = pack_half2(f0.x * g, f0.y * g);
-            out.y = pack_half2(f1.x * g, f1.y * g);
-            out.z = pack_half2(f2.x * g, f2.y * g);
-            out.w = pack_half2(f3.x * g, f3.y * g);
+            const float2 g2 = make_float2(gr[k], gr[k]);
+            out.x = pack_half2(__fmul2_rn(unpack_bf162(in[k].x), g2));
+            out.y = pack_half2(__fmul2_rn(unpack_bf162(in[k].y), g2));
+            out.z = pack_half2(__fmul2_rn(unpack_bf162(in[k].z), g2));
+            out.w = pack_half2(__fmul2_rn(unpack_bf162(in[k].w), g2));
           }
           *reinterpret_cast<uint4*>(sm + KB + i * 16) = out;
         }
@@ -346,7 +359,8 @@ __global__ void __launch_bounds__(kUtThreads, 3)
           float eb[16];
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) eb[jj] = sh.e[r0 + 16 * q + jj];
-          float cur = bv * __expf(Gt - sh.G[r0 + jstart]);
+          // (A21 is kept negated, so that the first small product gives N21 itself)
+          float cur = (lower && q < 2 ? -bv : bv) * __expf(Gt - sh.G[r0 + jstart]);
 #pragma unroll
           for (int jj = 15; jj >= 0; --jj) {
             const int j = 16 * q + jj;
@@ -396,8 +410,8 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     tc_fence_before();
     __syncthreads();
 
-    // ---- N21 = -T22 A21: [T_d,a; T_d,b] (K = 32..63; by columns, so M-major) x
-    //      [A21_a | A21_b]; the first half of K^ while it runs ----
+    // ---- N21 = -T22 A21 = T22 (-A21): [T_d,a; T_d,b] (K = 32..63; by columns, so
+    //      M-major) x [-A21_a | -A21_b]; the first half of K^ while it runs ----
     if (ok && tid == 0) {
       tc_fence_after();
       tc_mma2(tmem, dMN(XB + 32 * 128, 8192), 128, dMN(XB + 16384, 4096), 128, id_mnAB, 0);
@@ -411,12 +425,7 @@ __global__ void __launch_bounds__(kUtThreads, 3)
       uint8_t* nt = sm + XB + 16384;  // over A21, which the first small product has read
       const int nr = 32 * half + lane;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float nv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) nv[i] = -d[8 * cc + i];
-        *reinterpret_cast<uint4*>(nt + swz(nr, cc)) = pack8h(nv);
-      }
+      for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint4*>(nt + swz(nr, cc)) = pack8h(&d[8 * cc]);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -440,13 +449,9 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     if (ok) {
       uint8_t* tile = sm + XB + half * 16384;
       const float bc = sh.bet[tid];
+      const float2 bc2 = make_float2(bc, bc);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = x[8 * q + i] * bc;
-        *reinterpret_cast<uint4*>(tile + swz(jcol, 4 * bk + q)) = pack8h(v);
-      }
+      for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(tile + swz(jcol, 4 * bk + q)) = pack8h2(&x[8 * q], bc2);
       if (bk == 1) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(tile + swz(jcol, q)) = make_uint4(0u, 0u, 0u, 0u);
@@ -454,12 +459,7 @@ __global__ void __launch_bounds__(kUtThreads, 3)
         float d[32];
         tmem_ld32(lane_addr + 32 * half, d);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float v[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = d[8 * q + i] * bc;
-          *reinterpret_cast<uint4*>(tile + swz(jcol, 4 + q)) = pack8h(v);
-        }
+        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(tile + swz(jcol, 4 + q)) = pack8h2(&d[8 * q], bc2);
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k)
@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     tc_fence_before();
     __syncthreads();
 
-    // ---- W = [T''_a; 0] K^_a + [0; T''_b] K^_b;  T'' tiles -> workspace ----
+    // ---- -W = [T''_a; 0] K^_a + [0; T''_b] K^_b;  T'' tiles -> workspace ----
     if (ok && tid == 0) {
       tc_fence_after();
       tc_mma4(tmem, dMN(XB, kTile), 128, dMN(KB, 16384), 128, id_mnAB, 0);
@@ -493,12 +493,7 @@ __global__ void __launch_bounds__(kUtThreads, 3)
         tmem_ld64(lane_addr + 64 * hh, w);
         uint8_t* box = sm + KB + half * 16384 + hh * kTile;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          float nw[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) nw[i] = -w[8 * c + i];
-          *reinterpret_cast<uint4*>(box + swz(t, c)) = pack8h(nw);
-        }
+        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(box + swz(t, c)) = pack8h(&w[8 * c]);
       }
     }
     fence_proxy_async();
