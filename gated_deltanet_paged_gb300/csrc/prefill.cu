@@ -631,12 +631,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j0 = 32 * ph;
         const int jmax = min(j0 + 31, t);
         if (t >= lo && t < hi && jmax >= j0) {
+          // exp(G_t - G_j) by a running product downwards from j = jmax; the
+          // products with Q K^T in pairs (paired fp32 multiplies)
+          float ev[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 e4 = *reinterpret_cast<const float4*>(&gs.e[j0 + 4 * i]);
+            ev[4 * i] = e4.x;
+            ev[4 * i + 1] = e4.y;
+            ev[4 * i + 2] = e4.z;
+            ev[4 * i + 3] = e4.w;
+          }
           float cur = __expf(gs.G[t] - gs.G[jmax]);
 #pragma unroll
-          for (int jj = 31; jj >= 0; --jj) {
-            const int j = j0 + jj;
-            out[jj] = (j <= jmax && j >= lo) ? cur * x[jj] : 0.f;
-            if (j <= jmax) cur *= gs.e[j];
+          for (int i = 15; i >= 0; --i) {
+            const int ja = j0 + 2 * i, jb = ja + 1;
+            const float cb = cur;
+            if (jb <= jmax) cur *= ev[2 * i + 1];
+            const float ca = cur;
+            if (ja <= jmax) cur *= ev[2 * i];
+            const float2 pr = __fmul2_rn(make_float2(ca, cb), make_float2(x[2 * i], x[2 * i + 1]));
+            out[2 * i] = (ja <= jmax && ja >= lo) ? pr.x : 0.f;
+            out[2 * i + 1] = (jb <= jmax && jb >= lo) ? pr.y : 0.f;
           }
         } else {
 #pragma unroll

@@ -362,11 +362,15 @@ __global__ void __launch_bounds__(kUtThreads, 3)
           // (A21 is kept negated, so that the first small product gives N21 itself)
           float cur = (lower && q < 2 ? -bv : bv) * __expf(Gt - sh.G[r0 + jstart]);
 #pragma unroll
-          for (int jj = 15; jj >= 0; --jj) {
-            const int j = 16 * q + jj;
-            const bool in = (j <= jstart) && (j >= lo);
-            out[jj] = in ? cur * kk[j] : 0.f;
-            if (j <= jstart) cur *= eb[jj];
+          for (int i = 7; i >= 0; --i) {  // a running product downwards from jstart; products in pairs
+            const int ja = 16 * q + 2 * i, jb = ja + 1;
+            const float cb = cur;
+            if (jb <= jstart) cur *= eb[2 * i + 1];
+            const float ca = cur;
+            if (ja <= jstart) cur *= eb[2 * i];
+            const float2 pr = __fmul2_rn(make_float2(ca, cb), make_float2(kk[ja], kk[jb]));
+            out[2 * i] = (ja <= jstart && ja >= lo) ? pr.x : 0.f;
+            out[2 * i + 1] = (jb <= jstart && jb >= lo) ? pr.y : 0.f;
           }
         } else {
 #pragma unroll
