@@ -1007,6 +1007,7 @@ int launch(PrefillArgs& a, const void* q, const void* k, const void* v, void* wo
   if (rc != GDN_OK) return rc;
   a.num_slots = static_cast<int32_t>(ns);
   a.slot_geo = static_cast<int4*>(workspace);
+  a.item_counter = reinterpret_cast<int32_t*>(a.slot_geo + ns);
   a.tinv = reinterpret_cast<__half*>(static_cast<uint8_t*>(workspace) + workspace_map_bytes(ns));
   a.wneg = a.tinv + ns * a.H * (kTinvBytes / 2);
   rc = host::launch_chunk_inverse(a, k, stream);

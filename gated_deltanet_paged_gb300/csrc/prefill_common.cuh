@@ -47,6 +47,7 @@ struct PrefillArgs {
   // tile T'' = (I + A)^-1 diag(beta) and a 64 x 128 fp16 tile
   // -W = -T'' diag(gamma) K.
   int4* slot_geo;
+  int32_t* item_counter;  // the chunk-local kernel's work counter (after the map; zeroed by the slot map)
   __half* tinv;
   __half* wneg;
   int32_t num_slots;
@@ -66,8 +67,9 @@ __device__ inline int slot_base(int cu_b, int b) { return cu_b / 64 + 2 * b; }
 constexpr uint32_t kTinvBytes = 64 * 64 * 2;  // one T'' tile
 constexpr uint32_t kWBytes = 64 * 128 * 2;    // one -W tile
 
+// The map (16 bytes per slot) and the work counter (16 bytes), rounded up to 1 KB.
 __host__ __device__ inline size_t workspace_map_bytes(int64_t num_slots) {
-  return static_cast<size_t>((num_slots * 16 + 1023) / 1024 * 1024);
+  return static_cast<size_t>((num_slots * 16 + 16 + 1023) / 1024 * 1024);
 }
 __host__ __device__ inline size_t workspace_bytes(int64_t T, int64_t num_seqs, int64_t H) {
   const int64_t ns = num_chunk_slots(T, num_seqs);

@@ -70,6 +70,7 @@ struct UtSmall {
   uint64_t bar_tma, bar_mma;
   uint32_t tmem_base;
   int4 geo[2][2];  // [item parity][chunk]: first token, lo, hi, sequence of the chunk slot
+  int next_it[2];  // [item parity]: the item after this one
   int flag;
 };
 constexpr uint32_t UT_SMEM = UT_SMALL + ((sizeof(UtSmall) + 127) / 128) * 128 + 1024;
@@ -152,6 +153,7 @@ __global__ void slot_map_kernel(const PrefillArgs a) {
     }
   }
   a.slot_geo[s] = out;
+  if (s == 0) *a.item_counter = 0;
 }
 
 __global__ void __launch_bounds__(kUtThreads, 3)
@@ -165,10 +167,12 @@ __global__ void __launch_bounds__(kUtThreads, 3)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int half = tid >> 6, t = tid & 63, r0 = half * 64;
   const int H = a.H;
-  // Work items (pair of chunk slots, head), item = pair * H + head, taken in
-  // strides of the grid by persistent CTAs.  The two 32 KB regions swap roles
-  // from one item to the next (K of item i -> the A tiles of item i+1), so the
-  // next item's K is loaded while this one finishes.
+  // Work items (pair of chunk slots, head), item = pair * H + head, taken by
+  // persistent CTAs: items b and b + grid by CTA b, the rest one at a time from
+  // a counter (item 2 grid + counter), so that CTAs on faster SMs take more
+  // items and all finish together.  The two 32 KB regions swap roles from one
+  // item to the next (K of item i -> the A tiles of item i+1), so the next
+  // item's K is loaded while this one finishes.
   const int nitems = ((a.num_slots + 1) / 2) * H;
 
   // Geometry of item it's two chunk slots into geo[b] (threads t == 0).
@@ -211,6 +215,7 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     mbar_init(&sh.bar_tma, 1);
     mbar_init(&sh.bar_mma, 1);
     sh.flag = 0;
+    sh.next_it[0] = it + gridDim.x;
     fence_mbar_init();
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_t);
@@ -251,14 +256,24 @@ __global__ void __launch_bounds__(kUtThreads, 3)
   };
 
   bool ok = true;
-  for (int i = 0; it < nitems && ok; ++i, it += gridDim.x) {
+  for (int i = 0; it < nitems && ok; ++i) {
     const int b = i & 1;
     const uint32_t KB = (i & 1) ? 0u : UT_REGION;  // K, then K^, then the -W staging
     const uint32_t XB = UT_REGION - KB;            // A blocks, T_d, A21 -> N21, then the T'' tiles
-    const int pair = it / H, h = it % H, nit = it + gridDim.x;
+    const int pair = it / H, h = it % H, nit = sh.next_it[b];
+    // the item after the next one (warp 1 waits for the counter only at the
+    // end of this item, where it publishes the number for the next)
+    int grabbed = 0;
+    auto grab = [&]() {
+      if (tid == 32 && nit < nitems) grabbed = atomicAdd(a.item_counter, 1);
+    };
+    auto publish_next = [&]() {
+      if (tid == 32) sh.next_it[b ^ 1] = nit < nitems ? 2 * static_cast<int>(gridDim.x) + grabbed : nitems;
+    };
     const int4 ga = sh.geo[b][0], gb = sh.geo[b][1];
     const bool va = ga.z > ga.y, vb = gb.z > gb.y;
     const int lo = half ? gb.y : ga.y, hi = half ? gb.z : ga.z;
+    if (va || vb) grab();
     if (t == 0) load_geo(nit, b ^ 1);
 
     // Gates of this row; inclusive scan over the chunk's 64 rows.
@@ -331,9 +346,12 @@ __global__ void __launch_bounds__(kUtThreads, 3)
       }
     }
     if (!(va || vb)) {  // no chunk in either slot: nothing to compute or store
+      grab();
+      publish_next();
       __syncthreads();
       ok = sh.flag == 0;
       if (ok && tid == 0 && nit < nitems) issue_k(nit, b ^ 1, XB);
+      it = nit;
       continue;
     }
     // (if thread 0's wait for K ran out, the product was never committed: every
@@ -501,7 +519,9 @@ __global__ void __launch_bounds__(kUtThreads, 3)
       }
     }
     fence_proxy_async();
+    publish_next();
     __syncthreads();
+    it = nit;
     if (tid == 0) {
       if (ok)
         for (int hh = 0; hh < 2; ++hh)

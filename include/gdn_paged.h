@@ -316,8 +316,8 @@ int gdn_pool_zero_rows(void *pool, int64_t row_bytes, int64_t pool_row_stride_by
  * rule (A[t][j] = beta_t exp(G_t - G_j) k_t . k_j, j < t) and
  * -W = -T'' diag(exp(G)) K, and stores them as 64 x 64 and 64 x 128 fp16
  * tiles; the sequential state chain then reads them back.  The workspace holds
- * 16 bytes per chunk slot (rounded up to 1 KB) and 24 KB per (chunk slot,
- * head), with
+ * 16 bytes per chunk slot plus 16 (rounded up to 1 KB) and 24 KB per (chunk
+ * slot, head), with
  * total_tokens / 64 + 2 num_seqs + 2 chunk slots. */
 size_t gdn_prefill_workspace_bytes(int32_t num_seqs, int32_t total_tokens, int32_t H);
 

@@ -39,7 +39,7 @@ def test_status_strings_and_workspace():
     # 16 bytes per chunk slot (padded to 1 KB) + per (slot, head) a 64 x 64 and a 64 x 128
     # fp16 tile; slots = T / 64 + 2 S + 2
     slots = 100000 // 64 + 2 * 64 + 2
-    assert lib.gdn_prefill_workspace_bytes(64, 100000, 32) == (slots * 16 + 1023) // 1024 * 1024 + slots * 32 * 24576
+    assert lib.gdn_prefill_workspace_bytes(64, 100000, 32) == (slots * 16 + 16 + 1023) // 1024 * 1024 + slots * 32 * 24576
     assert lib.gdn_prefill_workspace_bytes(-1, 10, 2) == 0
 
 
