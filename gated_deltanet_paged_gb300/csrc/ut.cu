@@ -333,7 +333,6 @@ __global__ void __launch_bounds__(kUtThreads, 3)
 
     // ---- [K_a; K_b] [K_a; K_b]^T ----
     if (tid == 0) {
-      bulk_wait_read();  // the previous item's -W stores have read this item's A-tile region
       if (mbar_wait(&sh.bar_tma, i & 1)) {
         tc_fence_after();
         if (va || vb) {
@@ -344,6 +343,9 @@ __global__ void __launch_bounds__(kUtThreads, 3)
       } else {
         sh.flag = 1;
       }
+      // the previous item's -W stores have read this item's A-tile region
+      // (written after the barrier of the product's wait)
+      bulk_wait_read();
     }
     if (!(va || vb)) {  // no chunk in either slot: nothing to compute or store
       grab();
@@ -502,11 +504,6 @@ __global__ void __launch_bounds__(kUtThreads, 3)
       bulk_commit();
     }
     ok = ok && wait_mma();
-    // The T'' stores have read the A-tile region: the next item's K may land there.
-    if (ok && tid == 0 && nit < nitems) {
-      bulk_wait_read();
-      issue_k(nit, b ^ 1, XB);
-    }
     // -W rows into staging boxes over K^ (the MMA has read it), then TMA stores.
     if (ok) {
 #pragma unroll
@@ -517,6 +514,12 @@ __global__ void __launch_bounds__(kUtThreads, 3)
 #pragma unroll
         for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(box + swz(t, c)) = pack8h(&w[8 * c]);
       }
+    }
+    // Once the T'' stores (issued with the product, so normally done by now)
+    // have read the A-tile region, the next item's K may land there.
+    if (ok && tid == 0 && nit < nitems) {
+      bulk_wait_read();
+      issue_k(nit, b ^ 1, XB);
     }
     fence_proxy_async();
     publish_next();
