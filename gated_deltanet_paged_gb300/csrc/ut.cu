@@ -104,7 +104,9 @@ __device__ __forceinline__ uint32_t af(int r, int q) { return r * 128 + ((q ^ (r
 // Every thread reads the same row at the same time (broadcast); four partial
 // sums (j mod 4) keep the FMA chains short, and run as two paired fp32 FMAs
 // where both halves of a pair have a term (each half rounds as a scalar FMA).
-__device__ __forceinline__ void solve32(const uint8_t* blk, int c, float (&x)[32]) {
+// hook(t) runs after step t (independent work that fills the steps' latency).
+template <typename Hook>
+__device__ __forceinline__ void solve32(const uint8_t* blk, int c, float (&x)[32], Hook&& hook) {
 #pragma unroll
   for (int t = 0; t < 32; ++t) {
     float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
@@ -124,6 +126,7 @@ __device__ __forceinline__ void solve32(const uint8_t* blk, int c, float (&x)[32
     }
     const float s = (s01.x + s01.y) + (s23.x + s23.y);
     x[t] = t > c ? -s : (t == c ? 1.f : 0.f);
+    hook(t);
   }
 }
 
@@ -296,39 +299,41 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     sh.gam[tid] = __expf(s);
     load_gb(nit, b ^ 1);  // in flight during this item
 
-    // K -> K^ = -diag(gamma) K in fp16, in place (the first MMA has read K), in two
-    // halves done while the two small MMA products run; its sign makes the W
-    // product come out as -W.  Each batch loads its four 16-byte pieces and their
-    // gamma values before any store (a store could alias a later load, so the
-    // compiler would otherwise wait for every load in turn).
-    auto khat_half = [&](int part) {
-      const int lo0 = ga.y, hi0 = ga.z, lo1 = gb.y, hi1 = gb.z;
-      for (int i0 = tid + 1024 * part; i0 < 1024 * (part + 1); i0 += 4 * kUtThreads) {
-        uint4 in[4];
-        float gr[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int i = i0 + k * kUtThreads;
-          in[k] = *reinterpret_cast<const uint4*>(sm + KB + i * 16);
-          gr[k] = -sh.gam[((i >> 9) & 1) * 64 + ((i & 511) >> 3)];
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int i = i0 + k * kUtThreads;
-          const int hh = (i >> 9) & 1, row = (i & 511) >> 3;  // boxes K_a kb0 | K_b kb0 | K_a kb1 | K_b kb1
-          const bool keep = hh ? (row >= lo1 && row < hi1) : (row >= lo0 && row < hi0);
-          uint4 out = make_uint4(0u, 0u, 0u, 0u);
-          if (keep) {
-            const float2 g2 = make_float2(gr[k], gr[k]);
-            out.x = pack_half2(__fmul2_rn(unpack_bf162(in[k].x), g2));
-            out.y = pack_half2(__fmul2_rn(unpack_bf162(in[k].y), g2));
-            out.z = pack_half2(__fmul2_rn(unpack_bf162(in[k].z), g2));
-            out.w = pack_half2(__fmul2_rn(unpack_bf162(in[k].w), g2));
-          }
-          *reinterpret_cast<uint4*>(sm + KB + i * 16) = out;
-        }
+    // K -> K^ = -diag(gamma) K in fp16, in place (the first MMA has read K); its
+    // sign makes the W product come out as -W.  The 16 pieces of 16 bytes of a
+    // thread (piece i = tid + 128 k of the boxes K_a kb0 | K_b kb0 | K_a kb1 |
+    // K_b kb1) are converted between the steps of the 32 x 32 solve, whose
+    // dependent chain leaves the issue slots for them: piece k is loaded one
+    // hook before it is converted and stored.
+    uint4 kin = make_uint4(0u, 0u, 0u, 0u);
+    float kg = 0.f;
+    auto khat_load = [&](int k) {
+      const int i = tid + kUtThreads * k;
+      kin = *reinterpret_cast<const uint4*>(sm + KB + i * 16);
+      kg = -sh.gam[((i >> 9) & 1) * 64 + ((i & 511) >> 3)];
+    };
+    auto khat_store = [&](int k, const uint4 in, float g) {
+      const int i = tid + kUtThreads * k;
+      const int hh = (i >> 9) & 1, row = (i & 511) >> 3;
+      const bool keep = hh ? (row >= gb.y && row < gb.z) : (row >= ga.y && row < ga.z);
+      uint4 out = make_uint4(0u, 0u, 0u, 0u);
+      if (keep) {
+        const float2 g2 = make_float2(g, g);
+        out.x = pack_half2(__fmul2_rn(unpack_bf162(in.x), g2));
+        out.y = pack_half2(__fmul2_rn(unpack_bf162(in.y), g2));
+        out.z = pack_half2(__fmul2_rn(unpack_bf162(in.z), g2));
+        out.w = pack_half2(__fmul2_rn(unpack_bf162(in.w), g2));
       }
-      fence_proxy_async();
+      *reinterpret_cast<uint4*>(sm + KB + i * 16) = out;
+    };
+    // after odd solve steps t: piece k = t / 2 is stored, piece k + 1 loaded
+    auto khat_hook = [&](int t) {
+      if ((t & 1) == 0) return;
+      const int k = t >> 1;
+      const uint4 in = kin;
+      const float g = kg;
+      if (k + 1 < 16) khat_load(k + 1);
+      khat_store(k, in, g);
     };
 
     // ---- [K_a; K_b] [K_a; K_b]^T ----
@@ -418,7 +423,10 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     // ---- T_d: thread (chunk, block bk, column c) solves column c of block bk ----
     const int bk = warp & 1;
     float x[32];
-    if (ok) solve32(sm + XB + half * 8192 + bk * 32 * 128, lane, x);
+    if (ok) {
+      khat_load(0);
+      solve32(sm + XB + half * 8192 + bk * 32 * 128, lane, x, khat_hook);
+    }
     __syncwarp();  // every lane has read this warp's block: the space becomes its T_d columns
     // T_d is kept by columns (tile row j = column j of T_d, 64 rows t in 128
     // bytes), so each thread writes its solved column with four 16-byte stores.
@@ -435,13 +443,12 @@ __global__ void __launch_bounds__(kUtThreads, 3)
     __syncthreads();
 
     // ---- N21 = -T22 A21 = T22 (-A21): [T_d,a; T_d,b] (K = 32..63; by columns, so
-    //      M-major) x [-A21_a | -A21_b]; the first half of K^ while it runs ----
+    //      M-major) x [-A21_a | -A21_b] ----
     if (ok && tid == 0) {
       tc_fence_after();
       tc_mma2(tmem, dMN(XB + 32 * 128, 8192), 128, dMN(XB + 16384, 4096), 128, id_mnAB, 0);
       tc_commit(&sh.bar_mma);
     }
-    if (ok) khat_half(0);
     ok = ok && wait_mma();
     if (ok && bk == 1) {  // rows 32-63 of each chunk -> rows 32 h + i of the N21 stack
       float d[32];
@@ -457,13 +464,12 @@ __global__ void __launch_bounds__(kUtThreads, 3)
 
     // ---- T21^T = T11^T N21^T: [T_d,a by columns; T_d,b by columns] (K = rows
     //      0..31) x [N21_a; N21_b]^T (N = 64): lane 64 h + j, column 32 h + i holds
-    //      T21[i][j] of chunk h; the second half of K^ while it runs ----
+    //      T21[i][j] of chunk h ----
     if (ok && tid == 0) {
       tc_fence_after();
       tc_mma2(tmem, dK(XB), 2, dK(XB + 16384), 2, id_t21, 0);
       tc_commit(&sh.bar_mma);
     }
-    if (ok) khat_half(1);
     ok = ok && wait_mma();
 
     // ---- T'' = T diag(beta) by columns (tile row j = column j) into T''_a | 0 |
