@@ -5,6 +5,7 @@
 // status plumbing of the C ABI.
 #pragma once
 
+#include <atomic>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -487,6 +488,25 @@ int encode_tiles_map_f16(CUtensorMap* map, const void* base, int64_t rows, int64
 int encode_tokens_map_32(CUtensorMap* map, const void* base, int64_t T, int64_t H, int64_t D);  // 64B swizzle
 
 inline int launch_status() { return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+// cudaFuncSetAttribute once per device (the setting lasts for the process):
+// `done` is the call site's mask of devices already set.
+template <typename... Params>
+inline int func_attr_once(void (*kernel)(Params...), cudaFuncAttribute attr, int value, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GDN_ERR_CUDA;
+  }
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return GDN_OK;
+  if (cudaFuncSetAttribute(kernel, attr, value) != cudaSuccess) {
+    cudaGetLastError();
+    return GDN_ERR_CUDA;
+  }
+  if (bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return GDN_OK;
+}
 
 // Launch as a programmatic dependent of the previous kernel on the stream (the
 // kernel calls pdl_wait before it reads anything that kernel may write).

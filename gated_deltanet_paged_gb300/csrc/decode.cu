@@ -376,11 +376,10 @@ extern "C" int gdn_gated_delta_rule_decode_paged_ex(const gdn_bf16* q, const gdn
   cfg.stream = st;
   if (state_dtype == GDN_STATE_BF16) {
     // five 32 KB states per SM: ask for the largest shared-memory carveout
-    if (cudaFuncSetAttribute(decode_bf16_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared) != cudaSuccess) {
-      cudaGetLastError();
-      return GDN_ERR_CUDA;
-    }
+    static std::atomic<uint64_t> carveout_set{0};
+    const int rc2 = gdn_host::func_attr_once(decode_bf16_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             cudaSharedmemCarveoutMaxShared, carveout_set);
+    if (rc2 != GDN_OK) return rc2;
     cfg.gridDim = dim3(batch * H);
     cfg.blockDim = dim3(kBf16Threads);
     cudaLaunchKernelEx(&cfg, decode_bf16_kernel, a);

@@ -1003,15 +1003,15 @@ int launch(PrefillArgs& a, const void* q, const void* k, const void* v, void* wo
   const int64_t ns = num_chunk_slots(a.T, a.num_seqs);
   if (!workspace || workspace_bytes < gdn::workspace_bytes(a.T, a.num_seqs, a.H) || !gdn_host::aligned16(workspace))
     return GDN_ERR_INVALID_ARGUMENT;
-  int rc = gdn_host::check_device(nullptr);
+  int num_sms = 0;
+  int rc = gdn_host::check_device(&num_sms);
   if (rc != GDN_OK) return rc;
   a.num_slots = static_cast<int32_t>(ns);
   a.slot_geo = static_cast<int4*>(workspace);
   a.item_counter = reinterpret_cast<int32_t*>(a.slot_geo + ns);
   a.tinv = reinterpret_cast<__half*>(static_cast<uint8_t*>(workspace) + workspace_map_bytes(ns));
   a.wneg = a.tinv + ns * a.H * (kTinvBytes / 2);
-  rc = host::launch_chunk_inverse(a, k, stream);
-  if (rc != GDN_OK) return rc;
+  // (the maps of K, T'' and -W serve both kernels)
   CUtensorMap mq, mk, mv, mt, mo, mw;
   if (gdn_host::encode_tokens_map(&mq, q, a.T, a.H, kDimK) != GDN_OK ||
       gdn_host::encode_tokens_map(&mk, k, a.T, a.H, kDimK) != GDN_OK ||
@@ -1020,12 +1020,14 @@ int launch(PrefillArgs& a, const void* q, const void* k, const void* v, void* wo
       gdn_host::encode_tiles_map_f16(&mt, a.tinv, ns * a.H * 64, 64) != GDN_OK ||
       gdn_host::encode_tiles_map_f16(&mw, a.wneg, ns * a.H * 64, 128) != GDN_OK)
     return GDN_ERR_CUDA;
+  rc = host::launch_chunk_inverse(a, mk, mt, mw, num_sms, stream);
+  if (rc != GDN_OK) return rc;
+  static std::atomic<uint64_t> smem_set[4];
+  const int variant = (a.err_word ? 2 : 0) + (a.state_bf16 ? 1 : 0);
   auto kernel = a.err_word ? (a.state_bf16 ? prefill_kernel<true, true> : prefill_kernel<true, false>)
                            : (a.state_bf16 ? prefill_kernel<false, true> : prefill_kernel<false, false>);
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess) {
-    cudaGetLastError();
-    return GDN_ERR_CUDA;
-  }
+  rc = gdn_host::func_attr_once(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES, smem_set[variant]);
+  if (rc != GDN_OK) return rc;
   const long long grid = static_cast<long long>(a.num_seqs) * a.H;
   return gdn_host::launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), SMEM_BYTES, stream, mq, mk,
                               mv, mt, mo, mw, a);

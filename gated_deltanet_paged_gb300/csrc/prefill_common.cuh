@@ -105,8 +105,11 @@ __device__ inline bool seq_extent(const PrefillArgs& a, int b, int& cu_b, int& L
 __device__ inline int chunk_count(int P, int L) { return (P + L + 63) / 64 - P / 64; }
 
 namespace host {
-// Enqueue the slot map and the chunk-local inverse kernels (ut.cu).
-int launch_chunk_inverse(const PrefillArgs& a, const void* k, cudaStream_t stream);
+// Enqueue the slot map and the chunk-local inverse kernels (ut.cu): mk is the
+// tensor map of K, mt and mw those of the T'' and -W tiles (shared with the
+// state chain), num_sms the device's SM count.
+int launch_chunk_inverse(const PrefillArgs& a, const CUtensorMap& mk, const CUtensorMap& mt, const CUtensorMap& mw,
+                         int num_sms, cudaStream_t stream);
 }  // namespace host
 
 }  // namespace gdn

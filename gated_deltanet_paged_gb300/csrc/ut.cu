@@ -557,26 +557,16 @@ __global__ void __launch_bounds__(kUtThreads, 3)
 namespace gdn {
 namespace host {
 
-int launch_chunk_inverse(const PrefillArgs& a, const void* k, cudaStream_t stream) {
+int launch_chunk_inverse(const PrefillArgs& a, const CUtensorMap& mk, const CUtensorMap& mt, const CUtensorMap& mw,
+                         int num_sms, cudaStream_t stream) {
   if (a.num_seqs == 0 || a.num_slots == 0) return GDN_OK;
   int rc = gdn_host::launch_pdl(slot_map_kernel, dim3((a.num_slots + 255) / 256), dim3(256), 0, stream, a);
   if (rc != GDN_OK) return rc;
-  CUtensorMap mk, mt, mw;
-  const int64_t rows = static_cast<int64_t>(a.num_slots) * a.H * 64;
-  if (gdn_host::encode_tokens_map(&mk, k, a.T, a.H, kDimK) != GDN_OK ||
-      gdn_host::encode_tiles_map_f16(&mt, a.tinv, rows, 64) != GDN_OK ||
-      gdn_host::encode_tiles_map_f16(&mw, a.wneg, rows, 128) != GDN_OK)
-    return GDN_ERR_CUDA;
-  if (cudaFuncSetAttribute(ut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, UT_SMEM) != cudaSuccess) {
-    cudaGetLastError();
-    return GDN_ERR_CUDA;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  rc = gdn_host::func_attr_once(ut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, UT_SMEM, smem_set);
+  if (rc != GDN_OK) return rc;
   // Persistent CTAs: three per SM (the shared-memory and register budget), each
   // taking work items in strides of the grid.
-  int dev = 0, num_sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return GDN_ERR_CUDA;
   const long long items = static_cast<long long>((a.num_slots + 1) / 2) * a.H;
   const unsigned grid = static_cast<unsigned>(items < 3LL * num_sms ? items : 3LL * num_sms);
   return gdn_host::launch_pdl(ut_kernel, dim3(grid), dim3(kUtThreads), UT_SMEM, stream, mk, mt, mw, a);
