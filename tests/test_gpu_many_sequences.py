@@ -21,17 +21,15 @@ def _pools(pool, pool_dtype):
     return pool.cuda(), pool.numpy().copy()
 
 
-@pytest.mark.parametrize("use_slots", [False, True])
-def test_two_thousand_short_sequences(use_slots):
-    S, H, ps = 2000, 2, 128
-    rng = np.random.default_rng(71)
+def _short_sequences_case(S, H, ps, seed, use_slots):
+    rng = np.random.default_rng(seed)
     lens = rng.integers(0, 81, S)
     lens[rng.random(S) < 0.1] = 0
     prefixes = rng.integers(0, 301, S)
     edge = rng.random(S) < 0.1
     prefixes[edge] = ps * rng.integers(0, 3, int(edge.sum()))  # prefixes that end a page (or are empty)
     prefixes[(lens + prefixes) == 0] = 1
-    gen = torch.Generator().manual_seed(72)
+    gen = torch.Generator().manual_seed(seed + 1)
     ctx = (lens + prefixes).tolist()
     npages = sum(-(-c // ps) for c in ctx)
     ids = torch.randperm(npages + 3, generator=gen)
@@ -45,6 +43,17 @@ def test_two_thousand_short_sequences(use_slots):
     prefill_paged_both(workloads.PrefillCall(q, k, v, g, b, cu, ip, pi, lpl, ps), pool.cuda(), pool.numpy().copy(),
                        errs, use_slots=use_slots)
     print("%d sequences, %d tokens: %r" % (S, int(lens.sum()), errs))
+
+
+@pytest.mark.parametrize("use_slots", [False, True])
+def test_two_thousand_short_sequences(use_slots):
+    _short_sequences_case(2000, 2, 128, 71, use_slots)
+
+
+def test_more_than_4096_sequences():
+    """4,500 sequences: the state chain then takes sequence b = CTA / H in batch
+    order (below 4,096 sequences it orders them by length first)."""
+    _short_sequences_case(4500, 1, 64, 81, False)
 
 
 @pytest.mark.parametrize("pool_dtype", ["float32", "bfloat16"])
